@@ -1,0 +1,436 @@
+#!/usr/bin/env python
+"""Benchmark: paged decode attention KV GB/s (% of GB300 HBM peak) and decode steps/s.
+
+A *step* is one decode step of the 16-layer engine's attention hot path: for
+every layer, the fused RoPE + page-slot append of each sequence's new token,
+then paged GQA decode attention over the sequence's pages (split kernel + LSE
+merge).  Default workload ``b256``: batch 256, every sequence at 2,048 tokens
+(128 pages per sequence and layer), 32 query / 8 KV heads, head_dim 64, BF16 KV
+pool of 524,288 pages (16 GiB).  Other workloads: ``--config b64`` (log-normal
+lengths, median 300) and ``--config b8`` (uniform lengths).
+
+The timed region replays CUDA graphs of whole steps; the inputs (17 GB of KV per
+b256 step) are far larger than the 129 MB L2, so no flush is needed.  Each
+attention launch inside the graphs is bracketed by external timing events, which
+give the dominant kernel's average duration for the roofline.
+
+``--impl reference`` times the FP64 CPU oracle on a bounded sample of the same
+workload on the host cores (the reference arm; it runs none of the CUDA path).
+
+Multi-GPU (``torchrun --nproc-per-node N``): independent replicas, one per GPU,
+each with its own batch (weak scaling); the max elapsed time over ranks is used.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attention KV GB/s (% of GB300 HBM peak) and decode steps/s"
+CONFIG_TEXT = {
+    "b256": "long-context batch 256: every sequence 2048 tokens (128 pages), 16 layers, 32 Q / 8 KV heads, "
+            "head_dim 64, BF16 pool of 524288 pages (16 GiB), random page permutation",
+    "b64": "ragged batch 64: log-normal lengths (median 300, sigma 1, clipped to [1, 2048], boundary lengths "
+           "1/16/17/32/33/2048 included), 16 layers, 1% of keys x8, 4096 pages per layer",
+    "b8": "batch 8: lengths uniform in [1, 2048], 16 layers, 4096 pages of 32 KiB per layer",
+}
+VARIANTS = {"default": 0, "simt": 1, "mma": 2}
+L2_BYTES = 129 * 10**6
+
+
+# --------------------------------------------------------------------------- distributed helpers
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def reduce_max(value: float, world: int, device=None) -> float:
+    """Max of a per-rank float over all ranks (identity for one rank)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_seed(base_seed: int, rank: int) -> int:
+    """Each replica draws its own batch (weak scaling): seed offset by rank."""
+    return base_seed + 1000 * rank
+
+
+# --------------------------------------------------------------------------- peaks, clocks, profiles
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_id}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.6)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self, t0: float, t1: float):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, power, reasons = [], None, [], set()
+        for ts, line in self.lines:
+            if not (t0 <= ts <= t1 + 0.15):
+                continue
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+                power.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, v in zip(self.NAMES, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power) if power else None}
+
+
+def kernel_source_digest() -> str:
+    with open(os.path.join(ROOT, "paged_kv_decode_12_gb300", "csrc", "pkv_decode.cu"), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def measured_traffic(config: str, variant_name: str, pages_per_chunk: int):
+    """DRAM bytes per attention launch from a committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "decode_split_traffic.json")
+    try:
+        with open(path) as f:
+            entries = json.load(f)
+    except Exception:
+        return None
+    digest = kernel_source_digest()
+    for e in entries:
+        if (e.get("config") == config and e.get("variant") == variant_name and
+                e.get("pages_per_chunk") == pages_per_chunk and e.get("kernel_source_sha") == digest):
+            return e.get("dram_bytes_per_launch")
+    return None
+
+
+# --------------------------------------------------------------------------- CPU oracle sample
+
+def oracle_samples(w, n_seqs: int, seed: int):
+    """Host-side synthetic inputs for ``n_seqs`` sequences of one layer of workload ``w``
+    (same length mix), each in its own small paged pool."""
+    from paged_kv_decode_12_gb300 import workloads as wl
+
+    rng = np.random.default_rng(seed)
+    idx = rng.choice(w.batch, size=min(n_seqs, w.batch), replace=False)
+    out = []
+    for b in idx:
+        L = int(w.seq_lens[b])
+        npg = -(-L // wl.PAGE_SIZE)
+        pool = wl.bf16_normal_host(rng, (npg * 2 * wl.NUM_KV_HEADS * wl.PAGE_SIZE * wl.HEAD_DIM,))
+        bt = wl.permutation_block_tables(rng, [L], npg, w.max_blocks)
+        out.append(dict(L=L, npg=npg, pool=pool, bt=bt,
+                        q=wl.bf16_normal_host(rng, (1, wl.NUM_Q_HEADS, wl.HEAD_DIM)),
+                        k_new=wl.bf16_normal_host(rng, (1, wl.NUM_KV_HEADS, wl.HEAD_DIM)),
+                        v_new=wl.bf16_normal_host(rng, (1, wl.NUM_KV_HEADS, wl.HEAD_DIM))))
+    return out
+
+
+def oracle_run_sample(sample) -> int:
+    """One oracle pass (append + attention, all 32 heads) over each sampled sequence;
+    returns the KV tokens attended."""
+    import oracle
+    from paged_kv_decode_12_gb300 import workloads as wl
+
+    tokens = 0
+    for s in sample:
+        g = oracle.geom(s["npg"])
+        q = s["q"].copy()
+        oracle.append(s["pool"], g, s["bt"], [s["L"] - 1], s["k_new"], s["v_new"], q)
+        oracle.decode(s["pool"], g, s["bt"], [s["L"]], q, 1.0 / math.sqrt(wl.HEAD_DIM))
+        tokens += s["L"]
+    return tokens
+
+
+def cpu_baseline(w, seconds: float, seed: int) -> dict:
+    from paged_kv_decode_12_gb300 import workloads as wl
+
+    per_token = wl.kv_bytes_per_token(1)
+    pool = oracle_samples(w, 64, seed)
+    tokens, seqs = 0, 0
+    t0 = time.perf_counter()
+    for s in pool:
+        tokens += oracle_run_sample([s])
+        seqs += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": tokens * per_token / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{seqs} sequences of one layer ({tokens} KV tokens): append + attention for all 32 "
+                      f"query heads, FP64, single thread, {dt:.1f} s"}
+
+
+# --------------------------------------------------------------------------- arms
+
+def config_block(w, args, variant_name: str, graph: bool) -> dict:
+    kv = w.kv_bytes_per_step()
+    return {"workload": f"{args.config}: {CONFIG_TEXT[args.config]}", "batch": w.batch, "layers": w.layers,
+            "seq_len_max": int(w.seq_lens.max()), "seq_len_mean": float(w.seq_lens.mean()),
+            "pages_per_chunk": args.pages_per_chunk, "kernel_variant": variant_name, "cuda_graph": graph,
+            "kv_bytes_per_step": kv,
+            "l2": f"inputs larger than L2 ({kv / 1e9:.2f} GB of KV per step vs {L2_BYTES / 1e6:.0f} MB L2), "
+                  "no flush", "seed": args.seed}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    from paged_kv_decode_12_gb300 import workloads as wl
+
+    w = wl.make_workload(args.config, args.seed)
+    if args.layers:
+        w.layers = args.layers
+    per_token = wl.kv_bytes_per_token(1)
+    sample = oracle_samples(w, args.ref_seqs, args.seed)
+    for _ in range(args.warmup):
+        oracle_run_sample(sample)
+    times = []
+    tokens = 0
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        tokens = oracle_run_sample(sample)
+        times.append(time.perf_counter() - t0)
+    dt = sum(times)
+    value = tokens * per_token * args.steps / dt / 1e9
+    desc = (f"{len(sample)} sequences of one layer per step ({tokens} KV tokens): append + attention for all "
+            f"32 query heads, FP64 C oracle, single thread")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_block(w, args, "oracle", False),
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_pkv(args):
+    import torch
+
+    from paged_kv_decode_12_gb300 import harness, pkv
+
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the CUDA path has no CPU fallback)")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=device)
+
+    variant_name = args.variant
+    dw = harness.setup(args.config, replica_seed(args.seed, rank), args.pages_per_chunk, VARIANTS[variant_name],
+                       layers=args.layers)
+    w = dw.w
+    harness.warm(dw, 2)
+    dw.reset_q()
+    ext = harness.external_events_supported()
+    per_graph = max(1, min(args.steps, args.steps_per_graph))
+    warm_cap = harness.capture_steps(dw, max(1, min(args.warmup, per_graph)))
+    timed = []
+    left = args.steps
+    while left > 0:
+        n = min(per_graph, left)
+        timed.append(harness.capture_steps(dw, n, time_attention=ext))
+        left -= n
+    torch.cuda.synchronize()
+
+    # warm-up: W steps
+    done = 0
+    while done < args.warmup:
+        warm_cap.graph.replay()
+        done += warm_cap.steps
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+
+    uuid = str(getattr(torch.cuda.get_device_properties(device), "uuid", "") or "")
+    sampler = ClockSampler(uuid if uuid.startswith("GPU-") else (f"GPU-{uuid}" if uuid else str(local)))
+    sampler.start()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    t0 = time.time()
+    start.record()
+    for cap in timed:
+        cap.graph.replay()
+    end.record()
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop(t0, t1)
+    elapsed_ms = reduce_max(start.elapsed_time(end), world, device)
+
+    st, flag = dw.eng.check_errors()
+    if st != pkv.PKV_OK:
+        raise SystemExit(f"device error flag set during the timed region: {flag:#x}")
+
+    # dominant kernel: the attention launches (split + merge), timed inside the graphs
+    split_ms = [s.elapsed_time(e) for cap in timed for (s, e) in cap.split_events]
+    kv_step = w.kv_bytes_per_step()
+    kv_launch = kv_step // w.layers
+    peak, peak_src = hbm_peak()
+    steps_per_s = args.steps / (elapsed_ms / 1e3)
+    value = kv_step * steps_per_s * world / 1e9
+    roofline = None
+    if split_ms:
+        avg = sum(split_ms) / len(split_ms)
+        achieved = kv_launch / (avg / 1e3) / 1e9
+        roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                    "traffic": measured_traffic(args.config, variant_name, args.pages_per_chunk),
+                    "kernel": f"paged decode attention launch (split + merge), variant {variant_name}",
+                    "algorithmic_bytes_per_launch": kv_launch, "avg_launch_us": avg * 1e3,
+                    "launches_timed": len(split_ms), "peak_source": f"{peak_src} hbm_gbs (burst copy)"}
+
+    # end to end through the public API with pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = measure_e2e(dw, args, world, device)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, args.cpu_seconds, args.seed)
+
+    line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": config_block(w, args, variant_name, True),
+            "hbm_frac_of_peak": value / world / peak, "steps_per_s": steps_per_s,
+            "tokens_per_s": w.batch * steps_per_s * world,
+            "attended_kv_tokens_per_s": float(w.seq_lens.sum()) * w.layers * steps_per_s * world,
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": harness.kernels_per_step(dw) * args.steps, "clocks": clocks}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    dw.eng.close()
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def measure_e2e(dw, args, world, device):
+    """Same metric through DecodeEngine.run_host: every step copies q, k_new, v_new,
+    positions and lengths from pinned host memory and the output back, on the stream."""
+    import torch
+
+    from paged_kv_decode_12_gb300 import harness
+
+    host_in = harness.host_pinned_inputs(dw)
+    dev_in = {"q": dw.q, "k_new": dw.k_new, "v_new": dw.v_new, "pos": dw.pos, "seq_lens": dw.seq_lens}
+    out_host = torch.empty(dw.out.shape, dtype=dw.out.dtype).pin_memory()
+    n = max(1, min(args.steps, args.e2e_steps))
+    for _ in range(2):
+        dw.eng.run_host(host_in, dev_in, dw.out, out_host)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(n):
+            dw.eng.run_host(host_in, dev_in, dw.out, out_host)
+    g.replay()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    g.replay()
+    end.record()
+    torch.cuda.synchronize()
+    ms = reduce_max(start.elapsed_time(end), world, device)
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = out_host.numel() * out_host.element_size()
+    return {"value": dw.w.kv_bytes_per_step() * n * world / (ms / 1e3) / 1e9, "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n, "ms_per_step": ms / n,
+            "path": "DecodeEngine.run_host (pinned host in/out, copies on the kernels' stream, CUDA graph)"}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["pkv", "reference"], default="pkv")
+    ap.add_argument("--config", choices=sorted(CONFIG_TEXT), default="b256")
+    ap.add_argument("--pages-per-chunk", type=int, default=16)
+    ap.add_argument("--variant", choices=sorted(VARIANTS), default="default")
+    ap.add_argument("--seed", type=int, default=12)
+    ap.add_argument("--layers", type=int, default=None, help="override the layer count (small profiling runs)")
+    ap.add_argument("--steps-per-graph", type=int, default=25)
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-seqs", type=int, default=2, help="sequences per reference-arm step")
+    args = ap.parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_pkv(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

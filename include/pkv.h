@@ -1,0 +1,223 @@
+/*
+ * pkv.h -- C ABI of libpkv: paged-KV decode attention for GB300 (sm_103a).
+ *
+ * The library implements the decode-step hot path of a small Llama-3.2-1B
+ * serving engine as described in the samir-vllm README summary
+ * ("从零用 C++ 和 CUDA 实现 Llama 3.2 1B 推理引擎:6 小时视频与 85 页手写笔记",
+ * section "目前已完成的功能", features done so far):
+ *   - a shared BF16 KV page pool; each physical page holds K and V of 16
+ *     tokens; every (sequence, layer) reaches its pages through a block table;
+ *     the number of requests does not grow the pool;
+ *   - decode appends one new token per sequence at its absolute RoPE position;
+ *   - paged decode attention: each query head streams its sequence's cached
+ *     pages with an FP32 online softmax, without gathering a contiguous prefix
+ *     and without storing attention scores;
+ * plus, from the same page's section "当前范围" (current scope), pages that are
+ * allocated lazily and returned when a request finishes.
+ *
+ * Geometry supported by the kernels (Llama-3.2-1B attention): 32 query heads,
+ * 8 KV heads (grouped-query attention, group 4, query head h reads KV head
+ * h / 4), head_dim 64, 16 tokens per page.
+ *
+ * Memory layout (a reading: the pages fix no in-page layout):
+ *   pool slab   : num_pages pages, page p at  slab + p * PKV_PAGE_BYTES;
+ *   one page    : [2: K then V][8 KV heads][16 slots][64 dims] BF16 (32 KiB);
+ *                 the K tile of (page, head) is one contiguous 2 KiB run, its
+ *                 V tile another 2 KiB run 16 KiB further on;
+ *   block table : int32 [B][max_blocks] per layer; entry j of row b is the
+ *                 physical page holding tokens 16j .. 16j+15 of sequence b;
+ *                 unused entries are -1;
+ *   q, out      : BF16 [B][32][64];  k_new, v_new : BF16 [B][8][64];
+ *   seq_lens    : int32 [B], the length AFTER this step's append (the new
+ *                 token sits at position seq_len - 1 and attends to itself);
+ *   pos         : int32 [B], the absolute position of the appended token.
+ * BF16 values travel as uint16_t bit patterns.
+ *
+ * Ownership: the caller owns every device buffer (slab, q, k_new, v_new,
+ * tables, lengths, workspace, out, error flag); the library owns only the
+ * host-side pkv_pool object (free list and bookkeeping) and never frees the
+ * slab.  Kernel launches are asynchronous on the caller's stream
+ * (cudaStream_t passed as void*, NULL = legacy default stream).
+ *
+ * Errors: every entry point returns a status code synchronously after host
+ * checks (PKV_OK = 0, negative on error; nothing is launched on error).
+ * Faults the host cannot see (a block-table entry outside the pool, a length
+ * beyond the table) are caught by the kernels' own bounds checks: the unit is
+ * skipped, its outputs are written as zeros, and a bit is OR-ed into the
+ * caller's int32 device error flag; kernels never trap.  Read it with
+ * pkv_check_device_error().
+ *
+ * Thread safety: a pkv_pool is not thread-safe; calls on distinct pools are.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---------------------------------------------------------------- constants */
+#define PKV_PAGE_SIZE 16
+#define PKV_NUM_Q_HEADS 32
+#define PKV_NUM_KV_HEADS 8
+#define PKV_HEAD_DIM 64
+#define PKV_PAGE_BYTES (2 * PKV_NUM_KV_HEADS * PKV_PAGE_SIZE * PKV_HEAD_DIM * 2) /* 32768 */
+
+/* status codes */
+#define PKV_OK 0
+#define PKV_ERR_INVALID_ARG (-1)         /* null pointer, size or shape out of range */
+#define PKV_ERR_OUT_OF_PAGES (-2)        /* allocation larger than the free list (nothing taken) */
+#define PKV_ERR_DOUBLE_FREE (-3)         /* freeing a page that is not allocated */
+#define PKV_ERR_CUDA (-4)                /* a CUDA runtime / launch error */
+#define PKV_ERR_DEVICE_BOUNDS (-5)       /* the device error flag was set */
+#define PKV_ERR_BUDGET_EXCEEDS_POOL (-6) /* a request larger than the whole pool */
+#define PKV_ERR_UNSUPPORTED (-7)         /* geometry other than 32/8/64/16 */
+#define PKV_ERR_WORKSPACE_TOO_SMALL (-8)
+
+/* device error-flag bits (OR-ed by kernels into the caller's int32 flag) */
+#define PKV_DEVERR_PAGE_RANGE 0x1  /* a block-table entry outside [0, num_pages) */
+#define PKV_DEVERR_LENGTH 0x2      /* seq_len < 1, seq_len > max_blocks*16, or pos out of range */
+#define PKV_DEVERR_TIMEOUT 0x4     /* a bounded wait on a copy barrier gave up */
+
+/* decode kernel variants (pkv_decode_attention_variant) */
+#define PKV_DECODE_DEFAULT 0 /* the fastest measured variant */
+#define PKV_DECODE_SIMT 1    /* CUDA-core FP32 dot products and warp-shuffle reductions */
+#define PKV_DECODE_MMA 2     /* warp-level BF16 tensor-core MMA for the 16-token page tiles */
+
+typedef struct pkv_pool pkv_pool; /* opaque, host side */
+
+/* ------------------------------------------------------------------- pool */
+
+/* Create the host-side manager of a caller-owned device slab.
+ * Source: samir-vllm README summary, "目前已完成的功能" (shared BF16 KV page
+ * pool of 16-token pages) and "从零构建大模型推理引擎" section 5.1 (preallocate
+ * one large buffer and manage it by offsets).
+ *   dev_slab     device pointer, at least 16-byte aligned (checked; cudaMalloc
+ *                and torch give 256), never freed by the library
+ *   slab_bytes   size; num_pages = slab_bytes / PKV_PAGE_BYTES (>= 1)
+ *   page_size, num_kv_heads, head_dim  must be 16, 8, 64 (else PKV_ERR_UNSUPPORTED)
+ *   seed         seeds the shuffle of the free list, so pages handed out are
+ *                scattered through the slab reproducibly
+ *   out          receives the pool object
+ * Host only: no CUDA call is made. */
+int pkv_pool_create(void *dev_slab, size_t slab_bytes, int page_size, int num_kv_heads, int head_dim,
+                    uint64_t seed, pkv_pool **out);
+
+/* Destroy the host object (never touches the slab).  NULL is accepted. */
+int pkv_pool_destroy(pkv_pool *pool);
+
+/* Take n pages, all or nothing (samir-vllm README summary, "当前范围": pages are
+ * allocated lazily, on demand).  ids_out receives n int32 page ids.
+ * PKV_ERR_OUT_OF_PAGES if fewer than n are free (nothing is taken). */
+int pkv_pool_alloc(pkv_pool *pool, int n, int32_t *ids_out);
+
+/* Return n pages (same section: pages come back when a request finishes or
+ * stops early).  All ids are checked first: an id outside the pool is
+ * PKV_ERR_INVALID_ARG, an id not currently allocated (or repeated in the call)
+ * is PKV_ERR_DOUBLE_FREE; on error nothing is freed. */
+int pkv_pool_free(pkv_pool *pool, int n, const int32_t *ids);
+
+/* Report the slab's K base, V base (= K base + 16 KiB), page stride in bytes,
+ * page count and free-page count.  Any output pointer may be NULL. */
+int pkv_pool_info(const pkv_pool *pool, void **k_base, void **v_base, int64_t *page_stride_bytes,
+                  int *num_pages, int *num_free);
+
+/* Build block tables for `layers` layers and B sequences on the host (samir-
+ * vllm README summary, "目前已完成的功能": block tables per sequence and layer).
+ * For every (layer l, sequence b) it takes ceil(seq_lens[b]/16) pages from the
+ * free list and writes them to bt_host[l][b][0..], padding with -1 up to
+ * max_blocks.  All or nothing: PKV_ERR_OUT_OF_PAGES if the total does not fit,
+ * PKV_ERR_INVALID_ARG if a length is negative or needs more than max_blocks
+ * pages.  A length of 0 takes no pages.  Host only. */
+int pkv_block_tables_build(pkv_pool *pool, int layers, int B, const int32_t *seq_lens, int max_blocks,
+                           int32_t *bt_host);
+
+/* ------------------------------------------------------------------- RoPE */
+
+/* Fill a device table of rotary-embedding factors: dev_cos_sin[p][i] =
+ * {cos(p * theta^(-2i/(2*half_dim))), sin(...)} as FP32, computed on the host
+ * in FP64 and rounded once ("从零构建大模型推理引擎" section 4.1: rotary embedding
+ * injects the absolute position; the samir-vllm page's RoPE item).  The pairing
+ * is rotate-half: dimension i turns with dimension i + half_dim.
+ *   theta      base (500000 for Llama 3.2); half_dim must be 32
+ *   max_pos    rows; positions 0 .. max_pos-1 (2048 for the engine's context)
+ *   dev_cos_sin device buffer of max_pos * half_dim * 2 floats
+ * Copies synchronously with respect to the host (the stream is synchronised). */
+int pkv_rope_table_init(double theta, int max_pos, int half_dim, float *dev_cos_sin, void *cuda_stream);
+
+/* ----------------------------------------------------------------- append */
+
+/* Fused RoPE + page-slot append for one layer (samir-vllm README summary,
+ * "目前已完成的功能": decode appends one token at its absolute RoPE position).
+ * For every sequence b with p = pos_dev[b]: rotate k_new[b][g] to position p
+ * (FP32 arithmetic on the table's factors, rounded to BF16 to nearest even)
+ * and store it, with v_new[b][g] unrotated, into page bt_dev[b][p/16], slot
+ * p%16, for the 8 KV heads g.  If q is not NULL, the 32 query heads of q[b]
+ * are rotated in place by the same factors.
+ *   bt_dev     this layer's table [B][max_blocks]
+ *   rope_table from pkv_rope_table_init with max_pos rows
+ *   dev_err_flag int32 device flag (may be NULL: errors are then only skipped)
+ * Device checks: pos outside [0, min(max_pos, 16*max_blocks)) or a page id
+ * outside the pool sets the flag and skips that sequence. */
+int pkv_append_rope(const pkv_pool *pool, const uint16_t *k_new, const uint16_t *v_new, uint16_t *q,
+                    const int32_t *bt_dev, int max_blocks, const int32_t *pos_dev, int B,
+                    const float *rope_table, int max_pos, int32_t *dev_err_flag, void *cuda_stream);
+
+/* ---------------------------------------------------------------- decode */
+
+/* Bytes of device workspace pkv_decode_attention needs for B sequences, a
+ * table width of max_blocks and pages_per_chunk pages per work unit. */
+size_t pkv_decode_workspace_bytes(int B, int max_blocks, int pages_per_chunk);
+
+/* Paged decode attention for one layer (samir-vllm README summary, "目前已完成
+ * 的功能": each query head streams its sequence's cached pages with an FP32
+ * online softmax and accumulates weighted V, no contiguous gather, no stored
+ * scores; "从零构建大模型推理引擎" section 3.2: scores q.k / sqrt(head_dim), the
+ * maximum subtracted before the exponential).
+ * For each sequence b and query head h (KV head h/4):
+ *   out[b][h] = sum_t softmax_t(scale * q[b][h] . K_t) V_t,  t < seq_lens[b],
+ * K_t, V_t read from page bt_dev[b][t/16], slot t%16.  The result is rounded to
+ * BF16 (nearest even).
+ * Work split: a sequence's pages are cut into chunks of pages_per_chunk pages
+ * (1..128); one CTA handles one (sequence, KV head, chunk) and serves all 4
+ * query heads of the group from a single read of each page; chunk partials
+ * (running max, sum, unnormalised output in FP32) are merged by log-sum-exp.
+ * The chunking depends only on each sequence's own length and pages_per_chunk,
+ * never on B, so a sequence's result is bit-identical alone or in any batch.
+ *   workspace  device buffer of at least pkv_decode_workspace_bytes(...) bytes,
+ *              16-byte aligned; contents need no initialisation
+ *   scale      1/sqrt(64) = 0.125 for the engine
+ * Device checks: seq_len outside [1, 16*max_blocks] or a page id outside the
+ * pool sets the flag; the affected (sequence, head) outputs are zeros. */
+int pkv_decode_attention(const pkv_pool *pool, const uint16_t *q, const int32_t *bt_dev, int max_blocks,
+                         const int32_t *seq_lens_dev, int B, float scale, int pages_per_chunk,
+                         void *workspace, size_t workspace_bytes, uint16_t *out, int32_t *dev_err_flag,
+                         void *cuda_stream);
+
+/* As pkv_decode_attention, with the split kernel chosen explicitly
+ * (PKV_DECODE_DEFAULT, PKV_DECODE_SIMT or PKV_DECODE_MMA). */
+int pkv_decode_attention_variant(const pkv_pool *pool, const uint16_t *q, const int32_t *bt_dev,
+                                 int max_blocks, const int32_t *seq_lens_dev, int B, float scale,
+                                 int pages_per_chunk, void *workspace, size_t workspace_bytes, uint16_t *out,
+                                 int32_t *dev_err_flag, void *cuda_stream, int variant);
+
+/* ------------------------------------------------------------------ misc */
+
+/* Synchronise the stream, read the device error flag into *host_flag (may be
+ * NULL) and return PKV_ERR_DEVICE_BOUNDS if any bit is set, else PKV_OK. */
+int pkv_check_device_error(const int32_t *dev_err_flag, int32_t *host_flag, void *cuda_stream);
+
+/* Human-readable name of a status code (static storage). */
+const char *pkv_status_string(int status);
+
+/* Library version string, e.g. "pkv 0.1 sm_103a". */
+const char *pkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

@@ -1,0 +1,81 @@
+"""Build ``libpkv.so`` in-tree with nvcc for sm_103a (GB300).
+
+Each translation unit is compiled in parallel to an object file, then linked
+into one shared library next to this file.  The CUDA runtime is linked as a
+shared library so that the process uses one runtime instance with PyTorch.
+"""
+from __future__ import annotations
+
+import concurrent.futures
+import os
+import shutil
+import subprocess
+import sys
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+CSRC = os.path.join(HERE, "csrc")
+ROOT = os.path.dirname(HERE)
+INCLUDE = os.path.join(ROOT, "include")
+LIB = os.path.join(HERE, "libpkv.so")
+BUILD_DIR = os.path.join(ROOT, "_build")
+
+SOURCES = ["pkv_host.cpp", "pkv_append.cu", "pkv_decode.cu"]
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def _nvcc() -> str:
+    cand = os.environ.get("NVCC") or shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    return cand
+
+
+def _cuda_lib_dir(nvcc: str) -> str:
+    return os.path.join(os.path.dirname(os.path.dirname(os.path.realpath(nvcc))), "lib64")
+
+
+def _stale(outputs, inputs) -> bool:
+    if not all(os.path.exists(o) for o in outputs):
+        return True
+    newest_in = max(os.path.getmtime(i) for i in inputs)
+    return min(os.path.getmtime(o) for o in outputs) < newest_in
+
+
+def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
+    nvcc = _nvcc()
+    os.makedirs(BUILD_DIR, exist_ok=True)
+    headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh"))]
+    headers.append(os.path.join(INCLUDE, "pkv.h"))
+    srcs = [os.path.join(CSRC, s) for s in SOURCES]
+    objs = [os.path.join(BUILD_DIR, os.path.basename(s) + ".o") for s in srcs]
+    if not force and not _stale([LIB], srcs + headers + [__file__]):
+        return LIB
+    common = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "--expt-relaxed-constexpr"]
+    common += list(extra_flags or [])
+    if verbose:
+        common += ["-Xptxas", "-v"]
+
+    def compile_one(src_obj):
+        src, obj = src_obj
+        cmd = [nvcc] + ARCH + common + ["-c", src, "-o", obj]
+        if verbose:
+            print(" ".join(cmd), file=sys.stderr)
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0 or verbose:
+            sys.stderr.write(r.stdout + r.stderr)
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc failed on {os.path.basename(src)}")
+        return obj
+
+    with concurrent.futures.ThreadPoolExecutor(max_workers=len(srcs)) as ex:
+        list(ex.map(compile_one, zip(srcs, objs)))
+    tmp = LIB + f".tmp{os.getpid()}"
+    link = [nvcc] + ARCH + ["-shared", "-cudart", "shared", "-o", tmp] + objs + [
+        "-Xlinker", "-rpath," + _cuda_lib_dir(nvcc)]
+    if verbose:
+        print(" ".join(link), file=sys.stderr)
+    subprocess.run(link, check=True)
+    os.replace(tmp, LIB)
+    return LIB
+
+
+if __name__ == "__main__":
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))

@@ -1,0 +1,107 @@
+"""Multi-layer decode step over the C ABI: the public entry point a user calls.
+
+``DecodeEngine`` owns the device buffers one decode step needs (the KV page
+slab, per-layer block tables, the RoPE factor table, the attention workspace
+and the device error flag) and runs, for every layer, the two library calls of
+the hot path: ``pkv_append_rope`` (RoPE + page-slot append of the new token,
+query rotated in place) then ``pkv_decode_attention`` (paged GQA attention over
+the sequence's pages).  PyTorch only allocates memory and provides the stream;
+every step of the computation runs in libpkv's kernels.
+
+``run_host`` is the end-to-end form: inputs come from pinned host memory and
+the result goes back to it, with the copies on the same stream as the kernels.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+from . import pkv
+from . import workloads as wl
+
+
+class DecodeEngine:
+    def __init__(self, num_pages: int, layers: int, batch: int, max_blocks: int = wl.MAX_BLOCKS,
+                 pages_per_chunk: int = 16, variant: int = pkv.PKV_DECODE_DEFAULT, max_pos: int = wl.MAX_CONTEXT,
+                 theta: float = wl.ROPE_THETA, pool_seed: int = 0, device: str = "cuda"):
+        self.device = torch.device(device)
+        self.layers, self.batch, self.max_blocks = layers, batch, max_blocks
+        self.pages_per_chunk, self.variant, self.max_pos = pages_per_chunk, variant, max_pos
+        self.scale = 1.0 / math.sqrt(wl.HEAD_DIM)
+        self.slab = torch.empty(num_pages * pkv.PKV_PAGE_BYTES, dtype=torch.uint8, device=self.device)
+        self.pool = pkv.pkv_pool_create(self.slab, self.slab.numel(), seed=pool_seed)
+        self.num_pages = num_pages
+        self.rope = torch.empty(max_pos * (wl.HEAD_DIM // 2) * 2, dtype=torch.float32, device=self.device)
+        pkv.pkv_rope_table_init(theta, max_pos, wl.HEAD_DIM // 2, self.rope)
+        self.err = torch.zeros(1, dtype=torch.int32, device=self.device)
+        self.ws_bytes = pkv.pkv_decode_workspace_bytes(batch, max_blocks, pages_per_chunk)
+        self.workspace = torch.empty(max(self.ws_bytes, 16), dtype=torch.uint8, device=self.device)
+        self.bt = None
+        self.bt_host = None
+
+    # ------------------------------------------------------------------ setup
+    def pool_view(self) -> torch.Tensor:
+        """The slab as BF16 [pages][2 (K, V)][8 KV heads][16 slots][64 dims]."""
+        return self.slab.view(torch.bfloat16).view(self.num_pages, 2, wl.NUM_KV_HEADS, wl.PAGE_SIZE,
+                                                   wl.HEAD_DIM)
+
+    def build_tables(self, seq_lens) -> np.ndarray:
+        """Allocate pages for every (layer, sequence) and upload the block tables."""
+        bt = pkv.pkv_block_tables_build(self.pool, self.layers, seq_lens, self.max_blocks)
+        self.set_tables(bt)
+        return bt
+
+    def set_tables(self, bt_host: np.ndarray) -> None:
+        assert bt_host.shape == (self.layers, self.batch, self.max_blocks)
+        self.bt_host = np.ascontiguousarray(bt_host, dtype=np.int32)
+        self.bt = torch.from_numpy(self.bt_host).to(self.device)
+
+    def close(self) -> None:
+        if self.pool is not None:
+            pkv.pkv_pool_destroy(self.pool)
+            self.pool = None
+
+    def __del__(self):  # pragma: no cover
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # ------------------------------------------------------------------ step
+    def append(self, layer: int, k_new, v_new, q, pos_dev, stream=None) -> None:
+        pkv.pkv_append_rope(self.pool, k_new, v_new, q, self.bt[layer], self.max_blocks, pos_dev, self.batch,
+                            self.rope, self.max_pos, self.err, stream)
+
+    def attention(self, layer: int, q, seq_lens_dev, out, stream=None, variant=None) -> None:
+        pkv.pkv_decode_attention_variant(self.pool, q, self.bt[layer], self.max_blocks, seq_lens_dev, self.batch,
+                                         self.scale, self.pages_per_chunk, self.workspace, self.ws_bytes, out,
+                                         self.err, stream, self.variant if variant is None else variant)
+
+    def step(self, q, k_new, v_new, pos_dev, seq_lens_dev, out, stream=None, layer_hook=None) -> None:
+        """One decode step over all layers.
+
+        q: [layers][B][32][64] bf16 (rotated in place), k_new, v_new: [layers][B][8][64] bf16,
+        pos_dev, seq_lens_dev: [B] int32, out: [layers][B][32][64] bf16.
+        ``layer_hook(layer, phase)`` (optional) is called around each attention launch.
+        """
+        for layer in range(self.layers):
+            self.append(layer, k_new[layer], v_new[layer], q[layer], pos_dev, stream)
+            if layer_hook:
+                layer_hook(layer, "before")
+            self.attention(layer, q[layer], seq_lens_dev, out[layer], stream)
+            if layer_hook:
+                layer_hook(layer, "after")
+
+    def run_host(self, host_in: dict, dev_in: dict, out_dev, out_host, stream=None) -> None:
+        """End-to-end step: copy q, k_new, v_new, pos, seq_lens from pinned host tensors into the
+        device tensors, run the step, copy the output back to pinned host memory."""
+        for k in ("q", "k_new", "v_new", "pos", "seq_lens"):
+            dev_in[k].copy_(host_in[k], non_blocking=True)
+        self.step(dev_in["q"], dev_in["k_new"], dev_in["v_new"], dev_in["pos"], dev_in["seq_lens"], out_dev,
+                  stream)
+        out_host.copy_(out_dev, non_blocking=True)
+
+    def check_errors(self):
+        return pkv.pkv_check_device_error(self.err)

@@ -1,0 +1,179 @@
+"""CPU-only checks of libpkv: the library loads, exports every symbol the public
+header declares, and its host-side logic (page pool allocator, block-table
+builder, argument validation) behaves as documented.  No CUDA work is issued:
+the pool functions are host only, and the launch entry points are only called
+with arguments that fail validation before any CUDA call.
+"""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from paged_kv_decode_12_gb300 import pkv
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pkv.h")
+FAKE_SLAB = 0x7F0000000000  # never dereferenced by host code
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from paged_kv_decode_12_gb300 import _build
+
+    _build.build()
+
+
+def header_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^(?:int|size_t|const char \*)\s*(pkv_\w+)\(", text, flags=re.M)))
+
+
+def test_every_declared_symbol_is_exported():
+    declared = header_functions()
+    assert len(declared) >= 12
+    lib = ctypes.CDLL(pkv.LIB_PATH)
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert sorted(pkv.EXPORTED) == declared
+
+
+def test_version_and_status_strings():
+    assert "sm_103a" in pkv.pkv_version()
+    assert pkv.status_string(pkv.PKV_OK) == "ok"
+    assert "out of pages" in pkv.status_string(pkv.PKV_ERR_OUT_OF_PAGES)
+    assert pkv.status_string(12345) == "unknown status"
+
+
+def make_pool(pages, seed=1):
+    return pkv.pkv_pool_create(FAKE_SLAB, pages * pkv.PKV_PAGE_BYTES, seed=seed)
+
+
+def test_pool_create_validation():
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.pkv_pool_create(FAKE_SLAB + 8, 4 * pkv.PKV_PAGE_BYTES)
+    assert e.value.status == pkv.PKV_ERR_INVALID_ARG
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.pkv_pool_create(FAKE_SLAB, pkv.PKV_PAGE_BYTES - 1)
+    assert e.value.status == pkv.PKV_ERR_INVALID_ARG
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.pkv_pool_create(FAKE_SLAB, 4 * pkv.PKV_PAGE_BYTES, page_size=32)
+    assert e.value.status == pkv.PKV_ERR_UNSUPPORTED
+    with pytest.raises(pkv.PkvError):
+        pkv.pkv_pool_create(None, 4 * pkv.PKV_PAGE_BYTES)
+
+
+def test_pool_info_geometry():
+    p = make_pool(10)
+    info = pkv.pkv_pool_info(p)
+    assert info["num_pages"] == 10 and info["num_free"] == 10
+    assert info["k_base"] == FAKE_SLAB and info["v_base"] == FAKE_SLAB + 16384
+    assert info["page_stride_bytes"] == 32768
+    pkv.pkv_pool_destroy(p)
+
+
+def test_alloc_all_or_nothing_and_free():
+    p = make_pool(10)
+    a = pkv.pkv_pool_alloc(p, 7)
+    assert len(set(a.tolist())) == 7 and a.min() >= 0 and a.max() < 10
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.pkv_pool_alloc(p, 4)
+    assert e.value.status == pkv.PKV_ERR_OUT_OF_PAGES
+    assert pkv.pkv_pool_info(p)["num_free"] == 3          # nothing taken on failure
+    pkv.pkv_pool_free(p, a[:2])
+    assert pkv.pkv_pool_info(p)["num_free"] == 5
+    rest = pkv.pkv_pool_alloc(p, 5)
+    assert set(rest.tolist()) | set(a[2:].tolist()) == set(range(10))
+    pkv.pkv_pool_destroy(p)
+
+
+def test_free_errors_leave_pool_unchanged():
+    p = make_pool(6)
+    a = pkv.pkv_pool_alloc(p, 4)
+    pkv.pkv_pool_free(p, a[:1])
+    with pytest.raises(pkv.PkvError) as e:                 # a[0] already free
+        pkv.pkv_pool_free(p, [a[1], a[0]])
+    assert e.value.status == pkv.PKV_ERR_DOUBLE_FREE
+    with pytest.raises(pkv.PkvError) as e:                 # repeated in one call
+        pkv.pkv_pool_free(p, [a[2], a[2]])
+    assert e.value.status == pkv.PKV_ERR_DOUBLE_FREE
+    with pytest.raises(pkv.PkvError) as e:                 # foreign id
+        pkv.pkv_pool_free(p, [a[3], 6])
+    assert e.value.status == pkv.PKV_ERR_INVALID_ARG
+    assert pkv.pkv_pool_info(p)["num_free"] == 3
+    pkv.pkv_pool_free(p, a[1:])                            # the failed calls freed nothing
+    assert pkv.pkv_pool_info(p)["num_free"] == 6
+    pkv.pkv_pool_destroy(p)
+
+
+def test_block_tables_properties():
+    p = make_pool(400, seed=5)
+    lens = np.array([1, 16, 17, 32, 33, 0, 200], dtype=np.int32)
+    bt = pkv.pkv_block_tables_build(p, 3, lens, 16)
+    need = -(-lens // 16)
+    used = []
+    for layer in range(3):
+        for b, n in enumerate(need):
+            row = bt[layer, b]
+            assert np.all(row[:n] >= 0) and np.all(row[:n] < 400)
+            assert np.all(row[n:] == -1)
+            used.extend(row[:n].tolist())
+    assert len(used) == len(set(used)) == 3 * need.sum()     # no page shared between rows
+    assert pkv.pkv_pool_info(p)["num_free"] == 400 - 3 * need.sum()
+    # pages are scattered through the slab, not handed out in order
+    assert sorted(used) != used
+    pkv.pkv_pool_destroy(p)
+
+
+def test_block_tables_seeded_and_all_or_nothing():
+    lens = np.array([100, 50], dtype=np.int32)
+    a = pkv.pkv_block_tables_build(make_pool(64, seed=9), 2, lens, 8)
+    b = pkv.pkv_block_tables_build(make_pool(64, seed=9), 2, lens, 8)
+    c = pkv.pkv_block_tables_build(make_pool(64, seed=10), 2, lens, 8)
+    assert np.array_equal(a, b) and not np.array_equal(a, c)
+    p = make_pool(20)
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.pkv_block_tables_build(p, 2, lens, 8)          # needs 22 pages
+    assert e.value.status == pkv.PKV_ERR_OUT_OF_PAGES
+    assert pkv.pkv_pool_info(p)["num_free"] == 20
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.pkv_block_tables_build(p, 1, np.array([129], np.int32), 8)   # 9 pages > 8
+    assert e.value.status == pkv.PKV_ERR_INVALID_ARG
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.pkv_block_tables_build(p, 1, np.array([-1], np.int32), 8)
+    assert e.value.status == pkv.PKV_ERR_INVALID_ARG
+
+
+def test_workspace_bytes():
+    # B x 32 heads x chunks x (m, l) floats, 256-aligned, then x 64 floats of o
+    ws = pkv.pkv_decode_workspace_bytes(256, 128, 16)
+    chunks = 8
+    ml = 256 * 32 * chunks * 8
+    assert ws == ((ml + 255) // 256) * 256 + 256 * 32 * chunks * 64 * 4
+    assert pkv.pkv_decode_workspace_bytes(0, 128, 16) == 0
+
+
+def test_launch_entry_points_validate_before_any_cuda_call():
+    p = make_pool(8)
+    dummy = FAKE_SLAB
+    with pytest.raises(pkv.PkvError) as e:     # B = 0
+        pkv.pkv_decode_attention(p, dummy, dummy, 128, dummy, 0, 0.125, 16, dummy, 1 << 20, dummy, None, 0)
+    assert e.value.status == pkv.PKV_ERR_INVALID_ARG
+    with pytest.raises(pkv.PkvError) as e:     # chunk of 0 pages
+        pkv.pkv_decode_attention(p, dummy, dummy, 128, dummy, 4, 0.125, 0, dummy, 1 << 20, dummy, None, 0)
+    assert e.value.status == pkv.PKV_ERR_INVALID_ARG
+    with pytest.raises(pkv.PkvError) as e:     # workspace too small
+        pkv.pkv_decode_attention(p, dummy, dummy, 128, dummy, 4, 0.125, 16, dummy, 64, dummy, None, 0)
+    assert e.value.status == pkv.PKV_ERR_WORKSPACE_TOO_SMALL
+    with pytest.raises(pkv.PkvError) as e:     # unknown variant
+        pkv.pkv_decode_attention_variant(p, dummy, dummy, 128, dummy, 4, 0.125, 16, dummy, 1 << 20, dummy, None,
+                                         0, variant=9)
+    assert e.value.status == pkv.PKV_ERR_INVALID_ARG
+    with pytest.raises(pkv.PkvError) as e:     # misaligned k_new
+        pkv.pkv_append_rope(p, dummy + 2, dummy, None, dummy, 128, dummy, 4, dummy, 2048, None, 0)
+    assert e.value.status == pkv.PKV_ERR_INVALID_ARG
+    with pytest.raises(pkv.PkvError) as e:     # half_dim other than 32
+        pkv.pkv_rope_table_init(500000.0, 2048, 16, dummy, 0)
+    assert e.value.status == pkv.PKV_ERR_INVALID_ARG
+    pkv.pkv_pool_destroy(p)
