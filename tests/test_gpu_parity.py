@@ -191,11 +191,22 @@ def test_batch_invariance(variant):
 
 
 @pytest.mark.parametrize("variant", VARIANTS)
-def test_chunking_agrees_to_fp32_rounding(variant):
+def test_chunking_agrees_to_rounding(variant):
+    """One chunk per sequence vs one page per chunk.  The SIMT policy computes in
+    FP32 throughout, so the two differ by FP32 rounding only (<= 2 BF16 ulps after
+    the final rounding).  The MMA policy rounds each softmax weight p to BF16 (relative
+    error <= 2^-9) relative to a running max that depends on the chunking, so the two
+    outputs may differ by up to 2 * 2^-9 * max_t |v_t| plus the final rounding."""
     c = make_case(8, [2048, 1500, 129], max_blocks=128)
     one_chunk = gpu_run(c, chunk=128, variant=variant)
     per_page = gpu_run(c, chunk=1, variant=variant)
-    assert ulp_distance(one_chunk["out"], per_page["out"]).max() <= 2
+    if variant == pkv.PKV_DECODE_SIMT:
+        assert ulp_distance(one_chunk["out"], per_page["out"]).max() <= 2
+    else:
+        a, b = ph.bf16_to_f64(one_chunk["out"]), ph.bf16_to_f64(per_page["out"])
+        vmax = np.abs(ph.bf16_to_f64(c["V"])).max(axis=(2, 3))            # [B][Hkv]
+        bound = 2 * 2.0**-9 * np.repeat(vmax, HQ // HKV, axis=1)[..., None] + 2.0**-7 * np.abs(a)
+        assert np.all(np.abs(a - b) <= bound)
 
 
 def test_variants_agree():
