@@ -204,6 +204,34 @@ int pkv_decode_attention_variant(const pkv_pool *pool, const uint16_t *q, const 
                                  int pages_per_chunk, void *workspace, size_t workspace_bytes, uint16_t *out,
                                  int32_t *dev_err_flag, void *cuda_stream, int variant);
 
+/* Size of the library's static scratch used by pkv_decode_attention_noalloc. */
+#define PKV_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20) /* 32 MiB */
+
+/* pkv_decode_attention without a workspace argument and without any allocation.
+ * The pages have no counterpart: this entry point exists for callers that cannot
+ * call cudaMalloc -- a plugin inside an engine that owns the whole device-memory
+ * budget and gives its plugins no workspace, a latency-critical loop that must
+ * not call cudaMalloc/cudaFree (they can synchronise the device), or a C caller
+ * with no device allocator of its own.  The chunk partials go to a static
+ * device array of PKV_NOALLOC_SCRATCH_BYTES inside the library, which every GPU
+ * that loads the library holds until the process exits.
+ *   Arguments, layouts and results are those of pkv_decode_attention (the same
+ *   kernels run); the caller still passes every input and the output.
+ *   Limit: a problem whose pkv_decode_workspace_bytes(B, max_blocks,
+ *   pages_per_chunk) exceeds PKV_NOALLOC_SCRATCH_BYTES is rejected with
+ *   PKV_ERR_WORKSPACE_TOO_SMALL before anything is launched (for example batch
+ *   256 at 128 table entries fits with pages_per_chunk 16: 17.3 MB).
+ *   No cudaMalloc, cudaFree or allocating library routine is called.
+ *   The first call on a device looks up the array's device address with that
+ *   device current (cudaGetSymbolAddress); make that first call before any
+ *   stream capture begins.
+ *   All calls share the one array and it keeps the last call's contents; nothing
+ *   in it needs to start at zero.  Calls whose work overlaps on the GPU (other
+ *   streams, concurrent graph replays) race on it: serialise them. */
+int pkv_decode_attention_noalloc(const pkv_pool *pool, const uint16_t *q, const int32_t *bt_dev, int max_blocks,
+                                 const int32_t *seq_lens_dev, int B, float scale, int pages_per_chunk,
+                                 uint16_t *out, int32_t *dev_err_flag, void *cuda_stream);
+
 /* ------------------------------------------------------------------ misc */
 
 /* Synchronise the stream, read the device error flag into *host_flag (may be

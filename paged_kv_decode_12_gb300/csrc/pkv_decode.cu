@@ -39,6 +39,7 @@
 #include <cuda_bf16.h>
 
 #include <cmath>
+#include <mutex>
 
 #include "pkv_internal.h"
 
@@ -740,4 +741,77 @@ extern "C" int pkv_decode_attention(const pkv_pool *pool, const uint16_t *q, con
     return pkv_decode_attention_variant(pool, q, bt_dev, max_blocks, seq_lens_dev, B, scale, pages_per_chunk,
                                         workspace, workspace_bytes, out, dev_err_flag, cuda_stream,
                                         PKV_DECODE_DEFAULT);
+}
+
+// ---------------------------------------------------------------------------
+// Decode attention without any allocation by the caller or the library.
+//
+// For callers that cannot call cudaMalloc: a plugin hosted by an engine that
+// owns the whole device-memory budget through its own allocator and hands its
+// plugins no workspace; a latency-critical loop that must not call cudaMalloc or
+// cudaFree mid-run because they can synchronise the device; a C caller with no
+// device allocator of its own.  The chunk partials live in the file-scope array
+// below instead of a caller-supplied workspace.  That array is part of this
+// library's device image: every GPU that loads the library holds its
+// PKV_NOALLOC_SCRATCH_BYTES until the process exits.
+//
+// In host code `pkv_noalloc_scratch` names a host-side stand-in, not a device
+// address; handing it to a kernel would fault (or, where the GPU can reach host
+// memory, silently use the wrong memory).  The device address is looked up with
+// cudaGetSymbolAddress once per device, with that device current, on the
+// first call made on that device; make that first call before any stream
+// capture begins.
+static __device__ __align__(256) unsigned char pkv_noalloc_scratch[PKV_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kNoAllocMaxDevices = 64;
+
+struct NoAllocScratchSlot {
+    std::once_flag once;
+    void *ptr = nullptr;
+    cudaError_t err = cudaSuccess;
+};
+
+NoAllocScratchSlot g_noalloc_slots[kNoAllocMaxDevices];
+
+// Device address of the static scratch on the current device (looked up once).
+int noalloc_scratch_address(void **out)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices)
+        return PKV_ERR_CUDA;
+    NoAllocScratchSlot &slot = g_noalloc_slots[dev];
+    std::call_once(slot.once, [&slot] {
+        slot.err = cudaGetSymbolAddress(&slot.ptr, pkv_noalloc_scratch);
+    });
+    if (slot.err != cudaSuccess || slot.ptr == nullptr)
+        return PKV_ERR_CUDA;
+    *out = slot.ptr;
+    return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" int pkv_decode_attention_noalloc(const pkv_pool *pool, const uint16_t *q, const int32_t *bt_dev,
+                                            int max_blocks, const int32_t *seq_lens_dev, int B, float scale,
+                                            int pages_per_chunk, uint16_t *out, int32_t *dev_err_flag,
+                                            void *cuda_stream)
+{
+    if (!pool || !q || !bt_dev || !seq_lens_dev || !out)
+        return PKV_ERR_INVALID_ARG;
+    const size_t need = pkv_decode_workspace_bytes(B, max_blocks, pages_per_chunk);
+    if (need == 0)
+        return PKV_ERR_INVALID_ARG;
+    if (need > PKV_NOALLOC_SCRATCH_BYTES)
+        return PKV_ERR_WORKSPACE_TOO_SMALL;
+    void *scratch = nullptr;
+    const int st = noalloc_scratch_address(&scratch);
+    if (st != PKV_OK)
+        return st;
+    // The partials of every chunk are written by the split kernel before the merge
+    // reads them, so nothing left in the array by an earlier call is ever read and
+    // nothing needs clearing.
+    return pkv_decode_attention(pool, q, bt_dev, max_blocks, seq_lens_dev, B, scale, pages_per_chunk, scratch,
+                                PKV_NOALLOC_SCRATCH_BYTES, out, dev_err_flag, cuda_stream);
 }

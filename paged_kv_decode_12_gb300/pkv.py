@@ -45,7 +45,8 @@ PKV_DECODE_MMA = 2
 EXPORTED = (
     "pkv_pool_create", "pkv_pool_destroy", "pkv_pool_alloc", "pkv_pool_free", "pkv_pool_info",
     "pkv_block_tables_build", "pkv_rope_table_init", "pkv_append_rope", "pkv_decode_workspace_bytes",
-    "pkv_decode_attention", "pkv_decode_attention_variant", "pkv_check_device_error",
+    "pkv_decode_attention", "pkv_decode_attention_variant", "pkv_decode_attention_noalloc",
+    "pkv_check_device_error",
     "pkv_status_string", "pkv_version",
 )
 
@@ -85,6 +86,8 @@ def lib():
     L.pkv_decode_attention.argtypes = [_vp, _vp, _vp, _i32, _vp, _i32, ctypes.c_float, _i32, _vp,
                                        ctypes.c_size_t, _vp, _vp, _vp]
     L.pkv_decode_attention_variant.argtypes = L.pkv_decode_attention.argtypes + [_i32]
+    L.pkv_decode_attention_noalloc.argtypes = [_vp, _vp, _vp, _i32, _vp, _i32, ctypes.c_float, _i32, _vp, _vp,
+                                               _vp]
     L.pkv_check_device_error.argtypes = [_vp, _i32p, _vp]
     L.pkv_status_string.argtypes = [_i32]
     L.pkv_status_string.restype = ctypes.c_char_p
@@ -222,6 +225,18 @@ def pkv_decode_attention_variant(pool, q, bt_dev, max_blocks: int, seq_lens_dev,
                                               int(workspace_bytes), _ptr(out), _ptr(dev_err_flag),
                                               _stream(stream), int(variant)),
            "pkv_decode_attention_variant")
+
+
+PKV_NOALLOC_SCRATCH_BYTES = 32 << 20
+
+
+def pkv_decode_attention_noalloc(pool, q, bt_dev, max_blocks: int, seq_lens_dev, B: int, scale: float,
+                                 pages_per_chunk: int, out, dev_err_flag=None, stream=None) -> None:
+    """pkv_decode_attention with the library's static scratch instead of a workspace,
+    for callers that cannot allocate device memory (see include/pkv.h)."""
+    _check(lib().pkv_decode_attention_noalloc(pool, _ptr(q), _ptr(bt_dev), max_blocks, _ptr(seq_lens_dev), B,
+                                              float(scale), pages_per_chunk, _ptr(out), _ptr(dev_err_flag),
+                                              _stream(stream)), "pkv_decode_attention_noalloc")
 
 
 def pkv_check_device_error(dev_err_flag, stream=None):
