@@ -2,17 +2,21 @@
 """Benchmark: paged decode attention KV GB/s (% of GB300 HBM peak) and decode steps/s.
 
 A *step* is one decode step of the 16-layer engine's attention hot path: for
-every layer, the fused RoPE + page-slot append of each sequence's new token,
-then paged GQA decode attention over the sequence's pages (split kernel + LSE
-merge).  Default workload ``b256``: batch 256, every sequence at 2,048 tokens
+every layer, the RoPE + page-slot append of each sequence's new token, then
+paged GQA decode attention over the sequence's pages with the log-sum-exp merge
+of its chunks -- by default one fused kernel per layer (``--path separate``:
+append, split and merge launches).  Default workload ``b256``: batch 256, every sequence at 2,048 tokens
 (128 pages per sequence and layer), 32 query / 8 KV heads, head_dim 64, BF16 KV
 pool of 524,288 pages (16 GiB).  Other workloads: ``--config b64`` (log-normal
 lengths, median 300) and ``--config b8`` (uniform lengths).
 
 The timed region replays CUDA graphs of whole steps; the inputs (17 GB of KV per
-b256 step) are far larger than the 129 MB L2, so no flush is needed.  Each
-attention launch inside the graphs is bracketed by external timing events, which
-give the dominant kernel's average duration for the roofline.
+b256 step) are far larger than the 129 MB L2, so no flush is needed.  A second
+pass replays the same steps from graphs in which every attention launch is
+bracketed by external timing events; these give the dominant kernel's average
+duration for the roofline (the step time itself comes from uninstrumented
+graphs, since an event between two launches would serialise their programmatic
+dependent launch).
 
 ``--impl reference`` times the FP64 CPU oracle on a bounded sample of the same
 workload on the host cores (the reference arm; it runs none of the CUDA path).
@@ -48,6 +52,9 @@ CONFIG_TEXT = {
     "b8": "batch 8: lengths uniform in [1, 2048], 16 layers, 4096 pages of 32 KiB per layer",
 }
 VARIANTS = {"default": 0, "simt": 1, "mma": 2}
+# Pages per work unit, chosen per workload from a sweep of 8..128 (any fixed value keeps
+# results batch invariant: the chunking depends only on each sequence's own length).
+DEFAULT_CHUNK = {"b256": 128, "b64": 32, "b8": 16}
 L2_BYTES = 129 * 10**6
 
 
@@ -147,23 +154,30 @@ class ClockSampler:
                 "samples": len(sm), "power_w_max": max(power) if power else None}
 
 
+KERNEL_SOURCES = ("pkv_device.cuh", "pkv_decode.cu", "pkv_step.cu")
+
+
 def kernel_source_digest() -> str:
-    with open(os.path.join(ROOT, "paged_kv_decode_12_gb300", "csrc", "pkv_decode.cu"), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """Digest of the attention kernels' sources (ties a stored ncu figure to the code it measured)."""
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "paged_kv_decode_12_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
-def measured_traffic(config: str, variant_name: str, pages_per_chunk: int):
-    """DRAM bytes per attention launch from a committed ncu summary, if it was taken
-    on the current kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", "decode_split_traffic.json")
+def measured_traffic(config: str, path: str, variant_name: str, pages_per_chunk: int):
+    """DRAM bytes per attention launch from the committed ncu summary
+    (profiles/decode_traffic.json), if it was taken on the current kernel source;
+    else None."""
     try:
-        with open(path) as f:
+        with open(os.path.join(ROOT, "profiles", "decode_traffic.json")) as f:
             entries = json.load(f)
     except Exception:
         return None
     digest = kernel_source_digest()
     for e in entries:
-        if (e.get("config") == config and e.get("variant") == variant_name and
+        if (e.get("config") == config and e.get("path") == path and e.get("variant") == variant_name and
                 e.get("pages_per_chunk") == pages_per_chunk and e.get("kernel_source_sha") == digest):
             return e.get("dram_bytes_per_launch")
     return None
@@ -214,11 +228,9 @@ def cpu_baseline(w, seconds: float, seed: int) -> dict:
     pool = oracle_samples(w, 64, seed)
     tokens, seqs = 0, 0
     t0 = time.perf_counter()
-    for s in pool:
-        tokens += oracle_run_sample([s])
+    while time.perf_counter() - t0 < seconds:       # cycle over the prepared sample
+        tokens += oracle_run_sample([pool[seqs % len(pool)]])
         seqs += 1
-        if time.perf_counter() - t0 >= seconds:
-            break
     dt = time.perf_counter() - t0
     return {"value": tokens * per_token / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"{seqs} sequences of one layer ({tokens} KV tokens): append + attention for all 32 "
@@ -232,6 +244,8 @@ def config_block(w, args, variant_name: str, graph: bool) -> dict:
     return {"workload": f"{args.config}: {CONFIG_TEXT[args.config]}", "batch": w.batch, "layers": w.layers,
             "seq_len_max": int(w.seq_lens.max()), "seq_len_mean": float(w.seq_lens.mean()),
             "pages_per_chunk": args.pages_per_chunk, "kernel_variant": variant_name, "cuda_graph": graph,
+            "path": getattr(args, "path", "fused"), "pdl": not getattr(args, "no_pdl", False),
+            "schedule": getattr(args, "schedule", "auto"),
             "kv_bytes_per_step": kv,
             "l2": f"inputs larger than L2 ({kv / 1e9:.2f} GB of KV per step vs {L2_BYTES / 1e6:.0f} MB L2), "
                   "no flush", "seed": args.seed}
@@ -287,19 +301,27 @@ def run_pkv(args):
 
     variant_name = args.variant
     dw = harness.setup(args.config, replica_seed(args.seed, rank), args.pages_per_chunk, VARIANTS[variant_name],
-                       layers=args.layers)
+                       layers=args.layers, fused=args.path == "fused", pdl=not args.no_pdl,
+                       schedule=args.schedule)
     w = dw.w
     harness.warm(dw, 2)
     dw.reset_q()
     ext = harness.external_events_supported()
     per_graph = max(1, min(args.steps, args.steps_per_graph))
     warm_cap = harness.capture_steps(dw, max(1, min(args.warmup, per_graph)))
-    timed = []
-    left = args.steps
-    while left > 0:
-        n = min(per_graph, left)
-        timed.append(harness.capture_steps(dw, n, time_attention=ext))
-        left -= n
+
+    def capture_all(instrumented):
+        caps, left = [], args.steps
+        while left > 0:
+            n = min(per_graph, left)
+            caps.append(harness.capture_steps(dw, n, time_attention=instrumented))
+            left -= n
+        return caps
+
+    # the step time comes from plain graphs: a timing event between two launches
+    # would turn their programmatic (overlapping) dependency into a full one
+    timed = capture_all(False)
+    timed_ev = capture_all(True) if ext else []
     torch.cuda.synchronize()
 
     # warm-up: W steps
@@ -329,13 +351,17 @@ def run_pkv(args):
         torch.distributed.barrier()
     clocks = sampler.stop(t0, t1)
     elapsed_ms = reduce_max(start.elapsed_time(end), world, device)
+    # second pass, same steps: per-launch durations of the attention kernel
+    for cap in timed_ev:
+        cap.graph.replay()
+    torch.cuda.synchronize()
 
     st, flag = dw.eng.check_errors()
     if st != pkv.PKV_OK:
         raise SystemExit(f"device error flag set during the timed region: {flag:#x}")
 
     # dominant kernel: the attention launches (split + merge), timed inside the graphs
-    split_ms = [s.elapsed_time(e) for cap in timed for (s, e) in cap.split_events]
+    split_ms = [s.elapsed_time(e) for cap in timed_ev for (s, e) in cap.split_events]
     kv_step = w.kv_bytes_per_step()
     kv_launch = kv_step // w.layers
     peak, peak_src = hbm_peak()
@@ -346,8 +372,11 @@ def run_pkv(args):
         avg = sum(split_ms) / len(split_ms)
         achieved = kv_launch / (avg / 1e3) / 1e9
         roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                    "traffic": measured_traffic(args.config, variant_name, args.pages_per_chunk),
-                    "kernel": f"paged decode attention launch (split + merge), variant {variant_name}",
+                    "traffic": measured_traffic(args.config, args.path, variant_name, args.pages_per_chunk),
+                    "kernel": (f"fused decode step kernel (append + attention + merge), variant {variant_name}"
+                               if args.path == "fused" else
+                               f"paged decode attention launch (split + merge), variant {variant_name}"),
+                    "timing": "external events around every launch in a second pass of the same steps",
                     "algorithmic_bytes_per_launch": kv_launch, "avg_launch_us": avg * 1e3,
                     "launches_timed": len(split_ms), "peak_source": f"{peak_src} hbm_gbs (burst copy)"}
 
@@ -416,8 +445,15 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["pkv", "reference"], default="pkv")
     ap.add_argument("--config", choices=sorted(CONFIG_TEXT), default="b256")
-    ap.add_argument("--pages-per-chunk", type=int, default=16)
+    ap.add_argument("--pages-per-chunk", type=int, default=None,
+                    help="pages per work unit (default: the measured best for the workload, "
+                         + ", ".join(f"{k} {v}" for k, v in DEFAULT_CHUNK.items()) + ")")
     ap.add_argument("--variant", choices=sorted(VARIANTS), default="default")
+    ap.add_argument("--path", choices=["fused", "separate"], default="fused",
+                    help="one fused kernel per layer, or append + split + merge launches")
+    ap.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
+    ap.add_argument("--schedule", choices=["auto", "grid", "persistent"], default="auto",
+                    help="fused path: one CTA per unit, or persistent CTAs walking the units")
     ap.add_argument("--seed", type=int, default=12)
     ap.add_argument("--layers", type=int, default=None, help="override the layer count (small profiling runs)")
     ap.add_argument("--steps-per-graph", type=int, default=25)
@@ -427,6 +463,8 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-seqs", type=int, default=2, help="sequences per reference-arm step")
     args = ap.parse_args(argv)
+    if args.pages_per_chunk is None:
+        args.pages_per_chunk = DEFAULT_CHUNK[args.config]
     if args.impl == "reference":
         return run_reference(args)
     return run_pkv(args)

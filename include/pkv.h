@@ -204,6 +204,46 @@ int pkv_decode_attention_variant(const pkv_pool *pool, const uint16_t *q, const 
                                  int pages_per_chunk, void *workspace, size_t workspace_bytes, uint16_t *out,
                                  int32_t *dev_err_flag, void *cuda_stream, int variant);
 
+/* ------------------------------------------------------ fused decode step */
+
+/* option bits for pkv_decode_step */
+#define PKV_STEP_NO_PDL 0x100     /* launch without programmatic dependent launch */
+#define PKV_STEP_GRID 0x200       /* one CTA per (sequence, KV head, chunk) */
+#define PKV_STEP_PERSISTENT 0x400 /* a few CTAs per SM walk the units (B <= 512) */
+
+/* Bytes of device workspace pkv_decode_step needs (a per-(sequence, KV head)
+ * counter array followed by the chunk partials). */
+size_t pkv_decode_step_workspace_bytes(int B, int max_blocks, int pages_per_chunk);
+
+/* One layer of the decode step in ONE kernel launch: pkv_append_rope with
+ * pos = seq_lens - 1 (q rotated in place, the new key rotated and stored with its
+ * value into page bt_dev[b][pos/16], slot pos%16) followed by
+ * pkv_decode_attention -- the two steps the samir-vllm README summary lists in
+ * "目前已完成的功能" (append at the absolute RoPE position; paged decode
+ * attention with an FP32 online softmax).  Results are bit-identical to the two
+ * separate calls with the same variant and pages_per_chunk.
+ *   k_new, v_new [B][8][64] BF16; q [B][32][64] BF16, required, rotated in place;
+ *   rope_table / max_pos as for pkv_append_rope (seq_lens[b] <= max_pos);
+ *   workspace  >= pkv_decode_step_workspace_bytes(...) bytes, 16-byte aligned.
+ *              Its counter region must be zero before the FIRST call (e.g. one
+ *              cudaMemset after allocating); every call leaves it zero again.
+ *              Calls sharing a workspace must not overlap on the GPU.
+ *   options    PKV_DECODE_DEFAULT / _SIMT / _MMA, optionally | PKV_STEP_NO_PDL, and
+ *              a schedule: PKV_STEP_GRID (one CTA per unit) or PKV_STEP_PERSISTENT
+ *              (SMs x CTAs-per-SM CTAs walk a device-built list of the non-empty
+ *              units, prefetching across unit boundaries; B <= 512).  Neither:
+ *              grid.  Results are identical.
+ * Launch: programmatic dependent launch (unless PKV_STEP_NO_PDL).  Before its
+ * dependency wait a CTA reads only seq_lens and bt_dev and starts copying this
+ * layer's cached pages; the caller must therefore not have an immediately
+ * preceding kernel on the stream write those three (block tables of different
+ * layers must not share pages -- pkv_block_tables_build never does).
+ * Device checks as pkv_decode_attention, plus seq_len > max_pos. */
+int pkv_decode_step(const pkv_pool *pool, const uint16_t *k_new, const uint16_t *v_new, uint16_t *q,
+                    const int32_t *bt_dev, int max_blocks, const int32_t *seq_lens_dev, int B,
+                    const float *rope_table, int max_pos, float scale, int pages_per_chunk, void *workspace,
+                    size_t workspace_bytes, uint16_t *out, int32_t *dev_err_flag, void *cuda_stream, int options);
+
 /* Size of the library's static scratch used by pkv_decode_attention_noalloc. */
 #define PKV_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20) /* 32 MiB */
 

@@ -14,7 +14,7 @@
 // (about 2 KiB written per sequence); the kernel is latency-bound.
 #include <cuda_bf16.h>
 
-#include "pkv_internal.h"
+#include "pkv_device.cuh"
 
 namespace pkv {
 namespace {
@@ -70,10 +70,8 @@ append_rope_kernel(uint16_t *__restrict__ slab, int num_pages, const uint16_t *_
         const float2 x1 = __bfloat1622float2(lo);   // dims 2j, 2j+1
         const float2 x2 = __bfloat1622float2(hi);   // dims 2j+32, 2j+33
         float2 y1, y2;
-        y1.x = fmaf(x1.x, cs.x, -x2.x * cs.y);
-        y2.x = fmaf(x2.x, cs.x, x1.x * cs.y);
-        y1.y = fmaf(x1.y, cs.z, -x2.y * cs.w);
-        y2.y = fmaf(x2.y, cs.z, x1.y * cs.w);
+        dev::rope_rotate_pair(x1.x, x2.x, cs.x, cs.y, y1.x, y2.x);
+        dev::rope_rotate_pair(x1.y, x2.y, cs.z, cs.w, y1.y, y2.y);
         *reinterpret_cast<__nv_bfloat162 *>(dst + 2 * j) = __float22bfloat162_rn(y1);
         *reinterpret_cast<__nv_bfloat162 *>(dst + kD / 2 + 2 * j) = __float22bfloat162_rn(y2);
     }

@@ -41,420 +41,12 @@
 #include <cmath>
 #include <mutex>
 
-#include "pkv_internal.h"
+#include "pkv_device.cuh"
 
 namespace pkv {
 namespace {
 
-constexpr int kWarps = 4;
-constexpr int kThreads = kWarps * 32;
-constexpr int kTileBytes = kPage * kD * 2;   // one (page, KV head) K tile: 2 KiB
-constexpr int kStageBytes = 2 * kTileBytes;  // K tile then V tile
-constexpr int kStateFloats = 8 + kGroup * kD;  // m[4], l[4], o[4][64] per warp
-constexpr int kScratchFloats = 72;           // per-warp p[16][4] + alpha[4], padded
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr uint32_t kWaitLimit = 1u << 22;
-constexpr unsigned kFull = 0xffffffffu;
-
-static_assert(kThreads == kGroup * 32, "combine maps one thread per (head, dim pair)");
-
-// ------------------------------------------------------------------ PTX helpers
-
-__device__ __forceinline__ uint32_t smem_addr(const void *p)
-{
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void fence_barrier_init()
-{
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-__device__ __forceinline__ void fence_proxy_async_smem()
-{
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_addr(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Warp-uniform bounded wait: true once every lane has observed the phase.
-__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity)
-{
-    for (uint32_t i = 0; i < kWaitLimit; ++i)
-        if (__all_sync(kFull, mbar_try_wait(bar, parity)))
-            return true;
-    return false;
-}
-
-__device__ __forceinline__ uint64_t l2_evict_first_policy()
-{
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-
-// One (page, KV head): 16 K rows then 16 V rows of 128 B, 128-byte swizzled.
-__device__ __forceinline__ void tma_load_page_head(void *dst, const CUtensorMap *map, uint64_t *bar, int head,
-                                                   int page, uint64_t policy)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(smem_addr(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(0), "r"(head), "r"(0), "r"(page), "r"(smem_addr(bar)),
-        "l"(policy)
-        : "memory");
-}
-
-// Byte offset of the 16-byte chunk `chunk` (0..7) of row `row` in a 128-byte
-// swizzled tile (the TMA SWIZZLE_128B pattern on a 1024-byte aligned buffer).
-__device__ __forceinline__ uint32_t swz(int row, int chunk)
-{
-    return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
-}
-
-__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
-{
-    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t *>(&v);
-}
-
-// ------------------------------------------------------------------ SIMT policy
-
-struct SimtWarp {
-    float qf[kGroup][8];  // q[h][8*dg .. 8*dg+7] * scale * log2(e)
-    float acc[kGroup][2]; // o[h][2*lane], o[h][2*lane+1]
-    float m[2], l[2];     // heads h0 = 2*(lane&1), h0+1; l is a per-lane partial sum
-    float *ps;            // per-warp scratch: p[16 tokens][4 heads], alpha[4]
-    int lane;
-
-    __device__ __forceinline__ void init(const uint16_t *qg, float scale_log2, int lane_, float *scratch)
-    {
-        lane = lane_;
-        ps = scratch;
-        const int dg = lane & 7;
-#pragma unroll
-        for (int h = 0; h < kGroup; ++h) {
-            const uint4 v = *reinterpret_cast<const uint4 *>(qg + h * kD + 8 * dg);
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                qf[h][2 * i] = bf16lo(w[i]) * scale_log2;
-                qf[h][2 * i + 1] = bf16hi(w[i]) * scale_log2;
-            }
-            acc[h][0] = acc[h][1] = 0.f;
-        }
-        m[0] = m[1] = -INFINITY;
-        l[0] = l[1] = 0.f;
-    }
-
-    __device__ __forceinline__ void page(const uint8_t *st, int nvalid)
-    {
-        const int dg = lane & 7, tg = lane >> 3;
-        // ---- partial dot products: tokens 4tg..4tg+3, dims 8dg..8dg+7, 4 heads
-        float v[16];  // index i*4 + h
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int t = 4 * tg + i;
-            const uint4 kw = *reinterpret_cast<const uint4 *>(st + swz(t, dg));
-            const uint32_t w[4] = {kw.x, kw.y, kw.z, kw.w};
-            float k[8];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                k[2 * j] = bf16lo(w[j]);
-                k[2 * j + 1] = bf16hi(w[j]);
-            }
-#pragma unroll
-            for (int h = 0; h < kGroup; ++h) {
-                float s = qf[h][0] * k[0];
-#pragma unroll
-                for (int j = 1; j < 8; ++j)
-                    s = fmaf(qf[h][j], k[j], s);
-                v[i * 4 + h] = s;
-            }
-        }
-        // ---- reduce-scatter over the 8 lanes of a token group (lane bits 0..2)
-        const bool b2 = lane & 4, b1 = lane & 2, b0 = lane & 1;
-        float u[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const float send = b2 ? v[k] : v[k + 8];
-            const float keep = b2 ? v[k + 8] : v[k];
-            u[k] = keep + __shfl_xor_sync(kFull, send, 4);
-        }
-        float w4[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const float send = b1 ? u[k] : u[k + 4];
-            const float keep = b1 ? u[k + 4] : u[k];
-            w4[k] = keep + __shfl_xor_sync(kFull, send, 2);
-        }
-        float s[2];
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-            const float send = b0 ? w4[k] : w4[k + 2];
-            const float keep = b0 ? w4[k + 2] : w4[k];
-            s[k] = keep + __shfl_xor_sync(kFull, send, 1);
-        }
-        // this lane now holds token t = 4tg + 2*b2 + b1, heads h0 = 2*b0 and h0+1
-        const int t = 4 * tg + (b2 ? 2 : 0) + (b1 ? 1 : 0);
-        const int h0 = b0 ? 2 : 0;
-        if (t >= nvalid)
-            s[0] = s[1] = -INFINITY;
-        // ---- online softmax update (log2 domain)
-        float pm0 = s[0], pm1 = s[1];
-#pragma unroll
-        for (int off = 2; off <= 16; off <<= 1) {
-            pm0 = fmaxf(pm0, __shfl_xor_sync(kFull, pm0, off));
-            pm1 = fmaxf(pm1, __shfl_xor_sync(kFull, pm1, off));
-        }
-        const float mn0 = fmaxf(m[0], pm0), mn1 = fmaxf(m[1], pm1);
-        const float al0 = exp2f(m[0] - mn0), al1 = exp2f(m[1] - mn1);
-        const float p0 = exp2f(s[0] - mn0), p1 = exp2f(s[1] - mn1);
-        l[0] = fmaf(l[0], al0, p0);
-        l[1] = fmaf(l[1], al1, p1);
-        m[0] = mn0;
-        m[1] = mn1;
-        *reinterpret_cast<float2 *>(ps + t * 4 + h0) = make_float2(p0, p1);
-        if ((lane >> 1) == 0)
-            *reinterpret_cast<float2 *>(ps + 64 + h0) = make_float2(al0, al1);
-        __syncwarp();
-        // ---- o = alpha * o + sum_t p_t v_t, lane owns dims 2*lane, 2*lane+1
-        const float4 al = *reinterpret_cast<const float4 *>(ps + 64);
-        acc[0][0] *= al.x; acc[0][1] *= al.x;
-        acc[1][0] *= al.y; acc[1][1] *= al.y;
-        acc[2][0] *= al.z; acc[2][1] *= al.z;
-        acc[3][0] *= al.w; acc[3][1] *= al.w;
-        const uint8_t *vt = st + kTileBytes;
-        const uint32_t col = (uint32_t)((lane & 3) << 2);
-        if (nvalid == kPage) {
-#pragma unroll
-            for (int tt = 0; tt < kPage; ++tt)
-                pv_token(vt, tt, col);
-        } else {
-            for (int tt = 0; tt < nvalid; ++tt)
-                pv_token(vt, tt, col);
-        }
-        __syncwarp();
-    }
-
-    __device__ __forceinline__ void pv_token(const uint8_t *vt, int tt, uint32_t col)
-    {
-        const uint32_t w = *reinterpret_cast<const uint32_t *>(vt + swz(tt, lane >> 2) + col);
-        const float v0 = bf16lo(w), v1 = bf16hi(w);
-        const float4 p = *reinterpret_cast<const float4 *>(ps + tt * 4);
-        acc[0][0] = fmaf(p.x, v0, acc[0][0]); acc[0][1] = fmaf(p.x, v1, acc[0][1]);
-        acc[1][0] = fmaf(p.y, v0, acc[1][0]); acc[1][1] = fmaf(p.y, v1, acc[1][1]);
-        acc[2][0] = fmaf(p.z, v0, acc[2][0]); acc[2][1] = fmaf(p.z, v1, acc[2][1]);
-        acc[3][0] = fmaf(p.w, v0, acc[3][0]); acc[3][1] = fmaf(p.w, v1, acc[3][1]);
-    }
-
-    // write m[4], l[4] (log2 domain) and o[4][64] of this warp
-    __device__ __forceinline__ void store_state(float *dst)
-    {
-#pragma unroll
-        for (int off = 2; off <= 16; off <<= 1) {
-            l[0] += __shfl_xor_sync(kFull, l[0], off);
-            l[1] += __shfl_xor_sync(kFull, l[1], off);
-        }
-        if ((lane >> 1) == 0) {
-            const int h0 = (lane & 1) ? 2 : 0;
-            dst[h0] = m[0];
-            dst[h0 + 1] = m[1];
-            dst[4 + h0] = l[0];
-            dst[4 + h0 + 1] = l[1];
-        }
-#pragma unroll
-        for (int h = 0; h < kGroup; ++h)
-            *reinterpret_cast<float2 *>(dst + 8 + h * kD + 2 * lane) = make_float2(acc[h][0], acc[h][1]);
-    }
-};
-
-// ------------------------------------------------------------------ MMA policy
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4])
-{
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(addr));
-}
-
-__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4])
-{
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(addr));
-}
-
-__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a)
-{
-    uint32_t d;
-    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
-    return d;
-}
-
-// D = A(16x16, row) * B(16x8, col) + D, BF16 inputs, FP32 accumulate
-__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
-{
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-        "{%0, %1, %2, %3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-struct MmaWarp {
-    uint32_t qb[4][2];  // B fragments of Q^T for the 4 k-steps (dims 16ks..16ks+15)
-    float o[4][4];      // O^T accumulators, m-tile mt = dims 16mt..16mt+15
-    float m[2], l[2];   // heads 2*tig + e (meaningful in lanes with tig < 2)
-    float c;            // scale * log2(e)
-    int lane;
-
-    __device__ __forceinline__ void init(const uint16_t *qg, float scale_log2, int lane_, float *)
-    {
-        lane = lane_;
-        c = scale_log2;
-        const int gid = lane >> 2, tig = lane & 3;
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-            if (gid < kGroup) {
-                const uint16_t *row = qg + gid * kD + 16 * ks + 2 * tig;
-                qb[ks][0] = *reinterpret_cast<const uint32_t *>(row);
-                qb[ks][1] = *reinterpret_cast<const uint32_t *>(row + 8);
-            } else {
-                qb[ks][0] = qb[ks][1] = 0u;
-            }
-        }
-#pragma unroll
-        for (int mt = 0; mt < 4; ++mt)
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                o[mt][i] = 0.f;
-        m[0] = m[1] = -INFINITY;
-        l[0] = l[1] = 0.f;
-    }
-
-    __device__ __forceinline__ void page(const uint8_t *st, int nvalid)
-    {
-        const int gid = lane >> 2, tig = lane & 3;
-        const uint32_t kbase = smem_addr(st);
-        const uint32_t vbase = kbase + kTileBytes;
-        // ---- S^T[16 tokens][8 heads] = K . Q^T
-        float s[4] = {0.f, 0.f, 0.f, 0.f};
-        {
-            const int mi = lane >> 3, r = lane & 7;
-            const int tok = r + ((mi & 1) ? 8 : 0);
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-                uint32_t a[4];
-                ldsm_x4(kbase + swz(tok, 2 * ks + (mi >> 1)), a);
-                mma_bf16(s, a, qb[ks][0], qb[ks][1]);
-            }
-        }
-        // s[0], s[1]: token gid, heads 2tig, 2tig+1; s[2], s[3]: token gid+8
-        float x[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-            x[i] = s[i] * c;
-        if (gid >= nvalid)
-            x[0] = x[1] = -INFINITY;
-        if (gid + 8 >= nvalid)
-            x[2] = x[3] = -INFINITY;
-        float pm0 = fmaxf(x[0], x[2]), pm1 = fmaxf(x[1], x[3]);
-#pragma unroll
-        for (int off = 4; off <= 16; off <<= 1) {
-            pm0 = fmaxf(pm0, __shfl_xor_sync(kFull, pm0, off));
-            pm1 = fmaxf(pm1, __shfl_xor_sync(kFull, pm1, off));
-        }
-        const float mn0 = fmaxf(m[0], pm0), mn1 = fmaxf(m[1], pm1);
-        const float al0 = exp2f(m[0] - mn0), al1 = exp2f(m[1] - mn1);
-        const float p0 = exp2f(x[0] - mn0), p1 = exp2f(x[1] - mn1);
-        const float p2 = exp2f(x[2] - mn0), p3 = exp2f(x[3] - mn1);
-        l[0] = fmaf(l[0], al0, p0 + p2);
-        l[1] = fmaf(l[1], al1, p1 + p3);
-        m[0] = mn0;
-        m[1] = mn1;
-        // ---- P^T as the B operand: transpose the two 8x8 BF16 blocks
-        const uint32_t b0 = movmatrix_trans(pack_bf16x2(p0, p1));  // tokens 2tig, 2tig+1 ; head gid
-        const uint32_t b1 = movmatrix_trans(pack_bf16x2(p2, p3));  // tokens 2tig+8, 2tig+9
-        // ---- O^T = alpha * O^T + V^T . P^T
-        const int mi = lane >> 3, r = lane & 7;
-        const int tok = r + ((mi >> 1) ? 8 : 0);
-        const bool partial = nvalid < kPage;
-        // token masks of this lane's A-fragment halves: a0/a1 tokens 2tig, 2tig+1; a2/a3 +8
-        const uint32_t mlo = (2 * tig < nvalid ? 0x0000ffffu : 0u) | (2 * tig + 1 < nvalid ? 0xffff0000u : 0u);
-        const uint32_t mhi =
-            (2 * tig + 8 < nvalid ? 0x0000ffffu : 0u) | (2 * tig + 9 < nvalid ? 0xffff0000u : 0u);
-#pragma unroll
-        for (int mt = 0; mt < 4; ++mt) {
-            uint32_t a[4];
-            ldsm_x4_trans(vbase + swz(tok, 2 * mt + (mi & 1)), a);
-            if (partial) {  // zero V of slots past the sequence end (their bytes are arbitrary)
-                a[0] &= mlo;
-                a[1] &= mlo;
-                a[2] &= mhi;
-                a[3] &= mhi;
-            }
-            o[mt][0] *= al0;
-            o[mt][1] *= al1;
-            o[mt][2] *= al0;
-            o[mt][3] *= al1;
-            mma_bf16(o[mt], a, b0, b1);
-        }
-    }
-
-    __device__ __forceinline__ void store_state(float *dst)
-    {
-#pragma unroll
-        for (int off = 4; off <= 16; off <<= 1) {
-            l[0] += __shfl_xor_sync(kFull, l[0], off);
-            l[1] += __shfl_xor_sync(kFull, l[1], off);
-        }
-        const int gid = lane >> 2, tig = lane & 3;
-        if (tig < 2) {
-            if (gid == 0) {
-                dst[2 * tig] = m[0];
-                dst[2 * tig + 1] = m[1];
-                dst[4 + 2 * tig] = l[0];
-                dst[4 + 2 * tig + 1] = l[1];
-            }
-#pragma unroll
-            for (int mt = 0; mt < 4; ++mt) {
-                float *h0 = dst + 8 + (2 * tig) * kD + 16 * mt + gid;
-                float *h1 = h0 + kD;
-                h0[0] = o[mt][0];
-                h1[0] = o[mt][1];
-                h0[8] = o[mt][2];
-                h1[8] = o[mt][3];
-            }
-        }
-    }
-};
+using namespace dev;
 
 // ------------------------------------------------------------------ kernels
 
@@ -476,7 +68,7 @@ struct SplitArgs {
 template <int STAGES>
 constexpr int split_smem_bytes()
 {
-    return 1024 + kWarps * STAGES * kStageBytes + kWarps * STAGES * 8 + kWarps * kScratchFloats * 4;
+    return SmemLayout<STAGES>::kBaseBytes;
 }
 
 // Write this CTA's 4 heads as "no contribution": zeros if the sequence has one
@@ -498,10 +90,7 @@ template <class Warp, int STAGES>
 __global__ void __launch_bounds__(kThreads) decode_split_kernel(const __grid_constant__ CUtensorMap tmap, SplitArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *stages = smem;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kWarps * STAGES * kStageBytes);
-    float *scratch = reinterpret_cast<float *>(bars + kWarps * STAGES);
+    SmemLayout<STAGES> sm(smem_raw);
 
     const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -535,79 +124,30 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const __grid_con
         return;
     }
 
-    uint64_t *my_bars = bars + warp * STAGES;
-    uint8_t *my_stages = stages + warp * STAGES * kStageBytes;
-    if (lane == 0) {
-#pragma unroll
-        for (int s = 0; s < STAGES; ++s)
-            mbar_init(&my_bars[s], 1);
-        fence_barrier_init();
-    }
-    __syncwarp();
+    uint64_t *my_bars = sm.bars + warp * STAGES;
+    uint8_t *my_stages = sm.stages + warp * STAGES * kStageBytes;
+    init_warp_barriers<STAGES>(my_bars, lane);
     const uint64_t policy = l2_evict_first_policy();
-    const int prologue = min(STAGES, nmine);
-    for (int k = 0; k < prologue; ++k) {
-        const int pk = __shfl_sync(kFull, my_page, k);
-        if (lane == 0) {
-            mbar_arrive_expect_tx(&my_bars[k], kStageBytes);
-            tma_load_page_head(my_stages + k * kStageBytes, &tmap, &my_bars[k], g, pk, policy);
-        }
-    }
+    issue_prologue<STAGES>(&tmap, my_stages, my_bars, my_page, nmine, g, lane, policy);
 
     Warp w;
-    w.init(a.q + ((size_t)b * kHq + g * kGroup) * kD, a.scale_log2, lane, scratch + warp * kScratchFloats);
-
-    int k = 0;
-    for (; k < nmine; ++k) {
-        const int s = k % STAGES;
-        if (!mbar_wait_warp(&my_bars[s], (uint32_t)((k / STAGES) & 1)))
-            break;
-        const int j = j0 + warp + k * kWarps;
-        w.page(my_stages + s * kStageBytes, min(kPage, L - j * kPage));
-        __syncwarp();
-        if (k + STAGES < nmine) {
-            const int pk = __shfl_sync(kFull, my_page, k + STAGES);
-            if (lane == 0) {
-                fence_proxy_async_smem();
-                mbar_arrive_expect_tx(&my_bars[s], kStageBytes);
-                tma_load_page_head(my_stages + s * kStageBytes, &tmap, &my_bars[s], g, pk, policy);
-            }
-        }
-    }
-    const bool timed_out = k < nmine;
-    if (timed_out) {
-        // give the copies still in flight a bounded chance to land before the
-        // shared memory is reused; the result of this unit is flagged invalid
-        for (int kk = k; kk < min(nmine, k + STAGES); ++kk)
-            (void)mbar_wait_warp(&my_bars[kk % STAGES], (uint32_t)((kk / STAGES) & 1));
-        if (lane == 0 && a.err)
-            atomicOr(a.err, PKV_DEVERR_TIMEOUT);
-    }
+    w.init(a.q + ((size_t)b * kHq + g * kGroup) * kD, a.scale_log2, lane, sm.scratch + warp * kScratchFloats);
+    if (!consume_pages<STAGES>(&tmap, my_stages, my_bars, w, my_page, nmine, j0, warp, lane, L, g, policy,
+                               NoPatch{}) &&
+        lane == 0 && a.err)
+        atomicOr(a.err, PKV_DEVERR_TIMEOUT);
 
     // ---- combine the 4 warps' (m, l, o) in shared memory (stages are free now)
     __syncthreads();
-    float *state = reinterpret_cast<float *>(stages);
+    float *state = reinterpret_cast<float *>(sm.stages);
     w.store_state(state + warp * kStateFloats);
     __syncthreads();
     const int hl = threadIdx.x >> 5, dp = threadIdx.x & 31;
-    float M = -INFINITY;
-#pragma unroll
-    for (int ww = 0; ww < kWarps; ++ww)
-        M = fmaxf(M, state[ww * kStateFloats + hl]);
-    float lsum = 0.f, o0 = 0.f, o1 = 0.f;
-#pragma unroll
-    for (int ww = 0; ww < kWarps; ++ww) {
-        const float mw = state[ww * kStateFloats + hl];
-        const float f = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
-        lsum = fmaf(f, state[ww * kStateFloats + 4 + hl], lsum);
-        const float2 ow = *reinterpret_cast<const float2 *>(state + ww * kStateFloats + 8 + hl * kD + 2 * dp);
-        o0 = fmaf(f, ow.x, o0);
-        o1 = fmaf(f, ow.y, o1);
-    }
+    float M, lsum, o0, o1;
+    combine_warps(state, hl, dp, M, lsum, o0, o1);
     const int h = g * kGroup + hl;
     if (nchunks == 1) {
-        const float inv = 1.f / lsum;
-        reinterpret_cast<uint32_t *>(a.out + ((size_t)b * kHq + h) * kD)[dp] = pack_bf16x2(o0 * inv, o1 * inv);
+        reinterpret_cast<uint32_t *>(a.out + ((size_t)b * kHq + h) * kD)[dp] = finish_pair(o0, o1, lsum);
     } else {
         const size_t idx = ((size_t)b * kHq + h) * a.max_chunks + c;
         reinterpret_cast<float2 *>(a.part_o + idx * kD)[dp] = make_float2(o0, o1);

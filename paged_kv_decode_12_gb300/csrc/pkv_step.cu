@@ -1,0 +1,635 @@
+// pkv_step.cu -- one fused launch per layer: RoPE + page-slot append of the new
+// token, paged GQA decode attention over the sequence's pages, and the
+// log-sum-exp merge of the chunk partials.
+//
+// It computes exactly what pkv_append_rope (positions = seq_lens - 1, q rotated
+// in place) followed by pkv_decode_attention computes -- the samir-vllm README
+// summary ("从零用 C++ 和 CUDA 实现 Llama 3.2 1B 推理引擎", section "目前已完成的功能")
+// describes both steps: decode appends one token at its absolute RoPE position,
+// then each query head streams its sequence's pages with an FP32 online softmax
+// -- with the same arithmetic, so the results are bit-identical to the two
+// separate calls.  What changes is the schedule.
+//
+// Work unit = (sequence b, KV head g, chunk c of pages_per_chunk pages), as in the
+// split kernel.  Per unit:
+//  * the 4 query rows of group g are rotated to position L-1 by the unit itself;
+//    the rotated rows are written back once, by the unit that finishes (b, g) last;
+//  * the sequence's last chunk computes the new token's rotated key and its value,
+//    stores them into their page slot in HBM and patches them into the
+//    shared-memory copy of the last page, so no unit waits for an append kernel;
+//  * chunk partials are merged in-kernel: each unit publishes its partial and
+//    takes a ticket from a per-(b, g) counter (one release-acquire atomicAdd, no
+//    waiting); the unit drawing the last ticket merges all chunks in chunk order
+//    (deterministic) and resets the counter to zero for the next launch.
+// Two schedules:
+//  * grid: one CTA per unit (grid = chunks x 8 x B); best for long sequences
+//    with large chunks;
+//  * persistent: a few CTAs per SM walk a compact, device-built list of the
+//    non-empty units; each warp's TMA ring keeps prefetching pages ACROSS unit
+//    boundaries, so a unit's set-up and epilogue (combine, ticket, merge) hide
+//    behind copies already in flight.  Best for ragged and small batches.
+// Both use programmatic dependent launch: before griddepcontrol.wait a CTA only
+// reads this step's lengths and block tables and starts the TMA copies of this
+// layer's cached pages (which no earlier kernel of the step writes: every layer
+// has its own pages); q, k_new, v_new are read and every output is written after
+// the wait.
+#include <cuda_bf16.h>
+
+#include "pkv_device.cuh"
+
+namespace pkv {
+namespace {
+
+using namespace dev;
+
+struct StepArgs {
+    int num_pages;
+    uint16_t *slab;
+    const uint16_t *k_new;   // [B][8][64]
+    const uint16_t *v_new;   // [B][8][64]
+    uint16_t *q;             // [B][32][64], rotated in place
+    const int32_t *bt;       // [B][max_blocks]
+    int max_blocks;
+    const int32_t *seq_lens; // [B]
+    const float2 *rope;      // [max_pos][32] (cos, sin)
+    int max_pos;
+    float scale_log2;
+    int pages_per_chunk;
+    int *counters;           // [B][8], zero between launches
+    float2 *part_ml;         // [B][32][max_chunks]
+    float *part_o;           // [B][32][max_chunks][64]
+    int max_chunks;
+    uint16_t *out;           // [B][32][64]
+    int32_t *err;
+};
+
+constexpr int kStepStages = 4;
+constexpr int kMaxPersistentBatch = 512;
+
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_dependent_launch() { asm volatile("griddepcontrol.launch_dependents;" ::); }
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// Take a ticket: atomic increment with release and acquire semantics at GPU scope.
+__device__ __forceinline__ int ticket_acq_rel(int *counter)
+{
+    int t;
+    asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], 1;" : "=r"(t) : "l"(counter) : "memory");
+    return t;
+}
+
+__device__ __forceinline__ uint16_t bf16_bits(float x)
+{
+    const __nv_bfloat16 h = __float2bfloat16_rn(x);
+    return *reinterpret_cast<const uint16_t *>(&h);
+}
+
+__device__ __forceinline__ float bf16_value(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
+
+__device__ __forceinline__ bool length_ok(const StepArgs &a, int L)
+{
+    return L >= 1 && L <= a.max_blocks * kPage && L <= a.max_pos;
+}
+
+__device__ __forceinline__ int chunks_of(const StepArgs &a, int L)
+{
+    return ((L + kPage - 1) / kPage + a.pages_per_chunk - 1) / a.pages_per_chunk;
+}
+
+// All kThreads threads: the 4 query rows of group g rotated to position pos into
+// q_rot[4][64] (one pair per thread) and, for the sequence's last chunk, the new
+// token's rotated key row and its value row into new_kv[2][64].
+__device__ __forceinline__ void unit_rows(const StepArgs &a, int b, int g, int pos, bool last_chunk, uint16_t *q_rot,
+                                          uint16_t *new_kv)
+{
+    const int hl = threadIdx.x >> 5, i = threadIdx.x & 31;
+    const float2 cs = a.rope[(size_t)pos * (kD / 2) + i];
+    const uint16_t *qrow = a.q + ((size_t)b * kHq + g * kGroup + hl) * kD;
+    float y1, y2;
+    rope_rotate_pair(bf16_value(qrow[i]), bf16_value(qrow[i + kD / 2]), cs.x, cs.y, y1, y2);
+    q_rot[hl * kD + i] = bf16_bits(y1);
+    q_rot[hl * kD + i + kD / 2] = bf16_bits(y2);
+    if (last_chunk && hl == 0) {
+        const uint16_t *krow = a.k_new + ((size_t)b * kHkv + g) * kD;
+        rope_rotate_pair(bf16_value(krow[i]), bf16_value(krow[i + kD / 2]), cs.x, cs.y, y1, y2);
+        new_kv[i] = bf16_bits(y1);
+        new_kv[i + kD / 2] = bf16_bits(y2);
+    } else if (last_chunk && hl == 1) {
+        reinterpret_cast<uint32_t *>(new_kv + kD)[i] =
+            reinterpret_cast<const uint32_t *>(a.v_new + ((size_t)b * kHkv + g) * kD)[i];
+    }
+}
+
+// Threads 0..15: the appended token's K row and V row into their page slot.
+__device__ __forceinline__ void store_new_token(const StepArgs &a, int page, int g, int slot, const uint16_t *new_kv)
+{
+    const int part = threadIdx.x >> 3, ch = threadIdx.x & 7;  // part 0: K row, 1: V row
+    uint16_t *row = a.slab + (size_t)page * kPageElems + ((size_t)(part * kHkv + g) * kPage + slot) * kD;
+    reinterpret_cast<uint4 *>(row)[ch] = reinterpret_cast<const uint4 *>(new_kv + part * kD)[ch];
+}
+
+// The shared-memory copy of the last page carries the slot's previous contents:
+// lanes 0..15 overwrite it with the appended token (then the warp syncs).
+__device__ __forceinline__ void patch_stage(uint8_t *stage, int slot, const uint16_t *new_kv, int lane)
+{
+    if (lane < 16) {
+        const int part = lane >> 3, ch = lane & 7;
+        *reinterpret_cast<uint4 *>(stage + part * kTileBytes + swz(slot, ch)) =
+            reinterpret_cast<const uint4 *>(new_kv + part * kD)[ch];
+    }
+    __syncwarp();
+}
+
+// Zeros for the 4 heads of an invalid sequence (one (head, dim pair) per thread).
+__device__ __forceinline__ void write_zero_unit(const StepArgs &a, int b, int g)
+{
+    reinterpret_cast<uint32_t *>(a.out + ((size_t)b * kHq + g * kGroup + (threadIdx.x >> 5)) * kD)[threadIdx.x & 31] =
+        0u;
+    if (threadIdx.x == 0 && a.err)
+        atomicOr(a.err, PKV_DEVERR_LENGTH);
+}
+
+// Unit epilogue, all threads: combine the warps' states through `state`, then
+// write the output (single chunk) or publish the chunk partial and take a ticket;
+// the unit drawing the last ticket merges every chunk of (b, g) in chunk order,
+// writes the output and the rotated query rows, and resets the counter.
+template <class Warp>
+__device__ __forceinline__ void finish_unit(const StepArgs &a, Warp &w, float *state, int *ticket,
+                                            const uint16_t *q_rot, int b, int g, int c, int nchunks)
+{
+    const int tid = threadIdx.x, warp = tid >> 5;
+    __syncthreads();
+    w.store_state(state + warp * kStateFloats);
+    __syncthreads();
+    const int hl = tid >> 5, dp = tid & 31, h = g * kGroup + hl;
+    float M, lsum, o0, o1;
+    combine_warps(state, hl, dp, M, lsum, o0, o1);
+    uint32_t *out_row = reinterpret_cast<uint32_t *>(a.out + ((size_t)b * kHq + h) * kD);
+    uint32_t *q_row = reinterpret_cast<uint32_t *>(a.q + ((size_t)b * kHq + h) * kD);
+    const uint32_t q_word = reinterpret_cast<const uint32_t *>(q_rot + hl * kD)[dp];
+    if (nchunks == 1) {
+        out_row[dp] = finish_pair(o0, o1, lsum);
+        q_row[dp] = q_word;
+        return;
+    }
+    const size_t base = ((size_t)b * kHq + h) * a.max_chunks;
+    reinterpret_cast<float2 *>(a.part_o + (base + c) * kD)[dp] = make_float2(o0, o1);
+    if (dp == 0)
+        a.part_ml[base + c] = make_float2(M, lsum);
+    // publish: the CTA barrier orders every thread's partial stores before thread 0's
+    // release-acquire ticket; the acquire side plus the barrier orders the merging
+    // unit's loads after every other unit's partial stores
+    __syncthreads();
+    if (tid == 0)
+        *ticket = ticket_acq_rel(&a.counters[b * kHkv + g]);
+    __syncthreads();
+    if (*ticket != nchunks - 1)
+        return;
+    float Mx = -INFINITY;
+    for (int cc = 0; cc < nchunks; ++cc)
+        Mx = fmaxf(Mx, __ldcg(&a.part_ml[base + cc]).x);
+    float ls = 0.f, r0 = 0.f, r1 = 0.f;
+    if (Mx != -INFINITY) {
+        for (int cc = 0; cc < nchunks; ++cc) {
+            const float2 ml = __ldcg(&a.part_ml[base + cc]);
+            const float f = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - Mx);
+            const float2 oc = __ldcg(reinterpret_cast<const float2 *>(a.part_o + (base + cc) * kD) + dp);
+            ls = fmaf(f, ml.y, ls);
+            r0 = fmaf(f, oc.x, r0);
+            r1 = fmaf(f, oc.y, r1);
+        }
+    }
+    out_row[dp] = finish_pair(r0, r1, ls);
+    q_row[dp] = q_word;
+    if (tid == 0)
+        a.counters[b * kHkv + g] = 0;
+}
+
+// ------------------------------------------------------------------ grid schedule
+
+constexpr int kGridExtraBytes = kGroup * kD * 2 + 2 * kD * 2 + 16;  // rotated q rows, new K/V rows, ticket
+
+template <class Warp, int STAGES>
+__global__ void __launch_bounds__(kThreads) decode_step_kernel(const __grid_constant__ CUtensorMap tmap, StepArgs a)
+{
+    extern __shared__ uint8_t smem_raw[];
+    SmemLayout<STAGES> sm(smem_raw);
+    uint16_t *q_rot = reinterpret_cast<uint16_t *>(sm.extra);  // [4][64] rotated query rows
+    uint16_t *new_kv = q_rot + kGroup * kD;                     // [2][64] rotated key row, value row
+    int *ticket = reinterpret_cast<int *>(new_kv + 2 * kD);
+
+    const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int j0 = c * a.pages_per_chunk;
+    // the length and this chunk's table entries are fetched together (one round trip):
+    // entries inside the table row are always readable, whatever the length turns out to be
+    const int jcap = min(a.max_blocks - j0, a.pages_per_chunk);
+    const int ncap = warp < jcap ? (jcap - warp + kWarps - 1) / kWarps : 0;
+    int my_page = 0;
+    if (lane < ncap)
+        my_page = a.bt[(size_t)b * a.max_blocks + j0 + warp + lane * kWarps];
+    const int L = a.seq_lens[b];
+    if (!length_ok(a, L)) {
+        if (c == 0) {
+            grid_dependency_wait();
+            write_zero_unit(a, b, g);
+        }
+        return;
+    }
+    const int npages = (L + kPage - 1) / kPage;
+    const int nchunks = chunks_of(a, L);
+    if (c >= nchunks)
+        return;
+    const bool last_chunk = c == nchunks - 1;
+    const int jn = min(npages - j0, a.pages_per_chunk);
+    const int nmine = warp < jn ? (jn - warp + kWarps - 1) / kWarps : 0;
+    const bool bad = lane < nmine && (my_page < 0 || my_page >= a.num_pages);
+    const bool any_bad = __syncthreads_or(bad);  // the new token's page is one of the last chunk's pages
+
+    uint64_t *my_bars = sm.bars + warp * STAGES;
+    uint8_t *my_stages = sm.stages + warp * STAGES * kStageBytes;
+    const uint64_t policy = l2_evict_first_policy();
+    if (!any_bad) {
+        init_warp_barriers<STAGES>(my_bars, lane);
+        issue_prologue<STAGES>(&tmap, my_stages, my_bars, my_page, nmine, g, lane, policy);
+    }
+
+    grid_dependency_wait();  // q, k_new, v_new and every output belong to the dependency chain
+
+    const int pos = L - 1, slot = pos % kPage;
+    unit_rows(a, b, g, pos, last_chunk, q_rot, new_kv);
+    __syncthreads();
+    if (last_chunk && !any_bad && tid < 16)
+        store_new_token(a, a.bt[(size_t)b * a.max_blocks + npages - 1], g, slot, new_kv);
+    if (any_bad && tid == 0 && a.err)
+        atomicOr(a.err, PKV_DEVERR_PAGE_RANGE);
+
+    Warp w;
+    w.init(q_rot, a.scale_log2, lane, sm.scratch + warp * kScratchFloats);
+    if (!any_bad) {
+        const auto patch = [&](uint8_t *stage, int j) {
+            if (last_chunk && j == npages - 1)
+                patch_stage(stage, slot, new_kv, lane);
+        };
+        if (!consume_pages<STAGES>(&tmap, my_stages, my_bars, w, my_page, nmine, j0, warp, lane, L, g, policy,
+                                   patch) &&
+            lane == 0 && a.err)
+            atomicOr(a.err, PKV_DEVERR_TIMEOUT);
+    }
+    allow_dependent_launch();
+    // the stages are free now: they hold the combine area
+    finish_unit(a, w, reinterpret_cast<float *>(sm.stages), ticket, q_rot, b, g, c, nchunks);
+}
+
+
+// ------------------------------------------------------------------ persistent schedule
+
+struct UnitInfo {
+    int b, g, c, L, nchunks, npages, j0, jn;
+    bool valid;
+};
+
+// Unit r of the compact list.  prefix[b] is the first unit of sequence b, which owns
+// 8 * nchunks(b) units ordered (KV head, chunk); an invalid length owns 8 empty units.
+__device__ __forceinline__ UnitInfo decode_unit(const StepArgs &a, const int *prefix, int B, int r)
+{
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (prefix[mid] <= r)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    UnitInfo u;
+    u.b = lo;
+    u.nchunks = (prefix[lo + 1] - prefix[lo]) / kHkv;
+    const int rem = r - prefix[lo];
+    u.g = rem / u.nchunks;
+    u.c = rem - u.g * u.nchunks;
+    u.L = a.seq_lens[lo];
+    u.valid = length_ok(a, u.L);
+    u.npages = u.valid ? (u.L + kPage - 1) / kPage : 0;
+    u.j0 = u.c * a.pages_per_chunk;
+    u.jn = u.valid ? min(u.npages - u.j0, a.pages_per_chunk) : 0;
+    return u;
+}
+
+__device__ __forceinline__ int warp_pages(const UnitInfo &u, int warp)
+{
+    return warp < u.jn ? (u.jn - warp + kWarps - 1) / kWarps : 0;
+}
+
+template <int STAGES>
+constexpr int persistent_smem_bytes(int B)
+{
+    return SmemLayout<STAGES>::kBaseBytes + kWarps * kStateFloats * 4 + kGroup * kD * 2 + 2 * kD * 2 + 16 +
+           kWarps * STAGES * 4 + kWarps * 4 + (B + 1) * 4;
+}
+
+template <class Warp, int STAGES>
+__global__ void __launch_bounds__(kThreads)
+decode_step_persistent_kernel(const __grid_constant__ CUtensorMap tmap, StepArgs a, int B)
+{
+    extern __shared__ uint8_t smem_raw[];
+    SmemLayout<STAGES> sm(smem_raw);
+    float *state = reinterpret_cast<float *>(sm.extra);                  // [4 warps][kStateFloats]
+    uint16_t *q_rot = reinterpret_cast<uint16_t *>(state + kWarps * kStateFloats);  // [4][64]
+    uint16_t *new_kv = q_rot + kGroup * kD;                               // [2][64]
+    int *ticket = reinterpret_cast<int *>(new_kv + 2 * kD);              // [4]
+    int *stage_bad = ticket + 4;                                          // [4 warps][STAGES]
+    int *warp_sums = stage_bad + kWarps * STAGES;                         // [4 warps]
+    int *prefix = warp_sums + kWarps;                                     // [B + 1]
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    // ---- compact unit list: exclusive prefix sum over sequences (4 per thread)
+    int v[4], local = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int b = 4 * tid + i;
+        int n = 0;
+        if (b < B) {
+            const int L = a.seq_lens[b];
+            n = kHkv * (length_ok(a, L) ? chunks_of(a, L) : 1);
+        }
+        v[i] = n;
+        local += n;
+    }
+    int incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int t = __shfl_up_sync(kFull, incl, off);
+        if (lane >= off)
+            incl += t;
+    }
+    if (lane == 31)
+        warp_sums[warp] = incl;
+    __syncthreads();
+    int run = incl - local;
+    for (int ww = 0; ww < warp; ++ww)
+        run += warp_sums[ww];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if (4 * tid + i < B)
+            prefix[4 * tid + i] = run;
+        run += v[i];
+    }
+    if (tid == kThreads - 1)
+        prefix[B] = run;
+    __syncthreads();
+    const int R = prefix[B];
+    const int P = gridDim.x;
+    const int my_units = (int)blockIdx.x < R ? (R - 1 - (int)blockIdx.x) / P + 1 : 0;
+    if (my_units == 0)
+        return;
+
+    uint64_t *my_bars = sm.bars + warp * STAGES;
+    uint8_t *my_stages = sm.stages + warp * STAGES * kStageBytes;
+    int *my_bad = stage_bad + warp * STAGES;
+    init_warp_barriers<STAGES>(my_bars, lane);
+    const uint64_t policy = l2_evict_first_policy();
+
+    // ---- producer: walks this CTA's units ahead of the consumer, at most STAGES
+    //      pages ahead, across unit boundaries.  Lane k holds the page id of the
+    //      warp's k-th page of the unit being issued.
+    int p_i = 0;
+    UnitInfo pu = decode_unit(a, prefix, B, blockIdx.x);
+    int p_n = warp_pages(pu, warp), p_k = 0;
+    int p_id = lane < p_n ? a.bt[(size_t)pu.b * a.max_blocks + pu.j0 + warp + lane * kWarps] : 0;
+    uint32_t issued = 0, consumed = 0;
+    bool dead = false;  // a bounded wait gave up: stop streaming, keep the bookkeeping going
+    const auto produce = [&]() {
+        while (!dead && (int)(issued - consumed) < STAGES && p_i < my_units) {
+            if (p_k >= p_n) {
+                if (++p_i >= my_units)
+                    break;
+                pu = decode_unit(a, prefix, B, blockIdx.x + p_i * P);
+                p_n = warp_pages(pu, warp);
+                p_k = 0;
+                p_id = lane < p_n ? a.bt[(size_t)pu.b * a.max_blocks + pu.j0 + warp + lane * kWarps] : 0;
+                continue;
+            }
+            const int id = __shfl_sync(kFull, p_id, p_k);
+            const int s = issued % STAGES;
+            if (lane == 0) {
+                const bool ok = id >= 0 && id < a.num_pages;
+                my_bad[s] = ok ? 0 : 1;
+                if (ok) {
+                    fence_proxy_async_smem();
+                    mbar_arrive_expect_tx(&my_bars[s], kStageBytes);
+                    tma_load_page_head(my_stages + s * kStageBytes, &tmap, &my_bars[s], pu.g, id, policy);
+                } else {
+                    mbar_arrive(&my_bars[s]);  // completes the phase without a copy
+                }
+            }
+            __syncwarp();
+            ++issued;
+            ++p_k;
+        }
+    };
+    produce();
+
+    grid_dependency_wait();  // q, k_new, v_new and every output belong to the dependency chain
+
+    for (int i = 0; i < my_units; ++i) {
+        const UnitInfo u = decode_unit(a, prefix, B, blockIdx.x + i * P);
+        __syncthreads();  // the previous unit's epilogue no longer reads q_rot, new_kv, state
+        if (i == my_units - 1)
+            allow_dependent_launch();
+        if (!u.valid) {
+            write_zero_unit(a, u.b, u.g);
+            continue;
+        }
+        const int pos = u.L - 1, slot = pos % kPage;
+        const bool last_chunk = u.c == u.nchunks - 1;
+        unit_rows(a, u.b, u.g, pos, last_chunk, q_rot, new_kv);
+        __syncthreads();
+        if (last_chunk && tid < 16) {
+            const int page = a.bt[(size_t)u.b * a.max_blocks + u.npages - 1];
+            if (page >= 0 && page < a.num_pages)
+                store_new_token(a, page, u.g, slot, new_kv);
+        }
+        Warp w;
+        w.init(q_rot, a.scale_log2, lane, sm.scratch + warp * kScratchFloats);
+        const int n = warp_pages(u, warp);
+        for (int k = 0; k < n; ++k) {
+            const int s = consumed % STAGES;
+            const int j = u.j0 + warp + k * kWarps;
+            if (!dead && !mbar_wait_warp(&my_bars[s], (consumed / STAGES) & 1)) {
+                // give the other copies in flight a bounded chance to land, then stop
+                for (uint32_t kk = consumed + 1; kk < issued; ++kk)
+                    (void)mbar_wait_warp(&my_bars[kk % STAGES], (kk / STAGES) & 1);
+                dead = true;
+                if (lane == 0 && a.err)
+                    atomicOr(a.err, PKV_DEVERR_TIMEOUT);
+            }
+            if (!dead) {
+                uint8_t *stage = my_stages + s * kStageBytes;
+                if (my_bad[s]) {
+                    if (lane == 0 && a.err)
+                        atomicOr(a.err, PKV_DEVERR_PAGE_RANGE);
+                } else {
+                    if (last_chunk && j == u.npages - 1)
+                        patch_stage(stage, slot, new_kv, lane);
+                    w.page(stage, min(kPage, u.L - j * kPage));
+                }
+            }
+            __syncwarp();
+            ++consumed;
+            produce();
+        }
+        finish_unit(a, w, state, ticket, q_rot, u.b, u.g, u.c, u.nchunks);
+    }
+}
+
+// ------------------------------------------------------------------ launch
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+cudaLaunchAttribute pdl_attribute()
+{
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    return attr;
+}
+
+template <class Warp>
+int launch_grid(const CUtensorMap *tmap, const StepArgs &a, int B, cudaStream_t s, bool pdl)
+{
+    auto kernel = decode_step_kernel<Warp, kStepStages>;
+    constexpr int smem = SmemLayout<kStepStages>::kBaseBytes + kGridExtraBytes;
+    static bool attr_set = false;  // set once per process (before any graph capture)
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+            return PKV_ERR_CUDA;
+        attr_set = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.max_chunks, kHkv, B);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1] = {pdl_attribute()};
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return status_from_cuda(cudaLaunchKernelEx(&cfg, kernel, *tmap, a));
+}
+
+// CTAs per SM the persistent kernel is sized for, and the SM count, per device.
+struct PersistentShape {
+    int sms = 0;
+    int ctas_per_sm = 0;
+};
+
+template <class Warp>
+int launch_persistent(const CUtensorMap *tmap, const StepArgs &a, int B, cudaStream_t s, bool pdl)
+{
+    auto kernel = decode_step_persistent_kernel<Warp, kStepStages>;
+    constexpr int max_smem = persistent_smem_bytes<kStepStages>(kMaxPersistentBatch);
+    constexpr int kMaxDevices = 64;
+    static PersistentShape shape[kMaxDevices];  // filled on the first call per device (before any capture)
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return PKV_ERR_CUDA;
+    PersistentShape &ps = shape[dev];
+    if (ps.sms == 0) {
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem) != cudaSuccess ||
+            cudaDeviceGetAttribute(&ps.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ps.ctas_per_sm, kernel, kThreads, max_smem) !=
+                cudaSuccess ||
+            ps.ctas_per_sm < 1) {
+            ps.sms = 0;
+            return PKV_ERR_CUDA;
+        }
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(ps.sms * ps.ctas_per_sm);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = persistent_smem_bytes<kStepStages>(B);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1] = {pdl_attribute()};
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return status_from_cuda(cudaLaunchKernelEx(&cfg, kernel, *tmap, a, B));
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" size_t pkv_decode_step_workspace_bytes(int B, int max_blocks, int pages_per_chunk)
+{
+    using namespace pkv;
+    if (B < 1 || max_blocks < 1 || pages_per_chunk < 1)
+        return 0;
+    return align256((size_t)B * kHkv * sizeof(int)) + pkv_decode_workspace_bytes(B, max_blocks, pages_per_chunk);
+}
+
+extern "C" int pkv_decode_step(const pkv_pool *pool, const uint16_t *k_new, const uint16_t *v_new, uint16_t *q,
+                               const int32_t *bt_dev, int max_blocks, const int32_t *seq_lens_dev, int B,
+                               const float *rope_table, int max_pos, float scale, int pages_per_chunk,
+                               void *workspace, size_t workspace_bytes, uint16_t *out, int32_t *dev_err_flag,
+                               void *cuda_stream, int options)
+{
+    using namespace pkv;
+    if (!pool || !k_new || !v_new || !q || !bt_dev || !seq_lens_dev || !rope_table || !out || !workspace)
+        return PKV_ERR_INVALID_ARG;
+    if (B < 1 || B > 65535 || max_blocks < 1 || max_blocks > (1 << 20) || max_pos < 1)
+        return PKV_ERR_INVALID_ARG;
+    if (pages_per_chunk < 1 || pages_per_chunk > kMaxPagesPerChunk || !(scale > 0.f) || !(scale < INFINITY))
+        return PKV_ERR_INVALID_ARG;
+    const int variant = options & 0xff;
+    if (variant < PKV_DECODE_DEFAULT || variant > PKV_DECODE_MMA ||
+        (options & ~(0xff | PKV_STEP_NO_PDL | PKV_STEP_GRID | PKV_STEP_PERSISTENT)) ||
+        ((options & PKV_STEP_GRID) && (options & PKV_STEP_PERSISTENT)))
+        return PKV_ERR_INVALID_ARG;
+    if ((options & PKV_STEP_PERSISTENT) && B > kMaxPersistentBatch)
+        return PKV_ERR_INVALID_ARG;
+    const uintptr_t align = reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new) |
+                            reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out) |
+                            reinterpret_cast<uintptr_t>(rope_table) | reinterpret_cast<uintptr_t>(workspace);
+    if (align & 15u)
+        return PKV_ERR_INVALID_ARG;
+    if (workspace_bytes < pkv_decode_step_workspace_bytes(B, max_blocks, pages_per_chunk))
+        return PKV_ERR_WORKSPACE_TOO_SMALL;
+    const CUtensorMap *tmap = pool_tensor_map(pool);
+    if (!tmap)
+        return PKV_ERR_CUDA;
+    const int max_chunks = (max_blocks + pages_per_chunk - 1) / pages_per_chunk;
+    char *ws = static_cast<char *>(workspace);
+    const size_t counters_bytes = align256((size_t)B * kHkv * sizeof(int));
+    const size_t ml_bytes = align256((size_t)B * kHq * max_chunks * sizeof(float2));
+    StepArgs a;
+    a.num_pages = pool->num_pages;
+    a.slab = reinterpret_cast<uint16_t *>(pool->slab);
+    a.k_new = k_new;
+    a.v_new = v_new;
+    a.q = q;
+    a.bt = bt_dev;
+    a.max_blocks = max_blocks;
+    a.seq_lens = seq_lens_dev;
+    a.rope = reinterpret_cast<const float2 *>(rope_table);
+    a.max_pos = max_pos;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.pages_per_chunk = pages_per_chunk;
+    a.counters = reinterpret_cast<int *>(ws);
+    a.part_ml = reinterpret_cast<float2 *>(ws + counters_bytes);
+    a.part_o = reinterpret_cast<float *>(ws + counters_bytes + ml_bytes);
+    a.max_chunks = max_chunks;
+    a.out = out;
+    a.err = dev_err_flag;
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    const bool pdl = !(options & PKV_STEP_NO_PDL);
+    // the grid schedule is the measured default; the persistent one is chosen explicitly
+    const bool persistent = (options & PKV_STEP_PERSISTENT) != 0;
+    if (persistent)
+        return variant == PKV_DECODE_SIMT ? launch_persistent<SimtWarp>(tmap, a, B, s, pdl)
+                                          : launch_persistent<MmaWarp>(tmap, a, B, s, pdl);
+    return variant == PKV_DECODE_SIMT ? launch_grid<SimtWarp>(tmap, a, B, s, pdl)
+                                      : launch_grid<MmaWarp>(tmap, a, B, s, pdl);
+}

@@ -22,10 +22,14 @@ from . import pkv
 from . import workloads as wl
 
 
+SCHEDULES = {"auto": 0, "grid": pkv.PKV_STEP_GRID, "persistent": pkv.PKV_STEP_PERSISTENT}
+
+
 class DecodeEngine:
     def __init__(self, num_pages: int, layers: int, batch: int, max_blocks: int = wl.MAX_BLOCKS,
                  pages_per_chunk: int = 16, variant: int = pkv.PKV_DECODE_DEFAULT, max_pos: int = wl.MAX_CONTEXT,
-                 theta: float = wl.ROPE_THETA, pool_seed: int = 0, device: str = "cuda"):
+                 theta: float = wl.ROPE_THETA, pool_seed: int = 0, device: str = "cuda", fused: bool = True,
+                 pdl: bool = True, schedule: str = "auto"):
         self.device = torch.device(device)
         self.layers, self.batch, self.max_blocks = layers, batch, max_blocks
         self.pages_per_chunk, self.variant, self.max_pos = pages_per_chunk, variant, max_pos
@@ -38,6 +42,12 @@ class DecodeEngine:
         self.err = torch.zeros(1, dtype=torch.int32, device=self.device)
         self.ws_bytes = pkv.pkv_decode_workspace_bytes(batch, max_blocks, pages_per_chunk)
         self.workspace = torch.empty(max(self.ws_bytes, 16), dtype=torch.uint8, device=self.device)
+        # the fused step's workspace starts with per-(sequence, KV head) counters that
+        # must be zero before the first call (every call leaves them zero)
+        self.step_ws_bytes = pkv.pkv_decode_step_workspace_bytes(batch, max_blocks, pages_per_chunk)
+        self.step_ws = torch.zeros(self.step_ws_bytes, dtype=torch.uint8, device=self.device)
+        self.fused = fused
+        self.step_options = variant | (0 if pdl else pkv.PKV_STEP_NO_PDL) | SCHEDULES[schedule]
         self.bt = None
         self.bt_host = None
 
@@ -79,14 +89,29 @@ class DecodeEngine:
                                          self.scale, self.pages_per_chunk, self.workspace, self.ws_bytes, out,
                                          self.err, stream, self.variant if variant is None else variant)
 
+    def fused_layer(self, layer: int, q, k_new, v_new, seq_lens_dev, out, stream=None) -> None:
+        """Append + attention of one layer in one launch (positions are seq_lens - 1)."""
+        pkv.pkv_decode_step(self.pool, k_new, v_new, q, self.bt[layer], self.max_blocks, seq_lens_dev, self.batch,
+                            self.rope, self.max_pos, self.scale, self.pages_per_chunk, self.step_ws,
+                            self.step_ws_bytes, out, self.err, stream, self.step_options)
+
     def step(self, q, k_new, v_new, pos_dev, seq_lens_dev, out, stream=None, layer_hook=None) -> None:
         """One decode step over all layers.
 
         q: [layers][B][32][64] bf16 (rotated in place), k_new, v_new: [layers][B][8][64] bf16,
-        pos_dev, seq_lens_dev: [B] int32, out: [layers][B][32][64] bf16.
+        pos_dev, seq_lens_dev: [B] int32, out: [layers][B][32][64] bf16.  The fused path
+        (default) appends at seq_lens - 1 and ignores pos_dev; the separate path launches
+        pkv_append_rope at pos_dev then pkv_decode_attention.
         ``layer_hook(layer, phase)`` (optional) is called around each attention launch.
         """
         for layer in range(self.layers):
+            if self.fused:
+                if layer_hook:
+                    layer_hook(layer, "before")
+                self.fused_layer(layer, q[layer], k_new[layer], v_new[layer], seq_lens_dev, out[layer], stream)
+                if layer_hook:
+                    layer_hook(layer, "after")
+                continue
             self.append(layer, k_new[layer], v_new[layer], q[layer], pos_dev, stream)
             if layer_hook:
                 layer_hook(layer, "before")

@@ -40,13 +40,16 @@ PKV_DEVERR_TIMEOUT = 0x4
 PKV_DECODE_DEFAULT = 0
 PKV_DECODE_SIMT = 1
 PKV_DECODE_MMA = 2
+PKV_STEP_NO_PDL = 0x100
+PKV_STEP_GRID = 0x200
+PKV_STEP_PERSISTENT = 0x400
 
 # every symbol include/pkv.h declares
 EXPORTED = (
     "pkv_pool_create", "pkv_pool_destroy", "pkv_pool_alloc", "pkv_pool_free", "pkv_pool_info",
     "pkv_block_tables_build", "pkv_rope_table_init", "pkv_append_rope", "pkv_decode_workspace_bytes",
     "pkv_decode_attention", "pkv_decode_attention_variant", "pkv_decode_attention_noalloc",
-    "pkv_check_device_error",
+    "pkv_decode_step_workspace_bytes", "pkv_decode_step", "pkv_check_device_error",
     "pkv_status_string", "pkv_version",
 )
 
@@ -88,13 +91,18 @@ def lib():
     L.pkv_decode_attention_variant.argtypes = L.pkv_decode_attention.argtypes + [_i32]
     L.pkv_decode_attention_noalloc.argtypes = [_vp, _vp, _vp, _i32, _vp, _i32, ctypes.c_float, _i32, _vp, _vp,
                                                _vp]
+    L.pkv_decode_step_workspace_bytes.argtypes = [_i32, _i32, _i32]
+    L.pkv_decode_step_workspace_bytes.restype = ctypes.c_size_t
+    L.pkv_decode_step.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _vp, _i32, ctypes.c_float, _i32, _vp,
+                                  ctypes.c_size_t, _vp, _vp, _vp, _i32]
     L.pkv_check_device_error.argtypes = [_vp, _i32p, _vp]
     L.pkv_status_string.argtypes = [_i32]
     L.pkv_status_string.restype = ctypes.c_char_p
     L.pkv_version.argtypes = []
     L.pkv_version.restype = ctypes.c_char_p
     for name in EXPORTED:
-        if name not in ("pkv_decode_workspace_bytes", "pkv_status_string", "pkv_version"):
+        if name not in ("pkv_decode_workspace_bytes", "pkv_decode_step_workspace_bytes", "pkv_status_string",
+                        "pkv_version"):
             getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -225,6 +233,19 @@ def pkv_decode_attention_variant(pool, q, bt_dev, max_blocks: int, seq_lens_dev,
                                               int(workspace_bytes), _ptr(out), _ptr(dev_err_flag),
                                               _stream(stream), int(variant)),
            "pkv_decode_attention_variant")
+
+
+def pkv_decode_step_workspace_bytes(B: int, max_blocks: int, pages_per_chunk: int) -> int:
+    return int(lib().pkv_decode_step_workspace_bytes(B, max_blocks, pages_per_chunk))
+
+
+def pkv_decode_step(pool, k_new, v_new, q, bt_dev, max_blocks: int, seq_lens_dev, B: int, rope_table,
+                    max_pos: int, scale: float, pages_per_chunk: int, workspace, workspace_bytes: int, out,
+                    dev_err_flag=None, stream=None, options: int = PKV_DECODE_DEFAULT) -> None:
+    _check(lib().pkv_decode_step(pool, _ptr(k_new), _ptr(v_new), _ptr(q), _ptr(bt_dev), max_blocks,
+                                 _ptr(seq_lens_dev), B, _ptr(rope_table), max_pos, float(scale), pages_per_chunk,
+                                 _ptr(workspace), int(workspace_bytes), _ptr(out), _ptr(dev_err_flag),
+                                 _stream(stream), int(options)), "pkv_decode_step")
 
 
 PKV_NOALLOC_SCRATCH_BYTES = 32 << 20

@@ -1,0 +1,118 @@
+"""GPU parity of the fused per-layer step (pkv_decode_step).
+
+The fused kernel must produce bit-for-bit what pkv_append_rope (at seq_len - 1)
+followed by pkv_decode_attention produce -- the same pool bytes, the same rotated
+queries, the same outputs -- for both compute policies and every chunk size; and
+therefore match the oracle within the parity tolerance.  Its per-(sequence, KV
+head) counters must be back at zero after every call, and launching with or
+without programmatic dependent launch must not change a bit.
+"""
+import numpy as np
+import pytest
+import torch
+
+from paged_kv_decode_12_gb300 import pkv
+from paged_kv_decode_12_gb300.engine import DecodeEngine
+from tests.test_gpu_parity import RAGGED, VARIANTS, assert_close, dev_bf16, gpu_run, make_case, oracle_run, u16
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def native():
+    from paged_kv_decode_12_gb300 import _build
+
+    _build.build()
+    pkv.lib()
+
+
+SCHEDULES = ["grid", "persistent"]
+
+
+def fused_run(c, chunk=16, variant=pkv.PKV_DECODE_DEFAULT, pdl=True, seq_lens_override=None, repeats=1,
+              schedule="auto"):
+    eng = DecodeEngine(c["num_pages"], 1, c["B"], c["max_blocks"], chunk, variant, pdl=pdl, schedule=schedule)
+    eng.slab.copy_(torch.from_numpy(c["pool"].view(np.uint8)).cuda())
+    eng.set_tables(c["bt"][None])
+    lens = c["seq_lens"] if seq_lens_override is None else np.asarray(seq_lens_override, np.int32)
+    lens_d = torch.from_numpy(lens).cuda()
+    k_new, v_new = dev_bf16(c["k_new"]), dev_bf16(c["v_new"])
+    outs = []
+    for _ in range(repeats):
+        q = dev_bf16(c["q"])
+        out = torch.full((c["B"], 32, 64), 7.0, dtype=torch.bfloat16, device="cuda")
+        eng.fused_layer(0, q, k_new, v_new, lens_d, out)
+        outs.append(u16(out))
+    status, flag = eng.check_errors()
+    counters = eng.step_ws[: c["B"] * 8 * 4].view(torch.int32).cpu().numpy()
+    res = dict(pool=u16(eng.slab.view(torch.bfloat16)), q=u16(q), out=outs[-1], outs=outs, status=status,
+               flag=flag, counters=counters)
+    eng.close()
+    return res
+
+
+@pytest.mark.parametrize("schedule", SCHEDULES)
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("chunk", [1, 3, 16, 128])
+def test_fused_is_bit_identical_to_separate_calls(schedule, variant, chunk):
+    c = make_case(31, RAGGED, max_blocks=128)
+    f = fused_run(c, chunk=chunk, variant=variant, schedule=schedule)
+    s = gpu_run(c, chunk=chunk, variant=variant)
+    assert f["status"] == pkv.PKV_OK and f["flag"] == 0
+    assert np.array_equal(f["pool"], s["pool"])
+    assert np.array_equal(f["q"], s["q"])
+    assert np.array_equal(f["out"], s["out"])
+    assert np.all(f["counters"] == 0)
+
+
+@pytest.mark.parametrize("schedule", SCHEDULES)
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_fused_tiny_vs_oracle(schedule, variant):
+    c = make_case(12, [17, 40], num_pages=8)
+    f, o = fused_run(c, variant=variant, schedule=schedule), oracle_run(c)
+    assert_close(f["out"], o["out_f64"])
+
+
+@pytest.mark.parametrize("schedule", SCHEDULES)
+def test_fused_repeated_calls_and_pdl_switch(schedule):
+    c = make_case(32, [2048, 600, 1, 17, 999], max_blocks=128)
+    a = fused_run(c, chunk=8, repeats=3, schedule=schedule)
+    b = fused_run(c, chunk=8, pdl=False, schedule=schedule)
+    assert all(np.array_equal(o, a["outs"][0]) for o in a["outs"])
+    assert np.array_equal(a["out"], b["out"]) and np.array_equal(a["pool"], b["pool"])
+    assert np.all(a["counters"] == 0) and np.all(b["counters"] == 0)
+
+
+@pytest.mark.parametrize("schedule", SCHEDULES)
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_fused_bad_page_sets_flag_and_resets_counters(schedule, variant):
+    c = make_case(33, [300, 200, 64], max_blocks=32)
+    bad = c["bt"].copy()
+    bad[0, 3] = c["num_pages"] + 5
+    f = fused_run(dict(c, bt=bad), chunk=4, variant=variant, schedule=schedule)
+    assert f["status"] == pkv.PKV_ERR_DEVICE_BOUNDS and f["flag"] & pkv.PKV_DEVERR_PAGE_RANGE
+    assert np.all(f["counters"] == 0)
+    o = oracle_run(c)
+    assert_close(f["out"][1:], o["out_f64"][1:])          # untouched sequences stay right
+
+
+@pytest.mark.parametrize("schedule", SCHEDULES)
+def test_fused_zero_length_sets_flag_and_zeros(schedule):
+    c = make_case(34, [20, 30])
+    f = fused_run(c, seq_lens_override=[0, 30], schedule=schedule)
+    assert f["flag"] & pkv.PKV_DEVERR_LENGTH
+    assert np.all(f["out"][0] == 0)
+    assert_close(f["out"][1], oracle_run(c)["out_f64"][1])
+
+
+def test_persistent_many_units_per_cta():
+    # more units than CTAs (batch 300 > 152 SMs x 3 CTAs / 8 heads): every CTA walks
+    # several units, crossing unit boundaries with copies in flight
+    rng = np.random.default_rng(35)
+    lens = rng.integers(1, 300, size=300)
+    c = make_case(35, lens, max_blocks=64)
+    p = fused_run(c, chunk=2, schedule="persistent")
+    g = fused_run(c, chunk=2, schedule="grid")
+    assert p["status"] == pkv.PKV_OK and np.all(p["counters"] == 0)
+    assert np.array_equal(p["out"], g["out"]) and np.array_equal(p["pool"], g["pool"])
+    assert np.array_equal(p["q"], g["q"])
