@@ -55,6 +55,7 @@ VARIANTS = {"default": 0, "simt": 1, "mma": 2}
 # Pages per work unit, chosen per workload from a sweep of 8..128 (any fixed value keeps
 # results batch invariant: the chunking depends only on each sequence's own length).
 DEFAULT_CHUNK = {"b256": 128, "b64": 32, "b8": 16}
+DEFAULT_RING = {"b256": 4, "b64": 2, "b8": 2}   # TMA stages per warp (grid schedule), from the same sweep
 L2_BYTES = 129 * 10**6
 
 
@@ -245,7 +246,7 @@ def config_block(w, args, variant_name: str, graph: bool) -> dict:
             "seq_len_max": int(w.seq_lens.max()), "seq_len_mean": float(w.seq_lens.mean()),
             "pages_per_chunk": args.pages_per_chunk, "kernel_variant": variant_name, "cuda_graph": graph,
             "path": getattr(args, "path", "fused"), "pdl": not getattr(args, "no_pdl", False),
-            "schedule": getattr(args, "schedule", "auto"),
+            "schedule": getattr(args, "schedule", "auto"), "ring": getattr(args, "ring", 0),
             "kv_bytes_per_step": kv,
             "l2": f"inputs larger than L2 ({kv / 1e9:.2f} GB of KV per step vs {L2_BYTES / 1e6:.0f} MB L2), "
                   "no flush", "seed": args.seed}
@@ -302,7 +303,7 @@ def run_pkv(args):
     variant_name = args.variant
     dw = harness.setup(args.config, replica_seed(args.seed, rank), args.pages_per_chunk, VARIANTS[variant_name],
                        layers=args.layers, fused=args.path == "fused", pdl=not args.no_pdl,
-                       schedule=args.schedule)
+                       schedule=args.schedule, ring=args.ring)
     w = dw.w
     harness.warm(dw, 2)
     dw.reset_q()
@@ -454,6 +455,8 @@ def main(argv=None):
     ap.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
     ap.add_argument("--schedule", choices=["auto", "grid", "persistent"], default="auto",
                     help="fused path: one CTA per unit, or persistent CTAs walking the units")
+    ap.add_argument("--ring", type=int, default=None, choices=[2, 3, 4],
+                    help="grid schedule: TMA stages per warp (default: the measured best for the workload)")
     ap.add_argument("--seed", type=int, default=12)
     ap.add_argument("--layers", type=int, default=None, help="override the layer count (small profiling runs)")
     ap.add_argument("--steps-per-graph", type=int, default=25)
@@ -465,6 +468,8 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.pages_per_chunk is None:
         args.pages_per_chunk = DEFAULT_CHUNK[args.config]
+    if args.ring is None:
+        args.ring = DEFAULT_RING[args.config]
     if args.impl == "reference":
         return run_reference(args)
     return run_pkv(args)

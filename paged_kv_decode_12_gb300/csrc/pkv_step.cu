@@ -63,7 +63,8 @@ struct StepArgs {
     int32_t *err;
 };
 
-constexpr int kStepStages = 4;
+constexpr int kStepStages = 4;       // persistent schedule ring depth
+constexpr int kDefaultGridRing = 4;  // grid schedule ring depth unless the options choose one
 constexpr int kMaxPersistentBatch = 512;
 
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
@@ -499,11 +500,11 @@ cudaLaunchAttribute pdl_attribute()
     return attr;
 }
 
-template <class Warp>
+template <class Warp, int STAGES>
 int launch_grid(const CUtensorMap *tmap, const StepArgs &a, int B, cudaStream_t s, bool pdl)
 {
-    auto kernel = decode_step_kernel<Warp, kStepStages>;
-    constexpr int smem = SmemLayout<kStepStages>::kBaseBytes + kGridExtraBytes;
+    auto kernel = decode_step_kernel<Warp, STAGES>;
+    constexpr int smem = SmemLayout<STAGES>::kBaseBytes + kGridExtraBytes;
     static bool attr_set = false;  // set once per process (before any graph capture)
     if (!attr_set) {
         if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
@@ -519,6 +520,17 @@ int launch_grid(const CUtensorMap *tmap, const StepArgs &a, int B, cudaStream_t 
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
     return status_from_cuda(cudaLaunchKernelEx(&cfg, kernel, *tmap, a));
+}
+
+// Ring depth per warp: 2 stages (36 KB per CTA, 6 CTAs per SM), 3 (4 per SM) or 4 (3 per SM).
+template <class Warp>
+int launch_grid_depth(const CUtensorMap *tmap, const StepArgs &a, int B, cudaStream_t s, bool pdl, int depth)
+{
+    switch (depth) {
+    case 2: return launch_grid<Warp, 2>(tmap, a, B, s, pdl);
+    case 3: return launch_grid<Warp, 3>(tmap, a, B, s, pdl);
+    default: return launch_grid<Warp, 4>(tmap, a, B, s, pdl);
+    }
 }
 
 // CTAs per SM the persistent kernel is sized for, and the SM count, per device.
@@ -585,7 +597,7 @@ extern "C" int pkv_decode_step(const pkv_pool *pool, const uint16_t *k_new, cons
         return PKV_ERR_INVALID_ARG;
     const int variant = options & 0xff;
     if (variant < PKV_DECODE_DEFAULT || variant > PKV_DECODE_MMA ||
-        (options & ~(0xff | PKV_STEP_NO_PDL | PKV_STEP_GRID | PKV_STEP_PERSISTENT)) ||
+        (options & ~(0xff | PKV_STEP_NO_PDL | PKV_STEP_GRID | PKV_STEP_PERSISTENT | PKV_STEP_RING_MASK)) ||
         ((options & PKV_STEP_GRID) && (options & PKV_STEP_PERSISTENT)))
         return PKV_ERR_INVALID_ARG;
     if ((options & PKV_STEP_PERSISTENT) && B > kMaxPersistentBatch)
@@ -630,6 +642,10 @@ extern "C" int pkv_decode_step(const pkv_pool *pool, const uint16_t *k_new, cons
     if (persistent)
         return variant == PKV_DECODE_SIMT ? launch_persistent<SimtWarp>(tmap, a, B, s, pdl)
                                           : launch_persistent<MmaWarp>(tmap, a, B, s, pdl);
-    return variant == PKV_DECODE_SIMT ? launch_grid<SimtWarp>(tmap, a, B, s, pdl)
-                                      : launch_grid<MmaWarp>(tmap, a, B, s, pdl);
+    const int ring = (options & PKV_STEP_RING_MASK) >> 12;
+    if (ring != 0 && (ring < 2 || ring > 4))
+        return PKV_ERR_INVALID_ARG;
+    const int depth = ring ? ring : kDefaultGridRing;
+    return variant == PKV_DECODE_SIMT ? launch_grid_depth<SimtWarp>(tmap, a, B, s, pdl, depth)
+                                      : launch_grid_depth<MmaWarp>(tmap, a, B, s, pdl, depth);
 }

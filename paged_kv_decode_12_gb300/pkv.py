@@ -43,6 +43,11 @@ PKV_DECODE_MMA = 2
 PKV_STEP_NO_PDL = 0x100
 PKV_STEP_GRID = 0x200
 PKV_STEP_PERSISTENT = 0x400
+PKV_STEP_RING_MASK = 0xF000
+
+
+def PKV_STEP_RING(n: int) -> int:
+    return n << 12
 
 # every symbol include/pkv.h declares
 EXPORTED = (

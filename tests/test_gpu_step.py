@@ -30,8 +30,9 @@ SCHEDULES = ["grid", "persistent"]
 
 
 def fused_run(c, chunk=16, variant=pkv.PKV_DECODE_DEFAULT, pdl=True, seq_lens_override=None, repeats=1,
-              schedule="auto"):
-    eng = DecodeEngine(c["num_pages"], 1, c["B"], c["max_blocks"], chunk, variant, pdl=pdl, schedule=schedule)
+              schedule="auto", ring=0):
+    eng = DecodeEngine(c["num_pages"], 1, c["B"], c["max_blocks"], chunk, variant, pdl=pdl, schedule=schedule,
+                       ring=ring)
     eng.slab.copy_(torch.from_numpy(c["pool"].view(np.uint8)).cuda())
     eng.set_tables(c["bt"][None])
     lens = c["seq_lens"] if seq_lens_override is None else np.asarray(seq_lens_override, np.int32)
@@ -103,6 +104,15 @@ def test_fused_zero_length_sets_flag_and_zeros(schedule):
     assert f["flag"] & pkv.PKV_DEVERR_LENGTH
     assert np.all(f["out"][0] == 0)
     assert_close(f["out"][1], oracle_run(c)["out_f64"][1])
+
+
+@pytest.mark.parametrize("ring", [2, 3])
+def test_ring_depth_changes_no_bit(ring):
+    c = make_case(36, RAGGED, max_blocks=128)
+    a = fused_run(c, chunk=8)
+    b = fused_run(c, chunk=8, ring=ring)
+    assert np.array_equal(a["out"], b["out"]) and np.array_equal(a["pool"], b["pool"])
+    assert np.array_equal(a["q"], b["q"]) and np.all(b["counters"] == 0)
 
 
 def test_persistent_many_units_per_cta():
