@@ -453,7 +453,7 @@ def main(argv=None):
     ap.add_argument("--path", choices=["fused", "separate"], default="fused",
                     help="one fused kernel per layer, or append + split + merge launches")
     ap.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
-    ap.add_argument("--schedule", choices=["auto", "grid", "persistent"], default="auto",
+    ap.add_argument("--schedule", choices=["auto", "grid", "persistent", "ws"], default="auto",
                     help="fused path: one CTA per unit, or persistent CTAs walking the units")
     ap.add_argument("--ring", type=int, default=None, choices=[2, 3, 4],
                     help="grid schedule: TMA stages per warp (default: the measured best for the workload)")

@@ -210,13 +210,15 @@ int pkv_decode_attention_variant(const pkv_pool *pool, const uint16_t *q, const 
 #define PKV_STEP_NO_PDL 0x100     /* launch without programmatic dependent launch */
 #define PKV_STEP_GRID 0x200       /* one CTA per (sequence, KV head, chunk) */
 #define PKV_STEP_PERSISTENT 0x400 /* a few CTAs per SM walk the units (B <= 512) */
+#define PKV_STEP_WS 0x800         /* warp-specialised: a producer warp streams, 4 consumer warps compute (B <= 512) */
 /* grid schedule: TMA ring depth per warp, 2..4 stages of 4 KiB (0 = library default).
  * Fewer stages mean less shared memory per CTA and more CTAs resident per SM. */
 #define PKV_STEP_RING(n) ((n) << 12)
 #define PKV_STEP_RING_MASK 0xf000
 
 /* Bytes of device workspace pkv_decode_step needs (a per-(sequence, KV head)
- * counter array followed by the chunk partials). */
+ * counter array and two work-distribution counters, followed by the chunk
+ * partials). */
 size_t pkv_decode_step_workspace_bytes(int B, int max_blocks, int pages_per_chunk);
 
 /* One layer of the decode step in ONE kernel launch: pkv_append_rope with

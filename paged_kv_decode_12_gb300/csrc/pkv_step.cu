@@ -158,14 +158,24 @@ __device__ __forceinline__ void write_zero_unit(const StepArgs &a, int b, int g)
 // write the output (single chunk) or publish the chunk partial and take a ticket;
 // the unit drawing the last ticket merges every chunk of (b, g) in chunk order,
 // writes the output and the rotated query rows, and resets the counter.
-template <class Warp>
+struct CtaSync {
+    __device__ __forceinline__ void operator()() const { __syncthreads(); }
+};
+
+// The 4 consumer warps only (named barrier 1), for kernels with a producer warp.
+struct ConsumerSync {
+    __device__ __forceinline__ void operator()() const { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+};
+
+template <class Warp, class Sync = CtaSync>
 __device__ __forceinline__ void finish_unit(const StepArgs &a, Warp &w, float *state, int *ticket,
-                                            const uint16_t *q_rot, int b, int g, int c, int nchunks)
+                                            const uint16_t *q_rot, int b, int g, int c, int nchunks,
+                                            Sync sync = Sync())
 {
     const int tid = threadIdx.x, warp = tid >> 5;
-    __syncthreads();
+    sync();
     w.store_state(state + warp * kStateFloats);
-    __syncthreads();
+    sync();
     const int hl = tid >> 5, dp = tid & 31, h = g * kGroup + hl;
     float M, lsum, o0, o1;
     combine_warps(state, hl, dp, M, lsum, o0, o1);
@@ -184,10 +194,10 @@ __device__ __forceinline__ void finish_unit(const StepArgs &a, Warp &w, float *s
     // publish: the CTA barrier orders every thread's partial stores before thread 0's
     // release-acquire ticket; the acquire side plus the barrier orders the merging
     // unit's loads after every other unit's partial stores
-    __syncthreads();
+    sync();
     if (tid == 0)
         *ticket = ticket_acq_rel(&a.counters[b * kHkv + g]);
-    __syncthreads();
+    sync();
     if (*ticket != nchunks - 1)
         return;
     float Mx = -INFINITY;
@@ -223,7 +233,9 @@ __global__ void __launch_bounds__(kThreads) decode_step_kernel(const __grid_cons
     uint16_t *new_kv = q_rot + kGroup * kD;                     // [2][64] rotated key row, value row
     int *ticket = reinterpret_cast<int *>(new_kv + 2 * kD);
 
-    const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    // chunk index slowest: every first chunk is dispatched before any later one, so the
+    // CTAs left empty by short sequences come last
+    const int g = blockIdx.x, b = blockIdx.y, c = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int j0 = c * a.pages_per_chunk;
     // the length and this chunk's table entries are fetched together (one round trip):
@@ -488,6 +500,341 @@ decode_step_persistent_kernel(const __grid_constant__ CUtensorMap tmap, StepArgs
     }
 }
 
+// ------------------------------------------------------------------ warp-specialised schedule
+//
+// Per CTA, 4 consumer warps (threads 0..127) and one producer warp (128..159); 2 CTAs
+// per SM.  The producer walks the compact unit list -- the CTA's first unit is
+// blockIdx.x, every further one is drawn from a work counter after the dependency
+// wait -- and for each unit posts a descriptor (the unit's raw query rows, new key
+// and value rows and RoPE row, fetched by 1-D bulk copies) and streams the unit's
+// pages into a CTA-wide ring of kWsRing stages with full/empty mbarriers.  Consumers
+// read a unit's inputs from shared memory only; their epilogue (combine, ticket,
+// merge) overlaps the producer's copies of the next units.  The last CTA to finish
+// resets the work counter, so the workspace counters are zero between launches.
+// A unit's descriptor is posted before any of its pages beyond the first ring-full,
+// so the consumers can always drain the ring (no circular wait).
+
+constexpr int kWsRing = 24;
+constexpr int kWsUnitSlots = 4;
+constexpr int kWsThreads = kThreads + 32;
+
+struct WsDesc {
+    int b, g, c, L, nchunks, j0, jn, first, new_page, valid, end, pad[5];  // 64 B
+    uint16_t q[kGroup * kD];  // raw query rows of the group (512 B)
+    uint16_t k[kD];           // new key row, not yet rotated (128 B)
+    uint16_t v[kD];           // new value row (128 B)
+    float2 rope[kD / 2];      // (cos, sin) at position L-1 (256 B)
+};
+constexpr uint32_t kWsDescCopyBytes = kGroup * kD * 2 + kD * 2 + kD * 2 + (kD / 2) * 8;
+static_assert(sizeof(WsDesc) == 64 + kWsDescCopyBytes && sizeof(WsDesc) % 16 == 0, "descriptor layout");
+
+constexpr int ws_smem_bytes(int B)
+{
+    return 1024 + kWsRing * kStageBytes + (2 * kWsRing + 2 * kWsUnitSlots) * 8 + kWsRing * 4 +
+           kWsUnitSlots * (int)sizeof(WsDesc) + kWarps * kStateFloats * 4 + kWarps * kScratchFloats * 4 +
+           kGroup * kD * 2 + 2 * kD * 2 + 16 + (kWarps + 1) * 4 + (B + 1) * 4;
+}
+
+__device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_addr(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_addr(bar))
+                 : "memory");
+}
+
+// OR of a predicate over the 128 consumer threads (named barrier 1).
+__device__ __forceinline__ bool consumer_any(bool p)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\t"
+        "setp.ne.u32 pi, %1, 0;\n\t"
+        "bar.red.or.pred po, 1, 128, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)p)
+        : "memory");
+    return r != 0;
+}
+
+template <class Warp>
+__global__ void __launch_bounds__(kWsThreads)
+decode_step_ws_kernel(const __grid_constant__ CUtensorMap tmap, StepArgs a, int B, int *work_counter, int *exit_counter)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(ring + kWsRing * kStageBytes);
+    uint64_t *empty = full + kWsRing;
+    uint64_t *ufull = empty + kWsRing;
+    uint64_t *uempty = ufull + kWsUnitSlots;
+    int *bad = reinterpret_cast<int *>(uempty + kWsUnitSlots);
+    WsDesc *desc = reinterpret_cast<WsDesc *>(bad + kWsRing);
+    float *state = reinterpret_cast<float *>(desc + kWsUnitSlots);
+    float *scratch = state + kWarps * kStateFloats;
+    uint16_t *q_rot = reinterpret_cast<uint16_t *>(scratch + kWarps * kScratchFloats);
+    uint16_t *new_kv = q_rot + kGroup * kD;
+    int *ticket = reinterpret_cast<int *>(new_kv + 2 * kD);
+    int *warp_sums = ticket + 4;
+    int *prefix = warp_sums + kWarps + 1;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    // ---- compact unit list (as the persistent schedule), 4 sequences per thread
+    {
+        int v[4], local = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int b = 4 * tid + i;
+            int n = 0;
+            if (b < B) {
+                const int L = a.seq_lens[b];
+                n = kHkv * (length_ok(a, L) ? chunks_of(a, L) : 1);
+            }
+            v[i] = n;
+            local += n;
+        }
+        int incl = local;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int t = __shfl_up_sync(kFull, incl, off);
+            if (lane >= off)
+                incl += t;
+        }
+        if (lane == 31)
+            warp_sums[warp] = incl;
+        if (tid == 0) {
+            for (int s = 0; s < kWsRing; ++s) {
+                mbar_init(&full[s], 1);
+                mbar_init(&empty[s], 1);
+            }
+            for (int s = 0; s < kWsUnitSlots; ++s) {
+                mbar_init(&ufull[s], 1);
+                mbar_init(&uempty[s], 1);
+            }
+            fence_barrier_init();
+        }
+        __syncthreads();
+        int run = incl - local;
+        for (int ww = 0; ww < warp; ++ww)
+            run += warp_sums[ww];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if (4 * tid + i < B)
+                prefix[4 * tid + i] = run;
+            run += v[i];
+        }
+        if (tid == kWsThreads - 1)
+            prefix[B] = run;
+        __syncthreads();
+    }
+    const int R = prefix[B];
+
+    if (warp == kWarps) {
+        // ================================================================ producer
+        const uint64_t policy = l2_evict_first_policy();
+        int r = blockIdx.x;
+        uint32_t G = 0, ui = 0;
+        bool waited = false, dead = false;
+        for (;;) {
+            const int us = ui % kWsUnitSlots;
+            if (ui >= kWsUnitSlots && !dead &&
+                !mbar_wait_warp(&uempty[us], ((ui / kWsUnitSlots) - 1) & 1))
+                dead = true;
+            WsDesc *d = desc + us;
+            if (r >= R || dead) {
+                if (!waited)
+                    grid_dependency_wait();
+                if (lane == 0) {
+                    d->end = 1;
+                    mbar_arrive(&ufull[us]);
+                }
+                break;
+            }
+            const UnitInfo u = decode_unit(a, prefix, B, r);
+            int id[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int k = lane + 32 * i;
+                id[i] = k < u.jn ? a.bt[(size_t)u.b * a.max_blocks + u.j0 + k] : 0;
+            }
+            const auto page_id = [&](int k) {
+                const int i = k >> 5;
+                const int mine = i == 0 ? id[0] : i == 1 ? id[1] : i == 2 ? id[2] : id[3];
+                return __shfl_sync(kFull, mine, k & 31);
+            };
+            // Issue pages k .. k+n-1 (n <= 4) from lanes 0..n-1.  A stage is reused only
+            // after its consumer released it (empty barrier, acquire after release); the
+            // consumers' reads need no proxy fence before the copy overwrites them.
+            const auto issue_pages = [&](int k, int n) {
+                for (int i = 0; i < n; ++i) {
+                    const uint32_t gi = G + i;
+                    if (gi >= kWsRing && !dead &&
+                        !mbar_wait_warp(&empty[gi % kWsRing], ((gi / kWsRing) - 1) & 1))
+                        dead = true;
+                }
+                // k is a multiple of 4, so pages k..k+3 share one 32-entry register block
+                const int reg = k >> 5;
+                const int mine = reg == 0 ? id[0] : reg == 1 ? id[1] : reg == 2 ? id[2] : id[3];
+                const int pid = __shfl_sync(kFull, mine, (k & 31) + (lane & 3));
+                if (lane < n) {
+                    const int s = (G + lane) % kWsRing;
+                    const bool ok = pid >= 0 && pid < a.num_pages && !dead;
+                    bad[s] = ok ? 0 : 1;
+                    if (ok) {
+                        mbar_arrive_expect_tx(&full[s], kStageBytes);
+                        tma_load_page_head(ring + s * kStageBytes, &tmap, &full[s], u.g, pid, policy);
+                    } else {
+                        mbar_arrive(&full[s]);
+                    }
+                }
+                __syncwarp();
+                G += n;
+            };
+            const uint32_t first = G;
+            int k = 0;
+            if (!waited) {
+                // before the dependency wait: only this layer's cached pages, at most one ring-full
+                const int pre = min(u.jn, kWsRing);
+                for (; k < pre; k += 4)
+                    issue_pages(k, min(4, pre - k));
+                grid_dependency_wait();
+                waited = true;
+            }
+            // the unit's descriptor, then its remaining pages
+            const int new_page = (u.valid && u.c == u.nchunks - 1 && u.jn > 0) ? page_id(u.jn - 1) : -1;
+            if (lane == 0) {
+                d->b = u.b;
+                d->g = u.g;
+                d->c = u.c;
+                d->L = u.L;
+                d->nchunks = u.nchunks;
+                d->j0 = u.j0;
+                d->jn = u.jn;
+                d->first = (int)first;
+                d->new_page = new_page;
+                d->valid = u.valid ? 1 : 0;
+                d->end = 0;
+                if (u.valid) {
+                    fence_proxy_async_smem();
+                    mbar_arrive_expect_tx(&ufull[us], kWsDescCopyBytes);
+                    bulk_copy_g2s(d->q, a.q + ((size_t)u.b * kHq + u.g * kGroup) * kD, kGroup * kD * 2, &ufull[us]);
+                    bulk_copy_g2s(d->k, a.k_new + ((size_t)u.b * kHkv + u.g) * kD, kD * 2, &ufull[us]);
+                    bulk_copy_g2s(d->v, a.v_new + ((size_t)u.b * kHkv + u.g) * kD, kD * 2, &ufull[us]);
+                    bulk_copy_g2s(d->rope, a.rope + (size_t)(u.L - 1) * (kD / 2), (kD / 2) * 8, &ufull[us]);
+                } else {
+                    mbar_arrive(&ufull[us]);
+                }
+            }
+            int nxt = 0;
+            if (lane == 0)
+                nxt = (int)gridDim.x + atomicAdd(work_counter, 1);
+            for (; k < u.jn; k += 4)
+                issue_pages(k, min(4, u.jn - k));
+            r = __shfl_sync(kFull, nxt, 0);
+            ++ui;
+        }
+        allow_dependent_launch();
+    } else {
+        // ================================================================ consumers
+        const ConsumerSync csync;
+        uint32_t ui = 0;
+        bool dead = false, waited = false;
+        for (;;) {
+            const int us = ui % kWsUnitSlots;
+            csync();  // the previous unit's epilogue no longer reads q_rot, new_kv, state
+            const bool timed_out = !mbar_wait_warp(&ufull[us], (ui / kWsUnitSlots) & 1);
+            if (consumer_any(timed_out)) {
+                if (tid == 0 && a.err)
+                    atomicOr(a.err, PKV_DEVERR_TIMEOUT);
+                break;
+            }
+            const WsDesc *d = desc + us;
+            if (d->end)
+                break;
+            if (!waited) {
+                grid_dependency_wait();
+                waited = true;
+            }
+            const int b = d->b, g = d->g, c = d->c, L = d->L, nchunks = d->nchunks, j0 = d->j0, jn = d->jn;
+            const int first = d->first, new_page = d->new_page;
+            if (!d->valid) {
+                csync();
+                if (tid == 0)
+                    mbar_arrive(&uempty[us]);
+                write_zero_unit(a, b, g);
+                ++ui;
+                continue;
+            }
+            const int pos = L - 1, slot = pos % kPage, npages = (L + kPage - 1) / kPage;
+            const bool last_chunk = c == nchunks - 1;
+            {
+                const int hl = tid >> 5, i = tid & 31;
+                const float2 cs = d->rope[i];
+                float y1, y2;
+                rope_rotate_pair(bf16_value(d->q[hl * kD + i]), bf16_value(d->q[hl * kD + i + kD / 2]), cs.x, cs.y,
+                                 y1, y2);
+                q_rot[hl * kD + i] = bf16_bits(y1);
+                q_rot[hl * kD + i + kD / 2] = bf16_bits(y2);
+                if (last_chunk && hl == 0) {
+                    rope_rotate_pair(bf16_value(d->k[i]), bf16_value(d->k[i + kD / 2]), cs.x, cs.y, y1, y2);
+                    new_kv[i] = bf16_bits(y1);
+                    new_kv[i + kD / 2] = bf16_bits(y2);
+                } else if (last_chunk && hl == 1) {
+                    reinterpret_cast<uint32_t *>(new_kv + kD)[i] = reinterpret_cast<const uint32_t *>(d->v)[i];
+                }
+            }
+            csync();
+            if (tid == 0)
+                mbar_arrive(&uempty[us]);  // the descriptor is consumed
+            if (last_chunk && tid < 16 && new_page >= 0 && new_page < a.num_pages)
+                store_new_token(a, new_page, g, slot, new_kv);
+            Warp w;
+            w.init(q_rot, a.scale_log2, lane, scratch + warp * kScratchFloats);
+            for (int k = warp; k < jn; k += kWarps) {
+                const uint32_t gi = (uint32_t)first + k;
+                const int s = gi % kWsRing;
+                if (!dead && !mbar_wait_warp(&full[s], (gi / kWsRing) & 1)) {
+                    dead = true;
+                    if (lane == 0 && a.err)
+                        atomicOr(a.err, PKV_DEVERR_TIMEOUT);
+                }
+                if (!dead) {
+                    uint8_t *stage = ring + s * kStageBytes;
+                    if (bad[s]) {
+                        if (lane == 0 && a.err)
+                            atomicOr(a.err, PKV_DEVERR_PAGE_RANGE);
+                    } else {
+                        const int j = j0 + k;
+                        const bool patched = last_chunk && j == npages - 1;
+                        if (patched)
+                            patch_stage(stage, slot, new_kv, lane);
+                        w.page(stage, min(kPage, L - j * kPage));
+                        if (patched)  // generic stores into the stage precede the next copy into it
+                            fence_proxy_async_smem();
+                    }
+                }
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&empty[s]);
+            }
+            finish_unit(a, w, state, ticket, q_rot, b, g, c, nchunks, csync);
+            ++ui;
+        }
+    }
+
+    // ---- the last CTA to finish resets the work counter for the next launch
+    __syncthreads();
+    if (tid == 0) {
+        grid_dependency_wait();
+        __threadfence();
+        if (atomicAdd(exit_counter, 1) == (int)gridDim.x - 1) {
+            atomicExch(work_counter, 0);
+            atomicExch(exit_counter, 0);
+        }
+    }
+}
+
 // ------------------------------------------------------------------ launch
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -512,7 +859,7 @@ int launch_grid(const CUtensorMap *tmap, const StepArgs &a, int B, cudaStream_t 
         attr_set = true;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(a.max_chunks, kHkv, B);
+    cfg.gridDim = dim3(kHkv, B, a.max_chunks);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
@@ -571,6 +918,39 @@ int launch_persistent(const CUtensorMap *tmap, const StepArgs &a, int B, cudaStr
     return status_from_cuda(cudaLaunchKernelEx(&cfg, kernel, *tmap, a, B));
 }
 
+template <class Warp>
+int launch_ws(const CUtensorMap *tmap, const StepArgs &a, int B, cudaStream_t s, bool pdl)
+{
+    auto kernel = decode_step_ws_kernel<Warp>;
+    constexpr int max_smem = ws_smem_bytes(kMaxPersistentBatch);
+    constexpr int kMaxDevices = 64;
+    static PersistentShape shape[kMaxDevices];  // filled on the first call per device (before any capture)
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return PKV_ERR_CUDA;
+    PersistentShape &ps = shape[dev];
+    if (ps.sms == 0) {
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem) != cudaSuccess ||
+            cudaDeviceGetAttribute(&ps.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ps.ctas_per_sm, kernel, kWsThreads, max_smem) !=
+                cudaSuccess ||
+            ps.ctas_per_sm < 1) {
+            ps.sms = 0;
+            return PKV_ERR_CUDA;
+        }
+    }
+    int *work_counter = a.counters + (size_t)B * kHkv;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(ps.sms * ps.ctas_per_sm);
+    cfg.blockDim = dim3(kWsThreads);
+    cfg.dynamicSmemBytes = ws_smem_bytes(B);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1] = {pdl_attribute()};
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return status_from_cuda(cudaLaunchKernelEx(&cfg, kernel, *tmap, a, B, work_counter, work_counter + 1));
+}
+
 }  // namespace
 }  // namespace pkv
 
@@ -579,7 +959,7 @@ extern "C" size_t pkv_decode_step_workspace_bytes(int B, int max_blocks, int pag
     using namespace pkv;
     if (B < 1 || max_blocks < 1 || pages_per_chunk < 1)
         return 0;
-    return align256((size_t)B * kHkv * sizeof(int)) + pkv_decode_workspace_bytes(B, max_blocks, pages_per_chunk);
+    return align256(((size_t)B * kHkv + 2) * sizeof(int)) + pkv_decode_workspace_bytes(B, max_blocks, pages_per_chunk);
 }
 
 extern "C" int pkv_decode_step(const pkv_pool *pool, const uint16_t *k_new, const uint16_t *v_new, uint16_t *q,
@@ -597,10 +977,11 @@ extern "C" int pkv_decode_step(const pkv_pool *pool, const uint16_t *k_new, cons
         return PKV_ERR_INVALID_ARG;
     const int variant = options & 0xff;
     if (variant < PKV_DECODE_DEFAULT || variant > PKV_DECODE_MMA ||
-        (options & ~(0xff | PKV_STEP_NO_PDL | PKV_STEP_GRID | PKV_STEP_PERSISTENT | PKV_STEP_RING_MASK)) ||
-        ((options & PKV_STEP_GRID) && (options & PKV_STEP_PERSISTENT)))
+        (options & ~(0xff | PKV_STEP_NO_PDL | PKV_STEP_GRID | PKV_STEP_PERSISTENT | PKV_STEP_WS |
+                     PKV_STEP_RING_MASK)) ||
+        (!!(options & PKV_STEP_GRID) + !!(options & PKV_STEP_PERSISTENT) + !!(options & PKV_STEP_WS) > 1))
         return PKV_ERR_INVALID_ARG;
-    if ((options & PKV_STEP_PERSISTENT) && B > kMaxPersistentBatch)
+    if ((options & (PKV_STEP_PERSISTENT | PKV_STEP_WS)) && B > kMaxPersistentBatch)
         return PKV_ERR_INVALID_ARG;
     const uintptr_t align = reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new) |
                             reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out) |
@@ -613,8 +994,10 @@ extern "C" int pkv_decode_step(const pkv_pool *pool, const uint16_t *k_new, cons
     if (!tmap)
         return PKV_ERR_CUDA;
     const int max_chunks = (max_blocks + pages_per_chunk - 1) / pages_per_chunk;
+    if (max_chunks > 65535)  // the grid schedule puts the chunk index in gridDim.z
+        return PKV_ERR_INVALID_ARG;
     char *ws = static_cast<char *>(workspace);
-    const size_t counters_bytes = align256((size_t)B * kHkv * sizeof(int));
+    const size_t counters_bytes = align256(((size_t)B * kHkv + 2) * sizeof(int));
     const size_t ml_bytes = align256((size_t)B * kHq * max_chunks * sizeof(float2));
     StepArgs a;
     a.num_pages = pool->num_pages;
@@ -638,6 +1021,9 @@ extern "C" int pkv_decode_step(const pkv_pool *pool, const uint16_t *k_new, cons
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
     const bool pdl = !(options & PKV_STEP_NO_PDL);
     // the grid schedule is the measured default; the persistent one is chosen explicitly
+    if (options & PKV_STEP_WS)
+        return variant == PKV_DECODE_SIMT ? launch_ws<SimtWarp>(tmap, a, B, s, pdl)
+                                          : launch_ws<MmaWarp>(tmap, a, B, s, pdl);
     const bool persistent = (options & PKV_STEP_PERSISTENT) != 0;
     if (persistent)
         return variant == PKV_DECODE_SIMT ? launch_persistent<SimtWarp>(tmap, a, B, s, pdl)

@@ -22,7 +22,7 @@ from . import pkv
 from . import workloads as wl
 
 
-SCHEDULES = {"auto": 0, "grid": pkv.PKV_STEP_GRID, "persistent": pkv.PKV_STEP_PERSISTENT}
+SCHEDULES = {"auto": 0, "grid": pkv.PKV_STEP_GRID, "persistent": pkv.PKV_STEP_PERSISTENT, "ws": pkv.PKV_STEP_WS}
 
 
 class DecodeEngine:

@@ -43,6 +43,7 @@ PKV_DECODE_MMA = 2
 PKV_STEP_NO_PDL = 0x100
 PKV_STEP_GRID = 0x200
 PKV_STEP_PERSISTENT = 0x400
+PKV_STEP_WS = 0x800
 PKV_STEP_RING_MASK = 0xF000
 
 

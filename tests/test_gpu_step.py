@@ -26,7 +26,7 @@ def native():
     pkv.lib()
 
 
-SCHEDULES = ["grid", "persistent"]
+SCHEDULES = ["grid", "persistent", "ws"]
 
 
 def fused_run(c, chunk=16, variant=pkv.PKV_DECODE_DEFAULT, pdl=True, seq_lens_override=None, repeats=1,
@@ -45,7 +45,7 @@ def fused_run(c, chunk=16, variant=pkv.PKV_DECODE_DEFAULT, pdl=True, seq_lens_ov
         eng.fused_layer(0, q, k_new, v_new, lens_d, out)
         outs.append(u16(out))
     status, flag = eng.check_errors()
-    counters = eng.step_ws[: c["B"] * 8 * 4].view(torch.int32).cpu().numpy()
+    counters = eng.step_ws[: (c["B"] * 8 + 2) * 4].view(torch.int32).cpu().numpy()
     res = dict(pool=u16(eng.slab.view(torch.bfloat16)), q=u16(q), out=outs[-1], outs=outs, status=status,
                flag=flag, counters=counters)
     eng.close()
@@ -121,8 +121,9 @@ def test_persistent_many_units_per_cta():
     rng = np.random.default_rng(35)
     lens = rng.integers(1, 300, size=300)
     c = make_case(35, lens, max_blocks=64)
-    p = fused_run(c, chunk=2, schedule="persistent")
     g = fused_run(c, chunk=2, schedule="grid")
-    assert p["status"] == pkv.PKV_OK and np.all(p["counters"] == 0)
-    assert np.array_equal(p["out"], g["out"]) and np.array_equal(p["pool"], g["pool"])
-    assert np.array_equal(p["q"], g["q"])
+    for schedule in ("persistent", "ws"):
+        p = fused_run(c, chunk=2, schedule=schedule, repeats=2)
+        assert p["status"] == pkv.PKV_OK and np.all(p["counters"] == 0)
+        assert np.array_equal(p["out"], g["out"]) and np.array_equal(p["pool"], g["pool"])
+        assert np.array_equal(p["q"], g["q"])
