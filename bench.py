@@ -50,12 +50,15 @@ CONFIG_TEXT = {
     "b64": "ragged batch 64: log-normal lengths (median 300, sigma 1, clipped to [1, 2048], boundary lengths "
            "1/16/17/32/33/2048 included), 16 layers, 1% of keys x8, 4096 pages per layer",
     "b8": "batch 8: lengths uniform in [1, 2048], 16 layers, 4096 pages of 32 KiB per layer",
+    "trace": "continuous-batching trace: 500 steps, Poisson(0.6) arrivals per step, prompts U[8,1024], output "
+             "budgets U[16,1024], contexts <= 2048, batch cap 192, 16 layers, page-budget admission, prefill "
+             "page fill, lazy pages",
 }
 VARIANTS = {"default": 0, "simt": 1, "mma": 2}
 # Pages per work unit, chosen per workload from a sweep of 8..128 (any fixed value keeps
 # results batch invariant: the chunking depends only on each sequence's own length).
-DEFAULT_CHUNK = {"b256": 128, "b64": 32, "b8": 16}
-DEFAULT_RING = {"b256": 4, "b64": 2, "b8": 2}   # TMA stages per warp (grid schedule), from the same sweep
+DEFAULT_CHUNK = {"b256": 128, "b64": 32, "b8": 16, "trace": 32}
+DEFAULT_RING = {"b256": 4, "b64": 2, "b8": 2, "trace": 2}   # TMA stages per warp (grid schedule), from the same sweep
 L2_BYTES = 129 * 10**6
 
 
@@ -285,6 +288,70 @@ def run_reference(args):
     return 0
 
 
+def run_trace(args):
+    """The continuous-batching trace: the scheduler admits by page budget, prompts are
+    filled into pages, and every step runs the fused decode step of all layers on the
+    live batch.  value = KV bytes attended / summed device time of the decode steps;
+    e2e = the same bytes / wall-clock time of the whole trace (scheduling, prefill,
+    uploads and a host synchronisation per step included)."""
+    import torch
+
+    from paged_kv_decode_12_gb300 import pkv, workloads as wl
+    from paged_kv_decode_12_gb300.trace import TraceRunner
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    steps = 500 if args.steps == 400 else args.steps
+    seed = replica_seed(args.seed, rank)
+    options = VARIANTS[args.variant] | pkv.PKV_STEP_RING(args.ring) | (pkv.PKV_STEP_NO_PDL if args.no_pdl else 0)
+    pages = args.pool_mib * 2**20 // pkv.PKV_PAGE_BYTES
+    reqs = wl.trace_schedule(seed=seed, steps=steps)
+    # warm-up: a short trace on a small runner (kernel attributes, tensor maps)
+    warm = TraceRunner(pool_pages=4096, layers=16, max_batch=8, seed=seed + 1,
+                       pages_per_chunk=args.pages_per_chunk, options=options)
+    warm.run(wl.trace_schedule(seed=seed + 1, steps=max(args.warmup, 3), arrival_rate=2.0), max(args.warmup, 3))
+    warm.close()
+    runner = TraceRunner(pool_pages=pages, layers=16, max_batch=192, static=args.static, seed=seed,
+                         pages_per_chunk=args.pages_per_chunk, options=options)
+    uuid = str(getattr(torch.cuda.get_device_properties(local), "uuid", "") or "")
+    sampler = ClockSampler(uuid if uuid.startswith("GPU-") else (f"GPU-{uuid}" if uuid else str(local)))
+    sampler.start()
+    t0 = time.time()
+    res = runner.run(reqs, steps)
+    clocks = sampler.stop(t0, time.time())
+    st, flag = pkv.pkv_check_device_error(runner.err)
+    if st != pkv.PKV_OK:
+        raise SystemExit(f"device error flag set during the trace: {flag:#x}")
+    peak, peak_src = hbm_peak()
+    gpu_s = reduce_max(res.gpu_ms / 1e3, world)
+    wall_s = reduce_max(res.wall_s, world)
+    value = res.kv_bytes * world / gpu_s / 1e9
+    line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * gpu_s / max(res.decode_steps, 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"trace: {CONFIG_TEXT['trace']}", "layers": 16, "pool_mib": args.pool_mib,
+                       "pages_per_chunk": args.pages_per_chunk, "ring": args.ring, "kernel_variant": args.variant,
+                       "batching": "static" if args.static else "continuous", "requests": len(reqs),
+                       "seed": args.seed, "l2": "KV per step far above L2 once the batch has grown; no flush"},
+            "hbm_frac_of_peak": value / world / peak,
+            "decode_steps_per_s_wall": res.decode_steps * world / wall_s,
+            "tokens_per_s_wall": res.tokens * world / wall_s,
+            "batch": {"mean": float(np.mean(res.batch_sizes)), "max": int(max(res.batch_sizes))},
+            "roofline": {"bound": "hbm", "achieved": value / world, "peak": peak, "unit": "GB/s",
+                         "frac": value / world / peak, "traffic": None,
+                         "kernel": "fused decode step kernel, all layers of each step (events per step)",
+                         "peak_source": f"{peak_src} hbm_gbs (burst copy)"},
+            "e2e": {"value": res.kv_bytes * world / wall_s / 1e9, "unit": "GB/s",
+                    "h2d_bytes_per_step": None, "d2h_bytes_per_step": 0,
+                    "path": "TraceRunner.run: scheduler, prefill, table/length uploads, one sync per step"},
+            "scheduler_stats": res.stats, "cpu_baseline": None,
+            "gpu_launches": res.decode_steps * 16 + res.stats["admitted"], "clocks": clocks}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    runner.close()
+    return 0
+
+
 def run_pkv(args):
     import torch
 
@@ -453,6 +520,8 @@ def main(argv=None):
     ap.add_argument("--path", choices=["fused", "separate"], default="fused",
                     help="one fused kernel per layer, or append + split + merge launches")
     ap.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
+    ap.add_argument("--pool-mib", type=int, default=16384, help="trace: KV pool size (the engine's default is 128)")
+    ap.add_argument("--static", action="store_true", help="trace: static batching instead of continuous")
     ap.add_argument("--schedule", choices=["auto", "grid", "persistent", "ws"], default="auto",
                     help="fused path: one CTA per unit, or persistent CTAs walking the units")
     ap.add_argument("--ring", type=int, default=None, choices=[2, 3, 4],
@@ -472,6 +541,8 @@ def main(argv=None):
         args.ring = DEFAULT_RING[args.config]
     if args.impl == "reference":
         return run_reference(args)
+    if args.config == "trace":
+        return run_trace(args)
     return run_pkv(args)
 
 

@@ -204,6 +204,76 @@ int pkv_decode_attention_variant(const pkv_pool *pool, const uint16_t *q, const 
                                  int pages_per_chunk, void *workspace, size_t workspace_bytes, uint16_t *out,
                                  int32_t *dev_err_flag, void *cuda_stream, int variant);
 
+/* -------------------------------------------------------------- scheduler */
+
+/* Request scheduler over a page pool (samir-vllm README summary, "当前范围"):
+ * admission by page budget -- a request reserves prompt + allowed_new - 1 tokens,
+ * rounded up to 16-token pages in each layer, as credits separate from physical
+ * pages; allowed_new is capped so that prefix stays within the context -- FIFO
+ * waiting, rejection of budgets larger than the whole pool, lazy page allocation,
+ * pages and credits returned on finish or early stop, no preemption.  Continuous
+ * batching admits whenever credits allow; static batching admits the next group
+ * only after the current one has finished ("构建": --static / --continuous).
+ * Host only (no CUDA call).  The scheduler assumes it owns the pool's pages that
+ * are free when it is created (their number is the credit total); every page it
+ * hands out belongs to exactly one (request, layer).  Not thread-safe. */
+typedef struct pkv_sched pkv_sched;
+
+#define PKV_SCHED_CONTINUOUS 0
+#define PKV_SCHED_STATIC 1
+
+typedef struct pkv_sched_stats {
+    int64_t pool_pages;           /* pages in the pool */
+    int64_t peak_active;          /* most requests active at once */
+    int64_t max_decode_batch;     /* largest decode batch */
+    int64_t peak_allocated_pages; /* most physical pages held at once */
+    int64_t admission_waits;      /* admission rounds in which the FIFO head had to wait for credits */
+    int64_t final_free_pages;     /* pages free in the pool now */
+    int64_t submitted, admitted, finished, rejected;
+    int64_t active, waiting, allocated_pages, free_credits; /* current state */
+} pkv_sched_stats;
+
+/* layers: layers per request (16); max_blocks: table width (128); max_context:
+ * context cap in tokens (2048, at most 16*max_blocks); max_batch: decode batch cap;
+ * mode: PKV_SCHED_CONTINUOUS or PKV_SCHED_STATIC. */
+int pkv_sched_create(pkv_pool *pool, int layers, int max_blocks, int max_context, int max_batch, int mode,
+                     pkv_sched **out);
+/* Frees the pages of requests still active. */
+int pkv_sched_destroy(pkv_sched *sched);
+/* Queue a request.  PKV_ERR_BUDGET_EXCEEDS_POOL if its budget exceeds every credit
+ * (it could never run); PKV_ERR_INVALID_ARG for prompt < 1, prompt > max_context,
+ * max_new < 1 or a duplicate id. */
+int pkv_sched_submit(pkv_sched *sched, int64_t id, int prompt_tokens, int max_new_tokens);
+/* Admit waiting requests in FIFO order while credits and the batch cap allow (at
+ * most max_n).  For each: its id, prompt length and block-table rows
+ * bt_rows_out[i][layers][max_blocks] holding the pages of its prompt (allocated
+ * now), for the caller's prefill.  *n_out = number admitted. */
+int pkv_sched_admit(pkv_sched *sched, int max_n, int64_t *ids_out, int32_t *prompt_lens_out, int32_t *bt_rows_out,
+                    int *n_out);
+/* Next decode step: retire requests whose last step has run, then append one token
+ * to every active request (taking a new page per layer when it crosses a page
+ * boundary) and return the batch: ids_out[B], seq_lens_out[B] (lengths after the
+ * append) and bt_out[layers][B][max_blocks].  max_b bounds B. */
+int pkv_sched_decode_batch(pkv_sched *sched, int max_b, int64_t *ids_out, int32_t *seq_lens_out, int32_t *bt_out,
+                           int *B_out);
+/* Early stop (e.g. an end-of-sequence token): free the request's pages and credits
+ * now, or drop it from the queue. */
+int pkv_sched_finish(pkv_sched *sched, int64_t id);
+int pkv_sched_get_stats(const pkv_sched *sched, pkv_sched_stats *out);
+
+/* ------------------------------------------------------------ prefill fill */
+
+/* Write T consecutive tokens of ONE sequence into its pages, for `layers` layers:
+ * token t goes to position start_pos + t, its key rotated to that position exactly
+ * as pkv_append_rope rotates the decode token (samir-vllm README summary, "目前已完成
+ * 的功能": prefill fills the prompt's pages; decode appends at the absolute RoPE
+ * position).  k, v: [layers][T][8][64] BF16; bt_rows: device [layers][max_blocks]
+ * (this sequence's table in every layer).  Device checks: a position beyond the
+ * table or max_pos, or a page id outside the pool, sets the flag and skips it. */
+int pkv_prefill_append(const pkv_pool *pool, const uint16_t *k, const uint16_t *v, const int32_t *bt_rows,
+                       int max_blocks, int layers, int start_pos, int T, const float *rope_table, int max_pos,
+                       int32_t *dev_err_flag, void *cuda_stream);
+
 /* ------------------------------------------------------ fused decode step */
 
 /* option bits for pkv_decode_step */

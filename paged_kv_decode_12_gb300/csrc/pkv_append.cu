@@ -99,3 +99,74 @@ extern "C" int pkv_append_rope(const pkv_pool *pool, const uint16_t *k_new, cons
                                                     dev_err_flag);
     return status_from_cuda(cudaGetLastError());
 }
+
+// ---------------------------------------------------------------------------
+// Prefill page fill: T consecutive tokens of one sequence, every layer.  Same
+// rotation and placement as the decode append (one CTA per (token, layer)).
+namespace pkv {
+namespace {
+
+constexpr int kPrefillThreads = 128;
+
+__global__ void __launch_bounds__(kPrefillThreads)
+prefill_append_kernel(uint16_t *__restrict__ slab, int num_pages, const uint16_t *__restrict__ k,
+                      const uint16_t *__restrict__ v, const int32_t *__restrict__ bt_rows, int max_blocks, int start_pos,
+                      int T, const float2 *__restrict__ rope, int max_pos, int32_t *__restrict__ err)
+{
+    const int t = blockIdx.x, l = blockIdx.y;
+    const int p = start_pos + t;
+    if (p < 0 || p >= min(max_pos, max_blocks * kPage)) {
+        if (threadIdx.x == 0 && err)
+            atomicOr(err, PKV_DEVERR_LENGTH);
+        return;
+    }
+    const int page = bt_rows[(size_t)l * max_blocks + p / kPage];
+    if (page < 0 || page >= num_pages) {
+        if (threadIdx.x == 0 && err)
+            atomicOr(err, PKV_DEVERR_PAGE_RANGE);
+        return;
+    }
+    const int slot = p % kPage;
+    uint16_t *page_base = slab + (size_t)page * kPageElems;
+    const size_t row0 = ((size_t)l * T + t) * kHkv * kD;  // token t of layer l: [8][64]
+    if (threadIdx.x < kHkv * kD * 2 / 16) {                // values: 64 chunks of 16 B
+        const int h = threadIdx.x / 8, c = threadIdx.x % 8;
+        const uint4 val = reinterpret_cast<const uint4 *>(v + row0 + (size_t)h * kD)[c];
+        reinterpret_cast<uint4 *>(page_base + ((size_t)(kHkv + h) * kPage + slot) * kD)[c] = val;
+    }
+    for (int item = threadIdx.x; item < kHkv * (kD / 2); item += kPrefillThreads) {
+        const int h = item / (kD / 2), i = item % (kD / 2);
+        const float2 cs = rope[(size_t)p * (kD / 2) + i];
+        const uint16_t *src = k + row0 + (size_t)h * kD;
+        const float x1 = __uint_as_float((uint32_t)src[i] << 16);
+        const float x2 = __uint_as_float((uint32_t)src[i + kD / 2] << 16);
+        float y1, y2;
+        dev::rope_rotate_pair(x1, x2, cs.x, cs.y, y1, y2);
+        const __nv_bfloat16 b1 = __float2bfloat16_rn(y1), b2 = __float2bfloat16_rn(y2);
+        uint16_t *dst = page_base + ((size_t)h * kPage + slot) * kD;
+        dst[i] = *reinterpret_cast<const uint16_t *>(&b1);
+        dst[i + kD / 2] = *reinterpret_cast<const uint16_t *>(&b2);
+    }
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" int pkv_prefill_append(const pkv_pool *pool, const uint16_t *k, const uint16_t *v, const int32_t *bt_rows,
+                                  int max_blocks, int layers, int start_pos, int T, const float *rope_table,
+                                  int max_pos, int32_t *dev_err_flag, void *cuda_stream)
+{
+    using namespace pkv;
+    if (!pool || !k || !v || !bt_rows || !rope_table)
+        return PKV_ERR_INVALID_ARG;
+    if (T < 1 || T > INT32_MAX / 2 || layers < 1 || layers > 65535 || max_blocks < 1 || max_pos < 1 || start_pos < 0)
+        return PKV_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(rope_table)) &
+        15u)
+        return PKV_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    prefill_append_kernel<<<dim3(T, layers), kPrefillThreads, 0, s>>>(
+        reinterpret_cast<uint16_t *>(pool->slab), pool->num_pages, k, v, bt_rows, max_blocks, start_pos, T,
+        reinterpret_cast<const float2 *>(rope_table), max_pos, dev_err_flag);
+    return status_from_cuda(cudaGetLastError());
+}

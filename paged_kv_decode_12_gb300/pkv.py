@@ -273,3 +273,102 @@ def pkv_check_device_error(dev_err_flag, stream=None):
     if st not in (PKV_OK, PKV_ERR_DEVICE_BOUNDS):
         raise PkvError(st, "pkv_check_device_error")
     return st, int(flag.value)
+
+
+# ---------------------------------------------------------------------------- scheduler, prefill
+
+PKV_SCHED_CONTINUOUS = 0
+PKV_SCHED_STATIC = 1
+
+EXPORTED = EXPORTED + (
+    "pkv_sched_create", "pkv_sched_destroy", "pkv_sched_submit", "pkv_sched_admit", "pkv_sched_decode_batch",
+    "pkv_sched_finish", "pkv_sched_get_stats", "pkv_prefill_append",
+)
+
+
+class SchedStats(ctypes.Structure):
+    _fields_ = [(name, ctypes.c_int64) for name in (
+        "pool_pages", "peak_active", "max_decode_batch", "peak_allocated_pages", "admission_waits",
+        "final_free_pages", "submitted", "admitted", "finished", "rejected", "active", "waiting",
+        "allocated_pages", "free_credits")]
+
+    def as_dict(self) -> dict:
+        return {name: int(getattr(self, name)) for name, _ in self._fields_}
+
+
+_lib_core = lib
+_i64p = ctypes.POINTER(ctypes.c_int64)
+
+
+def lib():  # noqa: F811 -- extends the loader with the scheduler and prefill signatures
+    L = _lib_core()
+    if not getattr(L, "_pkv_sched_bound", False):
+        L.pkv_sched_create.argtypes = [_vp, _i32, _i32, _i32, _i32, _i32, ctypes.POINTER(_vp)]
+        L.pkv_sched_destroy.argtypes = [_vp]
+        L.pkv_sched_submit.argtypes = [_vp, ctypes.c_int64, _i32, _i32]
+        L.pkv_sched_admit.argtypes = [_vp, _i32, _i64p, _i32p, _i32p, ctypes.POINTER(_i32)]
+        L.pkv_sched_decode_batch.argtypes = [_vp, _i32, _i64p, _i32p, _i32p, ctypes.POINTER(_i32)]
+        L.pkv_sched_finish.argtypes = [_vp, ctypes.c_int64]
+        L.pkv_sched_get_stats.argtypes = [_vp, ctypes.POINTER(SchedStats)]
+        L.pkv_prefill_append.argtypes = [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _i32, _vp, _vp]
+        for name in ("pkv_sched_create", "pkv_sched_destroy", "pkv_sched_submit", "pkv_sched_admit",
+                     "pkv_sched_decode_batch", "pkv_sched_finish", "pkv_sched_get_stats", "pkv_prefill_append"):
+            getattr(L, name).restype = ctypes.c_int
+        L._pkv_sched_bound = True
+    return L
+
+
+def pkv_sched_create(pool, layers: int, max_blocks: int, max_context: int, max_batch: int,
+                     mode: int = PKV_SCHED_CONTINUOUS):
+    out = ctypes.c_void_p()
+    _check(lib().pkv_sched_create(pool, layers, max_blocks, max_context, max_batch, mode, ctypes.byref(out)),
+           "pkv_sched_create")
+    return out
+
+
+def pkv_sched_destroy(sched) -> None:
+    _check(lib().pkv_sched_destroy(sched), "pkv_sched_destroy")
+
+
+def pkv_sched_submit(sched, rid: int, prompt_tokens: int, max_new_tokens: int) -> None:
+    _check(lib().pkv_sched_submit(sched, int(rid), int(prompt_tokens), int(max_new_tokens)), "pkv_sched_submit")
+
+
+def pkv_sched_admit(sched, max_n: int, layers: int, max_blocks: int):
+    """Returns (ids int64 [n], prompt_lens int32 [n], bt_rows int32 [n][layers][max_blocks])."""
+    ids = np.empty(max_n, dtype=np.int64)
+    lens = np.empty(max_n, dtype=np.int32)
+    bt = np.empty((max_n, layers, max_blocks), dtype=np.int32)
+    n = ctypes.c_int(0)
+    _check(lib().pkv_sched_admit(sched, max_n, ids.ctypes.data_as(_i64p), lens.ctypes.data_as(_i32p),
+                                 bt.ctypes.data_as(_i32p), ctypes.byref(n)), "pkv_sched_admit")
+    return ids[:n.value], lens[:n.value], bt[:n.value]
+
+
+def pkv_sched_decode_batch(sched, max_b: int, layers: int, max_blocks: int):
+    """Returns (ids int64 [B], seq_lens int32 [B], bt int32 [layers][B][max_blocks])."""
+    ids = np.empty(max_b, dtype=np.int64)
+    lens = np.empty(max_b, dtype=np.int32)
+    bt = np.empty(layers * max_b * max_blocks, dtype=np.int32)
+    B = ctypes.c_int(0)
+    _check(lib().pkv_sched_decode_batch(sched, max_b, ids.ctypes.data_as(_i64p), lens.ctypes.data_as(_i32p),
+                                        bt.ctypes.data_as(_i32p), ctypes.byref(B)), "pkv_sched_decode_batch")
+    b = B.value
+    return ids[:b], lens[:b], bt[: layers * b * max_blocks].reshape(layers, b, max_blocks)
+
+
+def pkv_sched_finish(sched, rid: int) -> None:
+    _check(lib().pkv_sched_finish(sched, int(rid)), "pkv_sched_finish")
+
+
+def pkv_sched_get_stats(sched) -> dict:
+    st = SchedStats()
+    _check(lib().pkv_sched_get_stats(sched, ctypes.byref(st)), "pkv_sched_get_stats")
+    return st.as_dict()
+
+
+def pkv_prefill_append(pool, k, v, bt_rows_dev, max_blocks: int, layers: int, start_pos: int, T: int, rope_table,
+                       max_pos: int, dev_err_flag=None, stream=None) -> None:
+    _check(lib().pkv_prefill_append(pool, _ptr(k), _ptr(v), _ptr(bt_rows_dev), max_blocks, layers, start_pos, T,
+                                    _ptr(rope_table), max_pos, _ptr(dev_err_flag), _stream(stream)),
+           "pkv_prefill_append")

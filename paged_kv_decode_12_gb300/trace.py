@@ -1,0 +1,144 @@
+"""Continuous-batching trace over the C ABI: scheduler, prefill page fill, decode steps.
+
+Each step of the trace: submit the requests arriving at this step, admit waiting
+requests by page budget (``pkv_sched_admit``; FIFO, rejection, lazy pages), fill
+each admitted prompt's pages one prompt at a time (``pkv_prefill_append``; the
+README summary's "prefill fills the prompt's pages", prompts between decode
+iterations), then build the decode batch (``pkv_sched_decode_batch``: one new token
+per active sequence, pages taken at page boundaries) and run the fused decode step
+for every layer (``pkv_decode_step``).  Activations are seeded synthetic draws:
+there is no model, so prompt K/V, q, k_new and v_new are N(0,1) BF16 (the attention
+path does not depend on their origin).
+
+PyTorch allocates device memory and provides the stream; the scheduler is native
+(C++ in libpkv) and every step of the computation runs in libpkv's kernels.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+import time
+
+import numpy as np
+import torch
+
+from . import pkv
+from . import workloads as wl
+
+
+@dataclasses.dataclass
+class TraceResult:
+    steps: int
+    decode_steps: int              # steps with a non-empty batch
+    gpu_ms: float                  # summed device time of the decode steps (events)
+    wall_s: float                  # whole trace, host scheduling and uploads included
+    kv_bytes: int                  # K/V bytes attended over the trace
+    tokens: int                    # decode tokens produced (one per active sequence per step)
+    batch_sizes: list
+    stats: dict
+
+
+class TraceRunner:
+    def __init__(self, pool_pages: int, layers: int = 16, max_batch: int = 192, max_blocks: int = wl.MAX_BLOCKS,
+                 max_context: int = wl.MAX_CONTEXT, static: bool = False, seed: int = wl.DEFAULT_SEED,
+                 pages_per_chunk: int = 32, options: int = pkv.PKV_STEP_RING(2), device: str = "cuda"):
+        self.device = torch.device(device)
+        self.layers, self.max_batch, self.max_blocks, self.max_context = layers, max_batch, max_blocks, max_context
+        self.pages_per_chunk, self.options, self.seed = pages_per_chunk, options, seed
+        self.scale = 1.0 / math.sqrt(wl.HEAD_DIM)
+        self.slab = torch.zeros(pool_pages * pkv.PKV_PAGE_BYTES, dtype=torch.uint8, device=self.device)
+        self.pool = pkv.pkv_pool_create(self.slab, self.slab.numel(), seed=seed)
+        self.num_pages = pool_pages
+        self.sched = pkv.pkv_sched_create(self.pool, layers, max_blocks, max_context, max_batch,
+                                          pkv.PKV_SCHED_STATIC if static else pkv.PKV_SCHED_CONTINUOUS)
+        self.rope = torch.empty(max_context * wl.HEAD_DIM, dtype=torch.float32, device=self.device)
+        pkv.pkv_rope_table_init(wl.ROPE_THETA, max_context, wl.HEAD_DIM // 2, self.rope)
+        self.err = torch.zeros(1, dtype=torch.int32, device=self.device)
+        self.ws_bytes = pkv.pkv_decode_step_workspace_bytes(max_batch, max_blocks, pages_per_chunk)
+        self.ws = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=self.device)
+
+        def draw(shape, s):
+            return wl.fill_bf16_normal_(torch.empty(shape, dtype=torch.bfloat16, device=self.device), s)
+
+        self.q = draw((layers, max_batch, wl.NUM_Q_HEADS, wl.HEAD_DIM), seed + 1)
+        self.k_new = draw((layers, max_batch, wl.NUM_KV_HEADS, wl.HEAD_DIM), seed + 2)
+        self.v_new = draw((layers, max_batch, wl.NUM_KV_HEADS, wl.HEAD_DIM), seed + 3)
+        self.out = torch.zeros((layers, max_batch, wl.NUM_Q_HEADS, wl.HEAD_DIM), dtype=torch.bfloat16,
+                               device=self.device)
+        self.bt = torch.full((layers, max_batch, max_blocks), -1, dtype=torch.int32, device=self.device)
+        self.lens = torch.zeros(max_batch, dtype=torch.int32, device=self.device)
+        self.prompt_bt = torch.full((layers, max_blocks), -1, dtype=torch.int32, device=self.device)
+        self._prompt_seed = seed + 100
+
+    def close(self):
+        if self.sched is not None:
+            pkv.pkv_sched_destroy(self.sched)
+            self.sched = None
+        if self.pool is not None:
+            pkv.pkv_pool_destroy(self.pool)
+            self.pool = None
+
+    # ------------------------------------------------------------------ pieces
+    def prefill(self, bt_rows: np.ndarray, prompt_len: int):
+        """Fill one prompt's pages in every layer with seeded N(0,1) K/V."""
+        self.prompt_bt.copy_(torch.from_numpy(bt_rows))
+        self._prompt_seed += 1
+        g = torch.Generator(device=self.device)
+        g.manual_seed(self._prompt_seed)
+        shape = (self.layers, prompt_len, wl.NUM_KV_HEADS, wl.HEAD_DIM)
+        k = torch.randn(shape, generator=g, device=self.device, dtype=torch.float32).to(torch.bfloat16)
+        v = torch.randn(shape, generator=g, device=self.device, dtype=torch.float32).to(torch.bfloat16)
+        pkv.pkv_prefill_append(self.pool, k, v, self.prompt_bt, self.max_blocks, self.layers, 0, prompt_len,
+                               self.rope, self.max_context, self.err)
+
+    def decode(self, B: int):
+        for layer in range(self.layers):
+            pkv.pkv_decode_step(self.pool, self.k_new[layer, :B], self.v_new[layer, :B], self.q[layer, :B],
+                                self.bt[layer, :B], self.max_blocks, self.lens, B, self.rope, self.max_context,
+                                self.scale, self.pages_per_chunk, self.ws, self.ws_bytes, self.out[layer, :B],
+                                self.err, None, self.options)
+
+    # ------------------------------------------------------------------ trace
+    def run(self, requests, steps: int, before_step=None, after_step=None) -> TraceResult:
+        """Run ``steps`` trace steps.  ``before_step(step, ids, lens, bt_host)`` and
+        ``after_step(step, ids, lens, bt_host)`` (optional) see each decode batch."""
+        by_step = {}
+        for r in requests:
+            by_step.setdefault(r.arrival_step, []).append(r)
+        gpu_ms, kv_bytes, tokens, decode_steps, sizes = 0.0, 0, 0, 0, []
+        per_token = wl.kv_bytes_per_token(self.layers)
+        t0 = time.perf_counter()
+        for step in range(steps):
+            for r in by_step.get(step, []):
+                try:
+                    pkv.pkv_sched_submit(self.sched, r.rid, r.prompt_len, r.max_new)
+                except pkv.PkvError as e:
+                    if e.status != pkv.PKV_ERR_BUDGET_EXCEEDS_POOL:
+                        raise
+            ids, plens, bt_rows = pkv.pkv_sched_admit(self.sched, self.max_batch, self.layers, self.max_blocks)
+            for i in range(ids.size):
+                self.prefill(bt_rows[i], int(plens[i]))
+            ids, lens, bt = pkv.pkv_sched_decode_batch(self.sched, self.max_batch, self.layers, self.max_blocks)
+            B = ids.size
+            sizes.append(B)
+            if B == 0:
+                continue
+            self.lens[:B].copy_(torch.from_numpy(lens))
+            self.bt[:, :B].copy_(torch.from_numpy(bt))
+            if before_step:
+                before_step(step, ids, lens, bt)
+            start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            start.record()
+            self.decode(B)
+            end.record()
+            if after_step:
+                after_step(step, ids, lens, bt)
+            end.synchronize()
+            gpu_ms += start.elapsed_time(end)
+            kv_bytes += int(lens.astype(np.int64).sum()) * per_token
+            tokens += B
+            decode_steps += 1
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+        return TraceResult(steps, decode_steps, gpu_ms, wall, kv_bytes, tokens, sizes,
+                           pkv.pkv_sched_get_stats(self.sched))
