@@ -170,7 +170,7 @@ def kernel_source_digest() -> str:
     return h.hexdigest()[:16]
 
 
-def measured_traffic(config: str, path: str, variant_name: str, pages_per_chunk: int):
+def measured_traffic(config: str, path: str, variant_name: str, pages_per_chunk: int, ring: int):
     """DRAM bytes per attention launch from the committed ncu summary
     (profiles/decode_traffic.json), if it was taken on the current kernel source;
     else None."""
@@ -440,7 +440,7 @@ def run_pkv(args):
         avg = sum(split_ms) / len(split_ms)
         achieved = kv_launch / (avg / 1e3) / 1e9
         roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                    "traffic": measured_traffic(args.config, args.path, variant_name, args.pages_per_chunk),
+                    "traffic": measured_traffic(args.config, args.path, variant_name, args.pages_per_chunk, args.ring),
                     "kernel": (f"fused decode step kernel (append + attention + merge), variant {variant_name}"
                                if args.path == "fused" else
                                f"paged decode attention launch (split + merge), variant {variant_name}"),
