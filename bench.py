@@ -182,7 +182,8 @@ def measured_traffic(config: str, path: str, variant_name: str, pages_per_chunk:
     digest = kernel_source_digest()
     for e in entries:
         if (e.get("config") == config and e.get("path") == path and e.get("variant") == variant_name and
-                e.get("pages_per_chunk") == pages_per_chunk and e.get("kernel_source_sha") == digest):
+                e.get("pages_per_chunk") == pages_per_chunk and e.get("ring", 4) == ring and
+                e.get("kernel_source_sha") == digest):
             return e.get("dram_bytes_per_launch")
     return None
 
