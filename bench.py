@@ -251,6 +251,7 @@ def config_block(w, args, variant_name: str, graph: bool) -> dict:
             "pages_per_chunk": args.pages_per_chunk, "kernel_variant": variant_name, "cuda_graph": graph,
             "path": getattr(args, "path", "fused"), "pdl": not getattr(args, "no_pdl", False),
             "schedule": getattr(args, "schedule", "auto"), "ring": getattr(args, "ring", 0),
+            "early_trigger": getattr(args, "early_trigger", False),
             "kv_bytes_per_step": kv,
             "l2": f"inputs larger than L2 ({kv / 1e9:.2f} GB of KV per step vs {L2_BYTES / 1e6:.0f} MB L2), "
                   "no flush", "seed": args.seed}
@@ -371,7 +372,7 @@ def run_pkv(args):
     variant_name = args.variant
     dw = harness.setup(args.config, replica_seed(args.seed, rank), args.pages_per_chunk, VARIANTS[variant_name],
                        layers=args.layers, fused=args.path == "fused", pdl=not args.no_pdl,
-                       schedule=args.schedule, ring=args.ring)
+                       schedule=args.schedule, ring=args.ring, early_trigger=args.early_trigger)
     w = dw.w
     harness.warm(dw, 2)
     dw.reset_q()
@@ -521,6 +522,8 @@ def main(argv=None):
     ap.add_argument("--path", choices=["fused", "separate"], default="fused",
                     help="one fused kernel per layer, or append + split + merge launches")
     ap.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
+    ap.add_argument("--early-trigger", action="store_true",
+                    help="let the next layer's launch begin once a CTA has issued its page copies")
     ap.add_argument("--pool-mib", type=int, default=16384, help="trace: KV pool size (the engine's default is 128)")
     ap.add_argument("--static", action="store_true", help="trace: static batching instead of continuous")
     ap.add_argument("--schedule", choices=["auto", "grid", "persistent", "ws"], default="auto",

@@ -285,6 +285,10 @@ int pkv_prefill_append(const pkv_pool *pool, const uint16_t *k, const uint16_t *
  * Fewer stages mean less shared memory per CTA and more CTAs resident per SM. */
 #define PKV_STEP_RING(n) ((n) << 12)
 #define PKV_STEP_RING_MASK 0xf000
+/* grid schedule: let the next launch begin as soon as a CTA has issued its page
+ * copies, instead of after it has consumed them (helps layers that fit in one
+ * wave of CTAs; can slow launches of several waves) */
+#define PKV_STEP_EARLY_TRIGGER 0x10000
 
 /* Bytes of device workspace pkv_decode_step needs (a per-(sequence, KV head)
  * counter array and two work-distribution counters, followed by the chunk

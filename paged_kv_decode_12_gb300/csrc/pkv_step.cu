@@ -61,6 +61,7 @@ struct StepArgs {
     int max_chunks;
     uint16_t *out;           // [B][32][64]
     int32_t *err;
+    int early_trigger;       // grid schedule: allow the next launch as soon as the copies are issued
 };
 
 constexpr int kStepStages = 4;       // persistent schedule ring depth
@@ -270,6 +271,8 @@ __global__ void __launch_bounds__(kThreads) decode_step_kernel(const __grid_cons
         init_warp_barriers<STAGES>(my_bars, lane);
         issue_prologue<STAGES>(&tmap, my_stages, my_bars, my_page, nmine, g, lane, policy);
     }
+    if (a.early_trigger)
+        allow_dependent_launch();
 
     grid_dependency_wait();  // q, k_new, v_new and every output belong to the dependency chain
 
@@ -293,7 +296,8 @@ __global__ void __launch_bounds__(kThreads) decode_step_kernel(const __grid_cons
             lane == 0 && a.err)
             atomicOr(a.err, PKV_DEVERR_TIMEOUT);
     }
-    allow_dependent_launch();
+    if (!a.early_trigger)
+        allow_dependent_launch();
     // the stages are free now: they hold the combine area
     finish_unit(a, w, reinterpret_cast<float *>(sm.stages), ticket, q_rot, b, g, c, nchunks);
 }
@@ -978,7 +982,7 @@ extern "C" int pkv_decode_step(const pkv_pool *pool, const uint16_t *k_new, cons
     const int variant = options & 0xff;
     if (variant < PKV_DECODE_DEFAULT || variant > PKV_DECODE_MMA ||
         (options & ~(0xff | PKV_STEP_NO_PDL | PKV_STEP_GRID | PKV_STEP_PERSISTENT | PKV_STEP_WS |
-                     PKV_STEP_RING_MASK)) ||
+                     PKV_STEP_RING_MASK | PKV_STEP_EARLY_TRIGGER)) ||
         (!!(options & PKV_STEP_GRID) + !!(options & PKV_STEP_PERSISTENT) + !!(options & PKV_STEP_WS) > 1))
         return PKV_ERR_INVALID_ARG;
     if ((options & (PKV_STEP_PERSISTENT | PKV_STEP_WS)) && B > kMaxPersistentBatch)
@@ -1018,6 +1022,7 @@ extern "C" int pkv_decode_step(const pkv_pool *pool, const uint16_t *k_new, cons
     a.max_chunks = max_chunks;
     a.out = out;
     a.err = dev_err_flag;
+    a.early_trigger = (options & PKV_STEP_EARLY_TRIGGER) ? 1 : 0;
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
     const bool pdl = !(options & PKV_STEP_NO_PDL);
     // the grid schedule is the measured default; the persistent one is chosen explicitly

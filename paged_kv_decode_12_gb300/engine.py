@@ -29,7 +29,7 @@ class DecodeEngine:
     def __init__(self, num_pages: int, layers: int, batch: int, max_blocks: int = wl.MAX_BLOCKS,
                  pages_per_chunk: int = 16, variant: int = pkv.PKV_DECODE_DEFAULT, max_pos: int = wl.MAX_CONTEXT,
                  theta: float = wl.ROPE_THETA, pool_seed: int = 0, device: str = "cuda", fused: bool = True,
-                 pdl: bool = True, schedule: str = "auto", ring: int = 0):
+                 pdl: bool = True, schedule: str = "auto", ring: int = 0, early_trigger: bool = False):
         self.device = torch.device(device)
         self.layers, self.batch, self.max_blocks = layers, batch, max_blocks
         self.pages_per_chunk, self.variant, self.max_pos = pages_per_chunk, variant, max_pos
@@ -47,7 +47,8 @@ class DecodeEngine:
         self.step_ws_bytes = pkv.pkv_decode_step_workspace_bytes(batch, max_blocks, pages_per_chunk)
         self.step_ws = torch.zeros(self.step_ws_bytes, dtype=torch.uint8, device=self.device)
         self.fused = fused
-        self.step_options = variant | (0 if pdl else pkv.PKV_STEP_NO_PDL) | SCHEDULES[schedule] | pkv.PKV_STEP_RING(ring)
+        self.step_options = (variant | (0 if pdl else pkv.PKV_STEP_NO_PDL) | SCHEDULES[schedule]
+                             | pkv.PKV_STEP_RING(ring) | (pkv.PKV_STEP_EARLY_TRIGGER if early_trigger else 0))
         self.bt = None
         self.bt_host = None
 

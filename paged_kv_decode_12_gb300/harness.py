@@ -37,7 +37,8 @@ class DeviceWorkload:
 
 def setup(name: str, seed: int = wl.DEFAULT_SEED, pages_per_chunk: int = 16,
           variant: int = pkv.PKV_DECODE_DEFAULT, layers: int | None = None, device: str = "cuda",
-          fused: bool = True, pdl: bool = True, schedule: str = "auto", ring: int = 0) -> DeviceWorkload:
+          fused: bool = True, pdl: bool = True, schedule: str = "auto", ring: int = 0,
+          early_trigger: bool = False) -> DeviceWorkload:
     """Build the named workload on the GPU: pool filled with N(0,1) BF16 (plus the
     key outliers of ``b64``), block tables from the library's seeded allocator,
     per-layer q / k_new / v_new draws, positions = lengths - 1."""
@@ -45,7 +46,8 @@ def setup(name: str, seed: int = wl.DEFAULT_SEED, pages_per_chunk: int = 16,
     if layers is not None and layers != w.layers:
         w = dataclasses.replace(w, layers=layers, pool_pages=w.pool_pages * layers // w.layers)
     eng = DecodeEngine(w.pool_pages, w.layers, w.batch, w.max_blocks, pages_per_chunk, variant, pool_seed=seed,
-                       device=device, fused=fused, pdl=pdl, schedule=schedule, ring=ring)
+                       device=device, fused=fused, pdl=pdl, schedule=schedule, ring=ring,
+                       early_trigger=early_trigger)
     pool = eng.pool_view()
     wl.fill_bf16_normal_(pool, seed)
     wl.scale_key_rows_(pool, w.key_outlier_frac, seed + 7)

@@ -45,6 +45,7 @@ PKV_STEP_GRID = 0x200
 PKV_STEP_PERSISTENT = 0x400
 PKV_STEP_WS = 0x800
 PKV_STEP_RING_MASK = 0xF000
+PKV_STEP_EARLY_TRIGGER = 0x10000
 
 
 def PKV_STEP_RING(n: int) -> int:
