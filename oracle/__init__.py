@@ -217,3 +217,112 @@ def decode_contiguous(K, V, seq_lens, q, scale: float) -> np.ndarray:
 
 def library_path() -> str:
     return os.path.abspath(_build.LIB)
+
+
+# --------------------------------------------------------------------------- FP8 KV pages
+
+FP8_PAGE_BYTES = 2 * 8 * 16 * (64 + 4)   # codes + row scales, for 8 KV heads x 16 slots x 64 dims
+
+
+def _load_fp8():
+    lib = _load()
+    if getattr(lib, "_fp8_bound", False):
+        return lib
+    u8p = ctypes.POINTER(ctypes.c_uint8)
+    u16p = ctypes.POINTER(ctypes.c_uint16)
+    i32p = ctypes.POINTER(ctypes.c_int32)
+    f64p = ctypes.POINTER(ctypes.c_double)
+    f32p = ctypes.POINTER(ctypes.c_float)
+    gp = ctypes.POINTER(PoolGeom)
+    lib.oracle_e4m3_from_double.argtypes = [ctypes.c_double]
+    lib.oracle_e4m3_from_double.restype = ctypes.c_uint8
+    lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+    lib.oracle_e4m3_to_double.restype = ctypes.c_double
+    lib.oracle_quantize_row_fp8.argtypes = [u16p, ctypes.c_int, u8p, f32p]
+    lib.oracle_quantize_row_fp8.restype = None
+    lib.oracle_fp8_code_offset.argtypes = [gp] + [ctypes.c_int] * 5
+    lib.oracle_fp8_code_offset.restype = ctypes.c_int64
+    lib.oracle_fp8_scale_offset.argtypes = [gp] + [ctypes.c_int] * 4
+    lib.oracle_fp8_scale_offset.restype = ctypes.c_int64
+    lib.oracle_append_fp8.argtypes = [u8p, gp, i32p, ctypes.c_int, i32p, ctypes.c_int, u16p, u16p, u16p,
+                                      ctypes.c_int, ctypes.c_double]
+    lib.oracle_append_fp8.restype = ctypes.c_int
+    lib.oracle_decode_one_fp8.argtypes = [u8p, gp, i32p, ctypes.c_int, ctypes.c_int, u16p, ctypes.c_int,
+                                          ctypes.c_double, f64p, f64p]
+    lib.oracle_decode_one_fp8.restype = ctypes.c_int
+    lib.oracle_decode_fp8.argtypes = [u8p, gp, i32p, ctypes.c_int, i32p, ctypes.c_int, u16p, ctypes.c_int,
+                                      ctypes.c_double, u16p, f64p]
+    lib.oracle_decode_fp8.restype = ctypes.c_int
+    lib._fp8_bound = True
+    return lib
+
+
+def e4m3_from_f64(values) -> np.ndarray:
+    lib = _load_fp8()
+    v = np.ascontiguousarray(values, dtype=np.float64).reshape(-1)
+    return np.array([lib.oracle_e4m3_from_double(float(x)) for x in v], dtype=np.uint8).reshape(np.shape(values))
+
+
+def e4m3_to_f64(codes) -> np.ndarray:
+    lib = _load_fp8()
+    c = np.ascontiguousarray(codes, dtype=np.uint8).reshape(-1)
+    return np.array([lib.oracle_e4m3_to_double(int(x)) for x in c], dtype=np.float64).reshape(np.shape(codes))
+
+
+def quantize_row_fp8(row_bf16):
+    """One row of BF16 bits -> (codes uint8, scale float32)."""
+    lib = _load_fp8()
+    row = _u16(row_bf16)
+    codes = np.empty(row.size, dtype=np.uint8)
+    scale = ctypes.c_float()
+    lib.oracle_quantize_row_fp8(_ptr(row, ctypes.c_uint16), row.size, _ptr(codes, ctypes.c_uint8),
+                                ctypes.byref(scale))
+    return codes, np.float32(scale.value)
+
+
+def fp8_code_offset(g: PoolGeom, page, kv, head, slot, dim) -> int:
+    return int(_load_fp8().oracle_fp8_code_offset(ctypes.byref(g), page, kv, head, slot, dim))
+
+
+def fp8_scale_offset(g: PoolGeom, page, kv, head, slot) -> int:
+    return int(_load_fp8().oracle_fp8_scale_offset(ctypes.byref(g), page, kv, head, slot))
+
+
+def append_fp8(pool: np.ndarray, g: PoolGeom, bt, pos, k_new, v_new, q=None, num_q_heads: int = 32,
+               theta: float = 500000.0):
+    """As ``append`` for an FP8 pool (uint8 bytes, modified in place)."""
+    lib = _load_fp8()
+    assert pool.dtype == np.uint8 and pool.flags["C_CONTIGUOUS"]
+    bt, pos = _i32(bt), _i32(pos)
+    k_new, v_new = _u16(k_new), _u16(v_new)
+    B, max_blocks = bt.shape
+    st = lib.oracle_append_fp8(_ptr(pool, ctypes.c_uint8), ctypes.byref(g), _ptr(bt, ctypes.c_int32), max_blocks,
+                               _ptr(pos, ctypes.c_int32), B, _ptr(k_new, ctypes.c_uint16),
+                               _ptr(v_new, ctypes.c_uint16), _ptr(q, ctypes.c_uint16) if q is not None else None,
+                               num_q_heads, float(theta))
+    _check(st, "oracle_append_fp8")
+    return q
+
+
+def decode_one_fp8(pool, g: PoolGeom, bt_row, L: int, q_row, kv_head: int, scale: float):
+    lib = _load_fp8()
+    bt_row, q_row = _i32(bt_row), _u16(q_row)
+    out = np.empty(g.head_dim, dtype=np.float64)
+    st = lib.oracle_decode_one_fp8(_ptr(pool, ctypes.c_uint8), ctypes.byref(g), _ptr(bt_row, ctypes.c_int32),
+                                   bt_row.size, int(L), _ptr(q_row, ctypes.c_uint16), int(kv_head), float(scale),
+                                   _ptr(out, ctypes.c_double), None)
+    _check(st, "oracle_decode_one_fp8")
+    return out
+
+
+def decode_fp8(pool, g: PoolGeom, bt, seq_lens, q, scale: float):
+    lib = _load_fp8()
+    bt, seq_lens, q = _i32(bt), _i32(seq_lens), _u16(q)
+    B, Hq, D = q.shape
+    out_bf16 = np.empty((B, Hq, D), dtype=np.uint16)
+    out_f64 = np.empty((B, Hq, D), dtype=np.float64)
+    st = lib.oracle_decode_fp8(_ptr(pool, ctypes.c_uint8), ctypes.byref(g), _ptr(bt, ctypes.c_int32), bt.shape[1],
+                               _ptr(seq_lens, ctypes.c_int32), B, _ptr(q, ctypes.c_uint16), Hq, float(scale),
+                               _ptr(out_bf16, ctypes.c_uint16), _ptr(out_f64, ctypes.c_double))
+    _check(st, "oracle_decode_fp8")
+    return out_bf16, out_f64

@@ -347,3 +347,223 @@ int oracle_decode_contiguous(const double *K, const double *V, int S, const int3
     free(s);
     return ORACLE_OK;
 }
+
+/* ------------------------------------------------------------------------ */
+/* FP8 KV pages ("从零构建大模型推理引擎" section 5.1: store the KV cache in low
+ * precision and dequantize before attention).  The page gives no scheme; the
+ * reading taken here:
+ *  - element format FP8 E4M3 without infinities (largest finite 448), round to
+ *    nearest even, saturating at +-448;
+ *  - one FP32 scale per (token, KV head) row of 64 values: scale = amax / 448
+ *    (FP32 division; 1 for an all-zero row), code = E4M3(x / scale) with x / scale
+ *    an FP32 division; the row's input is the BF16 value the BF16 path would store;
+ *  - page = codes [2 (K,V)][kv_heads][page_size][head_dim] (1 byte each) followed by
+ *    scales [2][kv_heads][page_size] FP32: 16384 + 1024 bytes for 8 x 16 x 64.    */
+
+uint8_t oracle_e4m3_from_double(double x)
+{
+    if (isnan(x))
+        return 0x7F;
+    uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    double a = fabs(x);
+    if (a >= 448.0)
+        return (uint8_t)(sign | 0x7E);  /* saturate to the largest finite value */
+    if (a < ldexp(1.0, -6)) {           /* subnormal spacing 2^-9; 8 quanta = 2^-6 (code 8) */
+        double n = rint(a / ldexp(1.0, -9));
+        return (uint8_t)(sign | (uint8_t)n);
+    }
+    int e;
+    (void)frexp(a, &e);
+    int exponent = e - 1;               /* a in [2^exponent, 2^(exponent+1)), exponent >= -6 */
+    double n = rint(a / ldexp(1.0, exponent - 3));  /* 8 .. 16 */
+    if (n >= 16.0) {
+        n = 8.0;
+        exponent += 1;
+    }
+    if (exponent > 8 || (exponent == 8 && n > 14.0))
+        return (uint8_t)(sign | 0x7E);
+    return (uint8_t)(sign | ((exponent + 7) << 3) | ((int)n - 8));
+}
+
+double oracle_e4m3_to_double(uint8_t c)
+{
+    double s = (c & 0x80) ? -1.0 : 1.0;
+    int e = (c >> 3) & 0xF, m = c & 7;
+    if (e == 15 && m == 7)
+        return NAN;
+    if (e == 0)
+        return s * ldexp((double)m, -9);
+    return s * ldexp((double)(8 + m), e - 10);
+}
+
+/* Quantize n BF16 values (FP32 arithmetic, as defined above). */
+void oracle_quantize_row_fp8(const uint16_t *row, int n, uint8_t *codes, float *scale_out)
+{
+    float amax = 0.0f;
+    for (int i = 0; i < n; ++i) {
+        float a = fabsf((float)oracle_bf16_to_double(row[i]));
+        if (a > amax)
+            amax = a;
+    }
+    float scale = amax > 0.0f ? amax / 448.0f : 1.0f;
+    for (int i = 0; i < n; ++i) {
+        float v = (float)oracle_bf16_to_double(row[i]) / scale;
+        codes[i] = oracle_e4m3_from_double((double)v);
+    }
+    *scale_out = scale;
+}
+
+int64_t oracle_fp8_page_bytes(const oracle_pool_geom *g)
+{
+    return (int64_t)2 * g->num_kv_heads * g->page_size * (g->head_dim + 4);
+}
+
+/* byte offset of a code / of a row's scale inside the FP8 pool */
+int64_t oracle_fp8_code_offset(const oracle_pool_geom *g, int page, int kv, int head, int slot, int dim)
+{
+    int64_t row = ((int64_t)kv * g->num_kv_heads + head) * g->page_size + slot;
+    return (int64_t)page * oracle_fp8_page_bytes(g) + row * g->head_dim + dim;
+}
+
+int64_t oracle_fp8_scale_offset(const oracle_pool_geom *g, int page, int kv, int head, int slot)
+{
+    int64_t row = ((int64_t)kv * g->num_kv_heads + head) * g->page_size + slot;
+    return (int64_t)page * oracle_fp8_page_bytes(g) + (int64_t)2 * g->num_kv_heads * g->page_size * g->head_dim +
+           row * 4;
+}
+
+static void fp8_store_row(uint8_t *pool, const oracle_pool_geom *g, int page, int kv, int head, int slot,
+                          const uint16_t *row)
+{
+    uint8_t codes[1024];
+    float scale;
+    oracle_quantize_row_fp8(row, g->head_dim, codes, &scale);
+    for (int d = 0; d < g->head_dim; ++d)
+        pool[oracle_fp8_code_offset(g, page, kv, head, slot, d)] = codes[d];
+    memcpy(pool + oracle_fp8_scale_offset(g, page, kv, head, slot), &scale, sizeof scale);
+}
+
+/* As oracle_append, storing each appended K (rotated, BF16) and V row quantized. */
+int oracle_append_fp8(uint8_t *pool, const oracle_pool_geom *g, const int32_t *bt, int max_blocks,
+                      const int32_t *pos, int B, const uint16_t *k_new, const uint16_t *v_new, uint16_t *q,
+                      int num_q_heads, double theta)
+{
+    int D = g->head_dim;
+    if (D > 1024)
+        return ORACLE_BAD_ARG;
+    double x[1024], y[1024];
+    uint16_t rot[1024];
+    for (int b = 0; b < B; ++b) {
+        int p = pos[b], page, slot;
+        int st = token_page(g, bt + (size_t)b * max_blocks, max_blocks, p, &page, &slot);
+        if (st != ORACLE_OK)
+            return st;
+        for (int h = 0; h < g->num_kv_heads; ++h) {
+            const uint16_t *k = k_new + ((size_t)b * g->num_kv_heads + h) * D;
+            for (int d = 0; d < D; ++d)
+                x[d] = oracle_bf16_to_double(k[d]);
+            oracle_rope_rotate(x, D, p, theta, y);
+            for (int d = 0; d < D; ++d)
+                rot[d] = oracle_bf16_from_double(y[d]);
+            fp8_store_row(pool, g, page, 0, h, slot, rot);
+            fp8_store_row(pool, g, page, 1, h, slot, v_new + ((size_t)b * g->num_kv_heads + h) * D);
+        }
+        if (q) {
+            for (int h = 0; h < num_q_heads; ++h) {
+                uint16_t *qh = q + ((size_t)b * num_q_heads + h) * D;
+                for (int d = 0; d < D; ++d)
+                    x[d] = oracle_bf16_to_double(qh[d]);
+                oracle_rope_rotate(x, D, p, theta, y);
+                for (int d = 0; d < D; ++d)
+                    qh[d] = oracle_bf16_from_double(y[d]);
+            }
+        }
+    }
+    return ORACLE_OK;
+}
+
+static double fp8_value(const uint8_t *pool, const oracle_pool_geom *g, int page, int kv, int head, int slot, int d)
+{
+    float scale;
+    memcpy(&scale, pool + oracle_fp8_scale_offset(g, page, kv, head, slot), sizeof scale);
+    return oracle_e4m3_to_double(pool[oracle_fp8_code_offset(g, page, kv, head, slot, d)]) * (double)scale;
+}
+
+/* Paged decode attention over FP8 pages: the same definition as oracle_decode_one,
+ * each K and V element dequantized as code * row scale (exact in FP64). */
+int oracle_decode_one_fp8(const uint8_t *pool, const oracle_pool_geom *g, const int32_t *bt_row, int max_blocks,
+                          int L, const uint16_t *q_row, int kv_head, double scale, double *out, double *weights)
+{
+    int D = g->head_dim;
+    if (L < 1 || L > max_blocks * g->page_size || kv_head < 0 || kv_head >= g->num_kv_heads)
+        return ORACLE_BAD_ARG;
+    double *s = (double *)malloc(sizeof(double) * (size_t)L);
+    if (!s)
+        return ORACLE_NO_MEMORY;
+    for (int t = 0; t < L; ++t) {
+        int page, slot;
+        int st = token_page(g, bt_row, max_blocks, t, &page, &slot);
+        if (st != ORACLE_OK) {
+            free(s);
+            return st;
+        }
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d)
+            dot += oracle_bf16_to_double(q_row[d]) * fp8_value(pool, g, page, 0, kv_head, slot, d);
+        s[t] = scale * dot;
+    }
+    double m = s[0];
+    for (int t = 1; t < L; ++t)
+        if (s[t] > m)
+            m = s[t];
+    double z = 0.0;
+    for (int t = 0; t < L; ++t) {
+        s[t] = exp(s[t] - m);
+        z += s[t];
+    }
+    for (int d = 0; d < D; ++d)
+        out[d] = 0.0;
+    for (int t = 0; t < L; ++t) {
+        int page = 0, slot = 0;
+        (void)token_page(g, bt_row, max_blocks, t, &page, &slot);
+        double w = s[t] / z;
+        if (weights)
+            weights[t] = w;
+        for (int d = 0; d < D; ++d)
+            out[d] += w * fp8_value(pool, g, page, 1, kv_head, slot, d);
+    }
+    free(s);
+    return ORACLE_OK;
+}
+
+int oracle_decode_fp8(const uint8_t *pool, const oracle_pool_geom *g, const int32_t *bt, int max_blocks,
+                      const int32_t *seq_lens, int B, const uint16_t *q, int num_q_heads, double scale,
+                      uint16_t *out_bf16, double *out_f64)
+{
+    int D = g->head_dim;
+    if (num_q_heads < g->num_kv_heads || num_q_heads % g->num_kv_heads != 0)
+        return ORACLE_BAD_ARG;
+    int group = num_q_heads / g->num_kv_heads;
+    double *o = (double *)malloc(sizeof(double) * (size_t)D);
+    if (!o)
+        return ORACLE_NO_MEMORY;
+    for (int b = 0; b < B; ++b) {
+        for (int h = 0; h < num_q_heads; ++h) {
+            size_t row = (size_t)b * num_q_heads + h;
+            int st = oracle_decode_one_fp8(pool, g, bt + (size_t)b * max_blocks, max_blocks, seq_lens[b],
+                                           q + row * D, h / group, scale, o, NULL);
+            if (st != ORACLE_OK) {
+                free(o);
+                return st;
+            }
+            for (int d = 0; d < D; ++d) {
+                if (out_bf16)
+                    out_bf16[row * D + d] = oracle_bf16_from_double(o[d]);
+                if (out_f64)
+                    out_f64[row * D + d] = o[d];
+            }
+        }
+    }
+    free(o);
+    return ORACLE_OK;
+}
