@@ -357,8 +357,9 @@ int oracle_decode_contiguous(const double *K, const double *V, int S, const int3
  *  - one FP32 scale per (token, KV head) row of 64 values: scale = amax / 448
  *    (FP32 division; 1 for an all-zero row), code = E4M3(x / scale) with x / scale
  *    an FP32 division; the row's input is the BF16 value the BF16 path would store;
- *  - page = codes [2 (K,V)][kv_heads][page_size][head_dim] (1 byte each) followed by
- *    scales [2][kv_heads][page_size] FP32: 16384 + 1024 bytes for 8 x 16 x 64.    */
+ *  - page = kv_heads units, one per KV head, each the codes [2 (K,V)][page_size]
+ *    [head_dim] (1 byte each) followed by the scales [2][page_size] FP32:
+ *    8 x (2048 + 128) = 17408 bytes for 8 x 16 x 64.                                */
 
 uint8_t oracle_e4m3_from_double(double x)
 {
@@ -418,18 +419,24 @@ int64_t oracle_fp8_page_bytes(const oracle_pool_geom *g)
     return (int64_t)2 * g->num_kv_heads * g->page_size * (g->head_dim + 4);
 }
 
+/* bytes of one KV head's unit inside an FP8 page */
+static int64_t fp8_unit_bytes(const oracle_pool_geom *g)
+{
+    return (int64_t)2 * g->page_size * (g->head_dim + 4);
+}
+
 /* byte offset of a code / of a row's scale inside the FP8 pool */
 int64_t oracle_fp8_code_offset(const oracle_pool_geom *g, int page, int kv, int head, int slot, int dim)
 {
-    int64_t row = ((int64_t)kv * g->num_kv_heads + head) * g->page_size + slot;
-    return (int64_t)page * oracle_fp8_page_bytes(g) + row * g->head_dim + dim;
+    int64_t row = (int64_t)kv * g->page_size + slot;
+    return (int64_t)page * oracle_fp8_page_bytes(g) + head * fp8_unit_bytes(g) + row * g->head_dim + dim;
 }
 
 int64_t oracle_fp8_scale_offset(const oracle_pool_geom *g, int page, int kv, int head, int slot)
 {
-    int64_t row = ((int64_t)kv * g->num_kv_heads + head) * g->page_size + slot;
-    return (int64_t)page * oracle_fp8_page_bytes(g) + (int64_t)2 * g->num_kv_heads * g->page_size * g->head_dim +
-           row * 4;
+    int64_t row = (int64_t)kv * g->page_size + slot;
+    return (int64_t)page * oracle_fp8_page_bytes(g) + head * fp8_unit_bytes(g) +
+           (int64_t)2 * g->page_size * g->head_dim + row * 4;
 }
 
 static void fp8_store_row(uint8_t *pool, const oracle_pool_geom *g, int page, int kv, int head, int slot,

@@ -78,10 +78,14 @@ def fp8_pool(num_pages):
     return np.full(num_pages * PAGE, 0xA5, dtype=np.uint8)
 
 
+UNIT = PAGE // HKV            # one KV head's codes [2][16][64] then scales [2][16]
+
+
 def fp8_views(pool):
-    pages = pool.reshape(-1, PAGE)
-    codes = pages[:, :CODES].reshape(-1, 2, HKV, PS, D)
-    scales = pages[:, CODES:].view(np.float32).reshape(-1, 2, HKV, PS)
+    """(codes [pages][2][heads][16][64], scales [pages][2][heads][16]) as views of ``pool``."""
+    units = pool.reshape(-1, HKV, UNIT)
+    codes = units[:, :, :CODES // HKV].reshape(-1, HKV, 2, PS, D).transpose(0, 2, 1, 3, 4)
+    scales = units[:, :, CODES // HKV:].view(np.float32).reshape(-1, HKV, 2, PS).transpose(0, 2, 1, 3)
     return codes, scales
 
 
@@ -137,5 +141,7 @@ def test_fp8_append_matches_bf16_append_then_quantize():
             for kv in (0, 1):
                 c, s = oracle.quantize_row_fp8(R[page, kv, h, slot])
                 assert np.array_equal(codes_v[page, kv, h, slot], c) and scales_v[page, kv, h, slot] == s
-    assert oracle.fp8_code_offset(g, 1, 1, 2, 3, 4) == PAGE + ((1 * HKV + 2) * PS + 3) * D + 4
-    assert oracle.fp8_scale_offset(g, 1, 1, 2, 3) == PAGE + CODES + ((1 * HKV + 2) * PS + 3) * 4
+    # head-major page: head 2's unit starts at 2 * 2176; V row 3 of it at 16 rows of 64 + 3 rows
+    assert oracle.fp8_code_offset(g, 1, 1, 2, 3, 4) == PAGE + 2 * UNIT + (PS + 3) * D + 4
+    assert oracle.fp8_scale_offset(g, 1, 1, 2, 3) == PAGE + 2 * UNIT + 2 * PS * D + (PS + 3) * 4
+    assert UNIT == 2176 and oracle.fp8_code_offset(g, 0, 1, 7, 15, 63) + 1 + 2 * PS * 4 == PAGE
