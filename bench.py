@@ -245,13 +245,14 @@ def cpu_baseline(w, seconds: float, seed: int) -> dict:
 # --------------------------------------------------------------------------- arms
 
 def config_block(w, args, variant_name: str, graph: bool) -> dict:
-    kv = w.kv_bytes_per_step()
+    kv = w.kv_bytes_per_step(getattr(args, "kv", "bf16"))
     return {"workload": f"{args.config}: {CONFIG_TEXT[args.config]}", "batch": w.batch, "layers": w.layers,
             "seq_len_max": int(w.seq_lens.max()), "seq_len_mean": float(w.seq_lens.mean()),
             "pages_per_chunk": args.pages_per_chunk, "kernel_variant": variant_name, "cuda_graph": graph,
             "path": getattr(args, "path", "fused"), "pdl": not getattr(args, "no_pdl", False),
             "schedule": getattr(args, "schedule", "auto"), "ring": getattr(args, "ring", 0),
             "early_trigger": getattr(args, "early_trigger", False),
+            "kv_pages": getattr(args, "kv", "bf16"),
             "kv_bytes_per_step": kv,
             "l2": f"inputs larger than L2 ({kv / 1e9:.2f} GB of KV per step vs {L2_BYTES / 1e6:.0f} MB L2), "
                   "no flush", "seed": args.seed}
@@ -372,7 +373,7 @@ def run_pkv(args):
     variant_name = args.variant
     dw = harness.setup(args.config, replica_seed(args.seed, rank), args.pages_per_chunk, VARIANTS[variant_name],
                        layers=args.layers, fused=args.path == "fused", pdl=not args.no_pdl,
-                       schedule=args.schedule, ring=args.ring, early_trigger=args.early_trigger)
+                       schedule=args.schedule, ring=args.ring, early_trigger=args.early_trigger, kv=args.kv)
     w = dw.w
     harness.warm(dw, 2)
     dw.reset_q()
@@ -432,7 +433,7 @@ def run_pkv(args):
 
     # dominant kernel: the attention launches (split + merge), timed inside the graphs
     split_ms = [s.elapsed_time(e) for cap in timed_ev for (s, e) in cap.split_events]
-    kv_step = w.kv_bytes_per_step()
+    kv_step = w.kv_bytes_per_step(args.kv)
     kv_launch = kv_step // w.layers
     peak, peak_src = hbm_peak()
     steps_per_s = args.steps / (elapsed_ms / 1e3)
@@ -442,8 +443,11 @@ def run_pkv(args):
         avg = sum(split_ms) / len(split_ms)
         achieved = kv_launch / (avg / 1e3) / 1e9
         roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                    "traffic": measured_traffic(args.config, args.path, variant_name, args.pages_per_chunk, args.ring),
-                    "kernel": (f"fused decode step kernel (append + attention + merge), variant {variant_name}"
+                    "traffic": (measured_traffic(args.config, args.path, variant_name, args.pages_per_chunk,
+                                                 args.ring) if args.kv == "bf16" else None),
+                    "kernel": ("FP8-page decode step: quantizing append + FP8 split kernel + merge launches"
+                               if args.kv == "fp8" else
+                               f"fused decode step kernel (append + attention + merge), variant {variant_name}"
                                if args.path == "fused" else
                                f"paged decode attention launch (split + merge), variant {variant_name}"),
                     "timing": "external events around every launch in a second pass of the same steps",
@@ -461,7 +465,8 @@ def run_pkv(args):
 
     line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if args.kv == "bf16" else "fp8e4m3 KV, f16 MMA, f32 softmax", "data": "synthetic",
             "config": config_block(w, args, variant_name, True),
             "hbm_frac_of_peak": value / world / peak, "steps_per_s": steps_per_s,
             "tokens_per_s": w.batch * steps_per_s * world,
@@ -503,7 +508,7 @@ def measure_e2e(dw, args, world, device):
     ms = reduce_max(start.elapsed_time(end), world, device)
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
     d2h = out_host.numel() * out_host.element_size()
-    return {"value": dw.w.kv_bytes_per_step() * n * world / (ms / 1e3) / 1e9, "unit": "GB/s",
+    return {"value": dw.w.kv_bytes_per_step(dw.eng.kv) * n * world / (ms / 1e3) / 1e9, "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n, "ms_per_step": ms / n,
             "path": "DecodeEngine.run_host (pinned host in/out, copies on the kernels' stream, CUDA graph)"}
 
@@ -530,6 +535,8 @@ def main(argv=None):
                     help="fused path: one CTA per unit, or persistent CTAs walking the units")
     ap.add_argument("--ring", type=int, default=None, choices=[2, 3, 4],
                     help="grid schedule: TMA stages per warp (default: the measured best for the workload)")
+    ap.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
+                    help="KV page format: BF16 (the engine's) or FP8 E4M3 with per-row scales")
     ap.add_argument("--seed", type=int, default=12)
     ap.add_argument("--layers", type=int, default=None, help="override the layer count (small profiling runs)")
     ap.add_argument("--steps-per-graph", type=int, default=25)
@@ -542,7 +549,7 @@ def main(argv=None):
     if args.pages_per_chunk is None:
         args.pages_per_chunk = DEFAULT_CHUNK[args.config]
     if args.ring is None:
-        args.ring = DEFAULT_RING[args.config]
+        args.ring = DEFAULT_RING[args.config] if args.kv == "bf16" else 0
     if args.impl == "reference":
         return run_reference(args)
     if args.config == "trace":

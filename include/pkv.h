@@ -106,6 +106,29 @@ typedef struct pkv_pool pkv_pool; /* opaque, host side */
 int pkv_pool_create(void *dev_slab, size_t slab_bytes, int page_size, int num_kv_heads, int head_dim,
                     uint64_t seed, pkv_pool **out);
 
+/* KV storage formats of a pool */
+#define PKV_KV_BF16 0
+#define PKV_KV_FP8 1 /* FP8 E4M3 codes + one FP32 scale per (token, KV head) row */
+#define PKV_PAGE_BYTES_FP8 (2 * PKV_NUM_KV_HEADS * PKV_PAGE_SIZE * (PKV_HEAD_DIM + 4)) /* 17408 */
+
+/* As pkv_pool_create, for a pool of FP8 pages ("从零构建大模型推理引擎：KV缓存、算子融合与量化优化实战",
+ * section 5.1:
+ * keep the KV cache in low precision and dequantize before attention; the scheme
+ * is this library's reading).  A page is 17408 bytes: 8 units of 2176 bytes, one
+ * per KV head, each the codes [2 (K,V)][16 slots][64 dims] (one byte each, E4M3
+ * without infinities, largest 448) followed by the row scales [2][16] FP32, so that
+ * one (page, KV head) is one contiguous copy.  A row of 64 values x is stored
+ * as scale = amax|x| / 448 (FP32; 1 for an all-zero row) and codes
+ * E4M3_rne_satfinite(x / scale) (FP32 division); x is the BF16 value the BF16 path
+ * would store (the rotated key, or the value).  Every entry point below accepts
+ * an FP8 pool: appends and prefills quantize, attention dequantizes (codes are
+ * exact in FP16; K scales multiply the scores, V scales the softmax weights).
+ * The SIMT decode variant is not provided for FP8 (PKV_ERR_UNSUPPORTED). */
+int pkv_pool_create_fp8(void *dev_slab, size_t slab_bytes, uint64_t seed, pkv_pool **out);
+
+/* The pool's KV format (PKV_KV_BF16 or PKV_KV_FP8), or a negative status. */
+int pkv_pool_kv_format(const pkv_pool *pool);
+
 /* Destroy the host object (never touches the slab).  NULL is accepted. */
 int pkv_pool_destroy(pkv_pool *pool);
 
@@ -120,8 +143,10 @@ int pkv_pool_alloc(pkv_pool *pool, int n, int32_t *ids_out);
  * is PKV_ERR_DOUBLE_FREE; on error nothing is freed. */
 int pkv_pool_free(pkv_pool *pool, int n, const int32_t *ids);
 
-/* Report the slab's K base, V base (= K base + 16 KiB), page stride in bytes,
- * page count and free-page count.  Any output pointer may be NULL. */
+/* Report the slab's K base, V base (= K base + 16 KiB; FP8 pools: head 0's V
+ * codes, K base + 1 KiB, with the heads' units 2176 bytes apart), page stride in
+ * bytes (32768; FP8 pools 17408), page count and free-page count.  Any output
+ * pointer may be NULL. */
 int pkv_pool_info(const pkv_pool *pool, void **k_base, void **v_base, int64_t *page_stride_bytes,
                   int *num_pages, int *num_free);
 
@@ -318,7 +343,11 @@ size_t pkv_decode_step_workspace_bytes(int B, int max_blocks, int pages_per_chun
  * layer's cached pages; the caller must therefore not have an immediately
  * preceding kernel on the stream write those three (block tables of different
  * layers must not share pages -- pkv_block_tables_build never does).
- * Device checks as pkv_decode_attention, plus seq_len > max_pos. */
+ * Device checks as pkv_decode_attention, plus seq_len > max_pos.
+ * FP8 pools: the step runs as the quantizing append followed by the FP8 split
+ * (and merge) kernels -- two or three launches in stream order, same results as
+ * the separate calls; PKV_STEP_PERSISTENT / PKV_STEP_WS / PKV_STEP_RING /
+ * PKV_STEP_EARLY_TRIGGER and the SIMT variant return PKV_ERR_UNSUPPORTED. */
 int pkv_decode_step(const pkv_pool *pool, const uint16_t *k_new, const uint16_t *v_new, uint16_t *q,
                     const int32_t *bt_dev, int max_blocks, const int32_t *seq_lens_dev, int B,
                     const float *rope_table, int max_pos, float scale, int pages_per_chunk, void *workspace,

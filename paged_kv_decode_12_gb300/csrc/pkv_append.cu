@@ -93,6 +93,9 @@ extern "C" int pkv_append_rope(const pkv_pool *pool, const uint16_t *k_new, cons
          reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(rope_table)) & 15u)
         return PKV_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    if (pool->kv_format == PKV_KV_FP8)
+        return fp8_append_rope(pool, k_new, v_new, q, bt_dev, max_blocks, pos_dev, 0, B, rope_table, max_pos,
+                               dev_err_flag, s);
     append_rope_kernel<<<B, kAppendThreads, 0, s>>>(reinterpret_cast<uint16_t *>(pool->slab), pool->num_pages,
                                                     k_new, v_new, q, bt_dev, max_blocks, pos_dev,
                                                     reinterpret_cast<const float4 *>(rope_table), max_pos,
@@ -165,6 +168,9 @@ extern "C" int pkv_prefill_append(const pkv_pool *pool, const uint16_t *k, const
         15u)
         return PKV_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    if (pool->kv_format == PKV_KV_FP8)
+        return fp8_prefill_append(pool, k, v, bt_rows, max_blocks, layers, start_pos, T, rope_table, max_pos,
+                                  dev_err_flag, s);
     prefill_append_kernel<<<dim3(T, layers), kPrefillThreads, 0, s>>>(
         reinterpret_cast<uint16_t *>(pool->slab), pool->num_pages, k, v, bt_rows, max_blocks, start_pos, T,
         reinterpret_cast<const float2 *>(rope_table), max_pos, dev_err_flag);

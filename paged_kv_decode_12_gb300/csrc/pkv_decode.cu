@@ -209,6 +209,15 @@ int launch_split(const CUtensorMap *tmap, const SplitArgs &a, int B, cudaStream_
 }
 
 }  // namespace
+
+int launch_decode_merge(const int32_t *seq_lens, int max_blocks, int pages_per_chunk, const float2 *part_ml,
+                        const float *part_o, int max_chunks, uint16_t *out, int B, cudaStream_t s)
+{
+    decode_merge_kernel<<<dim3(B, kHkv), kThreads, 0, s>>>(seq_lens, max_blocks, pages_per_chunk, part_ml, part_o,
+                                                            max_chunks, out);
+    return status_from_cuda(cudaGetLastError());
+}
+
 }  // namespace pkv
 
 extern "C" size_t pkv_decode_workspace_bytes(int B, int max_blocks, int pages_per_chunk)
@@ -236,6 +245,8 @@ extern "C" int pkv_decode_attention_variant(const pkv_pool *pool, const uint16_t
         return PKV_ERR_INVALID_ARG;
     if (variant < PKV_DECODE_DEFAULT || variant > PKV_DECODE_MMA)
         return PKV_ERR_INVALID_ARG;
+    if (pool->kv_format == PKV_KV_FP8 && variant == PKV_DECODE_SIMT)
+        return PKV_ERR_UNSUPPORTED;  // FP8 pages have the MMA policy only
     if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out)) & 15u)
         return PKV_ERR_INVALID_ARG;
     const int max_chunks = (max_blocks + pages_per_chunk - 1) / pages_per_chunk;
@@ -265,12 +276,16 @@ extern "C" int pkv_decode_attention_variant(const pkv_pool *pool, const uint16_t
     a.err = dev_err_flag;
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
     const int v = variant == PKV_DECODE_DEFAULT ? PKV_DECODE_MMA : variant;
-    int st = v == PKV_DECODE_SIMT ? launch_split<SimtWarp>(tmap, a, B, s) : launch_split<MmaWarp>(tmap, a, B, s);
+    int st;
+    if (pool->kv_format == PKV_KV_FP8) {
+        st = fp8_decode_split(pool, q, bt_dev, max_blocks, seq_lens_dev, B, a.scale_log2, pages_per_chunk,
+                              a.part_ml, a.part_o, max_chunks, out, dev_err_flag, s);
+    } else {
+        st = v == PKV_DECODE_SIMT ? launch_split<SimtWarp>(tmap, a, B, s) : launch_split<MmaWarp>(tmap, a, B, s);
+    }
     if (st != PKV_OK || max_chunks == 1)
         return st;
-    decode_merge_kernel<<<dim3(B, kHkv), kThreads, 0, s>>>(seq_lens_dev, max_blocks, pages_per_chunk, a.part_ml,
-                                                            a.part_o, max_chunks, out);
-    return status_from_cuda(cudaGetLastError());
+    return launch_decode_merge(seq_lens_dev, max_blocks, pages_per_chunk, a.part_ml, a.part_o, max_chunks, out, B, s);
 }
 
 extern "C" int pkv_decode_attention(const pkv_pool *pool, const uint16_t *q, const int32_t *bt_dev, int max_blocks,

@@ -54,17 +54,18 @@ const char *pkv_status_string(int status)
     }
 }
 
-int pkv_pool_create(void *dev_slab, size_t slab_bytes, int page_size, int num_kv_heads, int head_dim,
-                    uint64_t seed, pkv_pool **out)
+}  // extern "C"
+
+namespace {
+
+int create_pool(void *dev_slab, size_t slab_bytes, int kv_format, size_t page_bytes, uint64_t seed, pkv_pool **out)
 {
     if (!out)
         return PKV_ERR_INVALID_ARG;
     *out = nullptr;
     if (!dev_slab || (reinterpret_cast<uintptr_t>(dev_slab) & 15u) != 0)
         return PKV_ERR_INVALID_ARG;
-    if (page_size != PKV_PAGE_SIZE || num_kv_heads != PKV_NUM_KV_HEADS || head_dim != PKV_HEAD_DIM)
-        return PKV_ERR_UNSUPPORTED;
-    size_t pages = slab_bytes / PKV_PAGE_BYTES;
+    size_t pages = slab_bytes / page_bytes;
     if (pages < 1 || pages > (size_t)INT32_MAX)
         return PKV_ERR_INVALID_ARG;
     pkv_pool *p = new (std::nothrow) pkv_pool();
@@ -73,6 +74,8 @@ int pkv_pool_create(void *dev_slab, size_t slab_bytes, int page_size, int num_kv
     p->slab = static_cast<char *>(dev_slab);
     p->slab_bytes = slab_bytes;
     p->num_pages = (int32_t)pages;
+    p->kv_format = kv_format;
+    p->page_bytes = page_bytes;
     try {
         p->free_list.resize(pages);
         p->allocated.assign(pages, 0);
@@ -91,6 +94,33 @@ int pkv_pool_create(void *dev_slab, size_t slab_bytes, int page_size, int num_kv
     }
     *out = p;
     return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pkv_pool_create(void *dev_slab, size_t slab_bytes, int page_size, int num_kv_heads, int head_dim,
+                    uint64_t seed, pkv_pool **out)
+{
+    if (!out)
+        return PKV_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (!dev_slab || (reinterpret_cast<uintptr_t>(dev_slab) & 15u) != 0)
+        return PKV_ERR_INVALID_ARG;
+    if (page_size != PKV_PAGE_SIZE || num_kv_heads != PKV_NUM_KV_HEADS || head_dim != PKV_HEAD_DIM)
+        return PKV_ERR_UNSUPPORTED;
+    return create_pool(dev_slab, slab_bytes, PKV_KV_BF16, PKV_PAGE_BYTES, seed, out);
+}
+
+int pkv_pool_create_fp8(void *dev_slab, size_t slab_bytes, uint64_t seed, pkv_pool **out)
+{
+    return create_pool(dev_slab, slab_bytes, PKV_KV_FP8, PKV_PAGE_BYTES_FP8, seed, out);
+}
+
+int pkv_pool_kv_format(const pkv_pool *pool)
+{
+    return pool ? pool->kv_format : PKV_ERR_INVALID_ARG;
 }
 
 int pkv_pool_destroy(pkv_pool *pool)
@@ -150,9 +180,9 @@ int pkv_pool_info(const pkv_pool *pool, void **k_base, void **v_base, int64_t *p
     if (k_base)
         *k_base = pool->slab;
     if (v_base)
-        *v_base = pool->slab + PKV_PAGE_BYTES / 2;
+        *v_base = pool->slab + (pool->kv_format == PKV_KV_FP8 ? pkv::kPage * pkv::kD : PKV_PAGE_BYTES / 2);
     if (page_stride_bytes)
-        *page_stride_bytes = PKV_PAGE_BYTES;
+        *page_stride_bytes = (int64_t)pool->page_bytes;
     if (num_pages)
         *num_pages = pool->num_pages;
     if (num_free)
@@ -250,15 +280,28 @@ const CUtensorMap *pool_tensor_map(const pkv_pool *cpool)
             return nullptr;
         encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     }
-    // dims innermost first: dim, slot, KV head, K/V, page
-    cuuint64_t dims[5] = {(cuuint64_t)kD, (cuuint64_t)kPage, (cuuint64_t)kHkv, 2, (cuuint64_t)pool->num_pages};
-    cuuint64_t strides[4] = {kD * 2, (cuuint64_t)kPage * kD * 2, (cuuint64_t)kHkv * kPage * kD * 2,
-                             (cuuint64_t)PKV_PAGE_BYTES};
-    cuuint32_t box[5] = {(cuuint32_t)kD, (cuuint32_t)kPage, 1, 2, 1};
+    CUresult r;
     cuuint32_t estride[5] = {1, 1, 1, 1, 1};
-    CUresult r = encode(&pool->tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, pool->slab, dims, strides, box,
-                        estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (pool->kv_format == PKV_KV_FP8) {
+        // dims innermost first: byte of a 64-byte row, row (32 code rows + 2 scale
+        // rows), KV head, page; one box is one head's 2176-byte unit
+        cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)(kFp8Unit / kD), (cuuint64_t)kHkv,
+                              (cuuint64_t)pool->num_pages};
+        cuuint64_t strides[3] = {(cuuint64_t)kD, (cuuint64_t)kFp8Unit, (cuuint64_t)pool->page_bytes};
+        cuuint32_t box[4] = {(cuuint32_t)kD, (cuuint32_t)(kFp8Unit / kD), 1, 1};
+        r = encode(&pool->tmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, pool->slab, dims, strides, box, estride,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+        // dims innermost first: dim, slot, KV head, K/V, page
+        cuuint64_t dims[5] = {(cuuint64_t)kD, (cuuint64_t)kPage, (cuuint64_t)kHkv, 2, (cuuint64_t)pool->num_pages};
+        cuuint64_t strides[4] = {kD * 2, (cuuint64_t)kPage * kD * 2, (cuuint64_t)kHkv * kPage * kD * 2,
+                                 (cuuint64_t)PKV_PAGE_BYTES};
+        cuuint32_t box[5] = {(cuuint32_t)kD, (cuuint32_t)kPage, 1, 2, 1};
+        r = encode(&pool->tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, pool->slab, dims, strides, box, estride,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
     if (r != CUDA_SUCCESS)
         return nullptr;
     pool->tmap_ready = true;

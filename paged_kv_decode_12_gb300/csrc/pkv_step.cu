@@ -955,6 +955,31 @@ int launch_ws(const CUtensorMap *tmap, const StepArgs &a, int B, cudaStream_t s,
     return status_from_cuda(cudaLaunchKernelEx(&cfg, kernel, *tmap, a, B, work_counter, work_counter + 1));
 }
 
+// FP8 pools: the quantizing append (pos = seq_len - 1) then the FP8 split kernel
+// and, for sequences of several chunks, the merge; the workspace's counter region
+// is left untouched.
+int fp8_step(const pkv_pool *pool, const uint16_t *k_new, const uint16_t *v_new, uint16_t *q, const int32_t *bt,
+             int max_blocks, const int32_t *seq_lens, int B, const float *rope, int max_pos, float scale, int ppc,
+             char *ws, uint16_t *out, int32_t *err, cudaStream_t s, int options)
+{
+    const int variant = options & 0xff;
+    if (variant == PKV_DECODE_SIMT ||
+        (options & (PKV_STEP_PERSISTENT | PKV_STEP_WS | PKV_STEP_RING_MASK | PKV_STEP_EARLY_TRIGGER)))
+        return PKV_ERR_UNSUPPORTED;
+    const int max_chunks = (max_blocks + ppc - 1) / ppc;
+    const size_t counters_bytes = align256(((size_t)B * kHkv + 2) * sizeof(int));
+    const size_t ml_bytes = align256((size_t)B * kHq * max_chunks * sizeof(float2));
+    float2 *part_ml = reinterpret_cast<float2 *>(ws + counters_bytes);
+    float *part_o = reinterpret_cast<float *>(ws + counters_bytes + ml_bytes);
+    int st = fp8_append_rope(pool, k_new, v_new, q, bt, max_blocks, seq_lens, -1, B, rope, max_pos, err, s);
+    if (st == PKV_OK)
+        st = fp8_decode_split(pool, q, bt, max_blocks, seq_lens, B, scale * 1.4426950408889634f, ppc, part_ml,
+                              part_o, max_chunks, out, err, s);
+    if (st != PKV_OK || max_chunks == 1)
+        return st;
+    return launch_decode_merge(seq_lens, max_blocks, ppc, part_ml, part_o, max_chunks, out, B, s);
+}
+
 }  // namespace
 }  // namespace pkv
 
@@ -994,6 +1019,10 @@ extern "C" int pkv_decode_step(const pkv_pool *pool, const uint16_t *k_new, cons
         return PKV_ERR_INVALID_ARG;
     if (workspace_bytes < pkv_decode_step_workspace_bytes(B, max_blocks, pages_per_chunk))
         return PKV_ERR_WORKSPACE_TOO_SMALL;
+    if (pool->kv_format == PKV_KV_FP8)
+        return fp8_step(pool, k_new, v_new, q, bt_dev, max_blocks, seq_lens_dev, B, rope_table, max_pos, scale,
+                        pages_per_chunk, static_cast<char *>(workspace), out, dev_err_flag,
+                        static_cast<cudaStream_t>(cuda_stream), options);
     const CUtensorMap *tmap = pool_tensor_map(pool);
     if (!tmap)
         return PKV_ERR_CUDA;

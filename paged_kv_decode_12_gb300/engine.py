@@ -29,13 +29,21 @@ class DecodeEngine:
     def __init__(self, num_pages: int, layers: int, batch: int, max_blocks: int = wl.MAX_BLOCKS,
                  pages_per_chunk: int = 16, variant: int = pkv.PKV_DECODE_DEFAULT, max_pos: int = wl.MAX_CONTEXT,
                  theta: float = wl.ROPE_THETA, pool_seed: int = 0, device: str = "cuda", fused: bool = True,
-                 pdl: bool = True, schedule: str = "auto", ring: int = 0, early_trigger: bool = False):
+                 pdl: bool = True, schedule: str = "auto", ring: int = 0, early_trigger: bool = False,
+                 kv: str = "bf16"):
+        if kv not in ("bf16", "fp8"):
+            raise ValueError(f"kv must be 'bf16' or 'fp8', not {kv!r}")
+        self.kv = kv
         self.device = torch.device(device)
         self.layers, self.batch, self.max_blocks = layers, batch, max_blocks
         self.pages_per_chunk, self.variant, self.max_pos = pages_per_chunk, variant, max_pos
         self.scale = 1.0 / math.sqrt(wl.HEAD_DIM)
-        self.slab = torch.empty(num_pages * pkv.PKV_PAGE_BYTES, dtype=torch.uint8, device=self.device)
-        self.pool = pkv.pkv_pool_create(self.slab, self.slab.numel(), seed=pool_seed)
+        self.page_bytes = pkv.PKV_PAGE_BYTES_FP8 if kv == "fp8" else pkv.PKV_PAGE_BYTES
+        self.slab = torch.empty(num_pages * self.page_bytes, dtype=torch.uint8, device=self.device)
+        if kv == "fp8":
+            self.pool = pkv.pkv_pool_create_fp8(self.slab, self.slab.numel(), seed=pool_seed)
+        else:
+            self.pool = pkv.pkv_pool_create(self.slab, self.slab.numel(), seed=pool_seed)
         self.num_pages = num_pages
         self.rope = torch.empty(max_pos * (wl.HEAD_DIM // 2) * 2, dtype=torch.float32, device=self.device)
         pkv.pkv_rope_table_init(theta, max_pos, wl.HEAD_DIM // 2, self.rope)
@@ -49,14 +57,30 @@ class DecodeEngine:
         self.fused = fused
         self.step_options = (variant | (0 if pdl else pkv.PKV_STEP_NO_PDL) | SCHEDULES[schedule]
                              | pkv.PKV_STEP_RING(ring) | (pkv.PKV_STEP_EARLY_TRIGGER if early_trigger else 0))
+        if kv == "fp8" and (schedule in ("persistent", "ws") or ring or early_trigger):
+            raise ValueError("FP8 pools run the step as append + split kernels: no schedule, ring or trigger "
+                             "options")
         self.bt = None
         self.bt_host = None
 
     # ------------------------------------------------------------------ setup
     def pool_view(self) -> torch.Tensor:
-        """The slab as BF16 [pages][2 (K, V)][8 KV heads][16 slots][64 dims]."""
+        """The slab as BF16 [pages][2 (K, V)][8 KV heads][16 slots][64 dims] (BF16 pools)."""
+        if self.kv != "bf16":
+            raise ValueError("pool_view is the BF16 layout; use fp8_views for an FP8 pool")
         return self.slab.view(torch.bfloat16).view(self.num_pages, 2, wl.NUM_KV_HEADS, wl.PAGE_SIZE,
                                                    wl.HEAD_DIM)
+
+    def fp8_views(self):
+        """(codes uint8 [pages][2][8][16][64], scales float32 [pages][2][8][16]) of an FP8 pool."""
+        if self.kv != "fp8":
+            raise ValueError("fp8_views needs an FP8 pool")
+        # a page is one 2176-byte unit per KV head: codes [2][16][64], then scales [2][16]
+        H, P, D = wl.NUM_KV_HEADS, wl.PAGE_SIZE, wl.HEAD_DIM
+        units = self.slab.view(self.num_pages, H, self.page_bytes // H)
+        codes = units[:, :, :2 * P * D].view(self.num_pages, H, 2, P, D).permute(0, 2, 1, 3, 4)
+        scales = units[:, :, 2 * P * D:].view(torch.float32).view(self.num_pages, H, 2, P).permute(0, 2, 1, 3)
+        return codes, scales
 
     def build_tables(self, seq_lens) -> np.ndarray:
         """Allocate pages for every (layer, sequence) and upload the block tables."""

@@ -373,3 +373,40 @@ def pkv_prefill_append(pool, k, v, bt_rows_dev, max_blocks: int, layers: int, st
     _check(lib().pkv_prefill_append(pool, _ptr(k), _ptr(v), _ptr(bt_rows_dev), max_blocks, layers, start_pos, T,
                                     _ptr(rope_table), max_pos, _ptr(dev_err_flag), _stream(stream)),
            "pkv_prefill_append")
+
+
+# ---------------------------------------------------------------------------- FP8 pages
+
+PKV_KV_BF16 = 0
+PKV_KV_FP8 = 1
+PKV_PAGE_BYTES_FP8 = 2 * PKV_NUM_KV_HEADS * PKV_PAGE_SIZE * (PKV_HEAD_DIM + 4)
+
+EXPORTED = EXPORTED + ("pkv_pool_create_fp8", "pkv_pool_kv_format")
+
+_lib_sched = lib
+
+
+def lib():  # noqa: F811 -- extends the loader with the FP8 pool signatures
+    L = _lib_sched()
+    if not getattr(L, "_pkv_fp8_bound", False):
+        L.pkv_pool_create_fp8.argtypes = [_vp, ctypes.c_size_t, ctypes.c_uint64, ctypes.POINTER(_vp)]
+        L.pkv_pool_create_fp8.restype = ctypes.c_int
+        L.pkv_pool_kv_format.argtypes = [_vp]
+        L.pkv_pool_kv_format.restype = ctypes.c_int
+        L._pkv_fp8_bound = True
+    return L
+
+
+def pkv_pool_create_fp8(dev_slab, slab_bytes: int, seed: int = 0):
+    """Pool of FP8 E4M3 pages (codes + per-row FP32 scales); opaque handle."""
+    out = ctypes.c_void_p()
+    _check(lib().pkv_pool_create_fp8(_ptr(dev_slab), int(slab_bytes), int(seed) & (2**64 - 1), ctypes.byref(out)),
+           "pkv_pool_create_fp8")
+    return out
+
+
+def pkv_pool_kv_format(pool) -> int:
+    st = lib().pkv_pool_kv_format(pool)
+    if st < 0:
+        raise PkvError(st, "pkv_pool_kv_format")
+    return st

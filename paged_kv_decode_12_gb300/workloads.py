@@ -39,9 +39,15 @@ ROPE_THETA = 500000.0
 DEFAULT_SEED = 12
 
 
+PAGE_BYTES_FP8 = 2 * NUM_KV_HEADS * PAGE_SIZE * (HEAD_DIM + 4)   # E4M3 codes + FP32 row scales: 17 KiB
+
+
 def kv_bytes_per_token(layers: int, kv_heads: int = NUM_KV_HEADS, head_dim: int = HEAD_DIM,
-                       elem_bytes: int = 2) -> int:
-    """KV-cache bytes one token adds: K and V, every layer and KV head."""
+                       elem_bytes: int = 2, kv: str = "bf16") -> int:
+    """KV-cache bytes one token adds: K and V, every layer and KV head (FP8 pages:
+    one code byte per value plus a 4-byte scale per row)."""
+    if kv == "fp8":
+        return 2 * layers * kv_heads * (head_dim + 4)
     return 2 * layers * kv_heads * head_dim * elem_bytes
 
 
@@ -63,9 +69,9 @@ class Workload:
     def positions(self) -> np.ndarray:
         return (self.seq_lens - 1).astype(np.int32)
 
-    def kv_bytes_per_step(self) -> int:
+    def kv_bytes_per_step(self, kv: str = "bf16") -> int:
         """KV bytes read by one pass over all layers: every cached token's K and V once."""
-        return int(self.seq_lens.astype(np.int64).sum()) * kv_bytes_per_token(self.layers)
+        return int(self.seq_lens.astype(np.int64).sum()) * kv_bytes_per_token(self.layers, kv=kv)
 
     def pages_per_layer(self) -> int:
         return int(sum(math.ceil(int(L) / PAGE_SIZE) for L in self.seq_lens))
@@ -170,6 +176,32 @@ def scale_key_rows_(pool_bf16, frac: float, seed: int):
         keys = pool_bf16[p0:p1, 0]
         keys.mul_(torch.where(mask, 8.0, 1.0).to(keys.dtype).unsqueeze(-1))
     return pool_bf16
+
+
+def fill_fp8_pages_(codes, scales, seed: int, key_outlier_frac: float = 0.0):
+    """Fill an FP8 pool's codes (uint8 [pages][2][Hkv][P][D]) and row scales (float32
+    [pages][2][Hkv][P]) in place with seeded draws shaped like quantized N(0,1) rows:
+    codes are N(0, 128^2) draws converted to E4M3 by torch's float8_e4m3fn dtype
+    (clamped to +-448 first), scales uniform in [0.005, 0.009] (about 3/448, the
+    scale of a 64-value N(0,1) row).  A ``key_outlier_frac`` share of key rows get
+    8x scales."""
+    import torch
+
+    g = torch.Generator(device=codes.device)
+    g.manual_seed(seed)
+    pages = codes.shape[0]
+    step = 4096
+    for p0 in range(0, pages, step):
+        p1 = min(p0 + step, pages)
+        x = torch.randn(codes[p0:p1].shape, generator=g, device=codes.device, dtype=torch.float32) * 128.0
+        codes[p0:p1].copy_(x.clamp_(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8))
+        u = torch.rand(scales[p0:p1].shape, generator=g, device=codes.device, dtype=torch.float32)
+        s = 0.005 + 0.004 * u
+        if key_outlier_frac > 0:
+            mask = torch.rand((p1 - p0, NUM_KV_HEADS, PAGE_SIZE), generator=g, device=codes.device) < key_outlier_frac
+            s[:, 0] = torch.where(mask, s[:, 0] * 8.0, s[:, 0])
+        scales[p0:p1].copy_(s)
+    return codes, scales
 
 
 # --------------------------------------------------------------------------- trace

@@ -177,3 +177,43 @@ def test_launch_entry_points_validate_before_any_cuda_call():
         pkv.pkv_rope_table_init(500000.0, 2048, 16, dummy, 0)
     assert e.value.status == pkv.PKV_ERR_INVALID_ARG
     pkv.pkv_pool_destroy(p)
+
+
+def test_fp8_pool_geometry_and_format():
+    assert pkv.PKV_PAGE_BYTES_FP8 == 17408
+    p = pkv.pkv_pool_create_fp8(FAKE_SLAB, 10 * pkv.PKV_PAGE_BYTES_FP8 + 100, seed=3)
+    info = pkv.pkv_pool_info(p)
+    assert info["num_pages"] == 10 and info["num_free"] == 10
+    assert info["k_base"] == FAKE_SLAB and info["v_base"] == FAKE_SLAB + 1024   # head 0: K rows, then V rows
+    assert info["page_stride_bytes"] == 17408
+    assert pkv.pkv_pool_kv_format(p) == pkv.PKV_KV_FP8
+    b = make_pool(2)
+    assert pkv.pkv_pool_kv_format(b) == pkv.PKV_KV_BF16
+    # same allocator: the seeded shuffle hands out the same ids as a BF16 pool
+    q = make_pool(10, seed=3)
+    assert np.array_equal(pkv.pkv_pool_alloc(p, 10), pkv.pkv_pool_alloc(q, 10))
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.pkv_pool_create_fp8(FAKE_SLAB + 8, 4 * pkv.PKV_PAGE_BYTES_FP8)
+    assert e.value.status == pkv.PKV_ERR_INVALID_ARG
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.pkv_pool_create_fp8(FAKE_SLAB, pkv.PKV_PAGE_BYTES_FP8 - 1)
+    assert e.value.status == pkv.PKV_ERR_INVALID_ARG
+    for x in (p, b, q):
+        pkv.pkv_pool_destroy(x)
+
+
+def test_fp8_pool_rejects_unsupported_options_before_any_cuda_call():
+    p = pkv.pkv_pool_create_fp8(FAKE_SLAB, 8 * pkv.PKV_PAGE_BYTES_FP8)
+    dummy = FAKE_SLAB
+    with pytest.raises(pkv.PkvError) as e:     # SIMT policy has no FP8 form
+        pkv.pkv_decode_attention_variant(p, dummy, dummy, 128, dummy, 4, 0.125, 16, dummy, 1 << 20, dummy, None,
+                                         0, variant=pkv.PKV_DECODE_SIMT)
+    assert e.value.status == pkv.PKV_ERR_UNSUPPORTED
+    ws = pkv.pkv_decode_step_workspace_bytes(4, 128, 16)
+    for opt in (pkv.PKV_STEP_PERSISTENT, pkv.PKV_STEP_WS, pkv.PKV_STEP_RING(2), pkv.PKV_STEP_EARLY_TRIGGER,
+                pkv.PKV_DECODE_SIMT):
+        with pytest.raises(pkv.PkvError) as e:
+            pkv.pkv_decode_step(p, dummy, dummy, dummy, dummy, 128, dummy, 4, dummy, 2048, 0.125, 16, dummy, ws,
+                                dummy, None, 0, options=opt)
+        assert e.value.status == pkv.PKV_ERR_UNSUPPORTED, hex(opt)
+    pkv.pkv_pool_destroy(p)
