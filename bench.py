@@ -158,7 +158,7 @@ class ClockSampler:
                 "samples": len(sm), "power_w_max": max(power) if power else None}
 
 
-KERNEL_SOURCES = ("pkv_device.cuh", "pkv_decode.cu", "pkv_step.cu")
+KERNEL_SOURCES = ("pkv_device.cuh", "pkv_decode.cu", "pkv_step.cu", "pkv_fp8.cu", "pkv_host.cpp")
 
 
 def kernel_source_digest() -> str:
@@ -170,7 +170,8 @@ def kernel_source_digest() -> str:
     return h.hexdigest()[:16]
 
 
-def measured_traffic(config: str, path: str, variant_name: str, pages_per_chunk: int, ring: int):
+def measured_traffic(config: str, path: str, variant_name: str, pages_per_chunk: int, ring: int,
+                     kv: str = "bf16"):
     """DRAM bytes per attention launch from the committed ncu summary
     (profiles/decode_traffic.json), if it was taken on the current kernel source;
     else None."""
@@ -183,7 +184,7 @@ def measured_traffic(config: str, path: str, variant_name: str, pages_per_chunk:
     for e in entries:
         if (e.get("config") == config and e.get("path") == path and e.get("variant") == variant_name and
                 e.get("pages_per_chunk") == pages_per_chunk and e.get("ring", 4) == ring and
-                e.get("kernel_source_sha") == digest):
+                e.get("kv", "bf16") == kv and e.get("kernel_source_sha") == digest):
             return e.get("dram_bytes_per_launch")
     return None
 
@@ -443,8 +444,8 @@ def run_pkv(args):
         avg = sum(split_ms) / len(split_ms)
         achieved = kv_launch / (avg / 1e3) / 1e9
         roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                    "traffic": (measured_traffic(args.config, args.path, variant_name, args.pages_per_chunk,
-                                                 args.ring) if args.kv == "bf16" else None),
+                    "traffic": measured_traffic(args.config, args.path, variant_name, args.pages_per_chunk,
+                                                args.ring, args.kv),
                     "kernel": ("FP8-page decode step: quantizing append + FP8 split kernel + merge launches"
                                if args.kv == "fp8" else
                                f"fused decode step kernel (append + attention + merge), variant {variant_name}"

@@ -283,12 +283,14 @@ const CUtensorMap *pool_tensor_map(const pkv_pool *cpool)
     CUresult r;
     cuuint32_t estride[5] = {1, 1, 1, 1, 1};
     if (pool->kv_format == PKV_KV_FP8) {
-        // dims innermost first: byte of a 64-byte row, row (32 code rows + 2 scale
-        // rows), KV head, page; one box is one head's 2176-byte unit
-        cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)(kFp8Unit / kD), (cuuint64_t)kHkv,
+        // dims innermost first: byte of a 128-byte line, line (17 per unit: 16 of
+        // codes, 1 of scales), KV head, page; one box is one head's 2176-byte unit,
+        // landing in shared memory exactly as it lies in the page
+        constexpr int kLine = 128;
+        cuuint64_t dims[4] = {(cuuint64_t)kLine, (cuuint64_t)(kFp8Unit / kLine), (cuuint64_t)kHkv,
                               (cuuint64_t)pool->num_pages};
-        cuuint64_t strides[3] = {(cuuint64_t)kD, (cuuint64_t)kFp8Unit, (cuuint64_t)pool->page_bytes};
-        cuuint32_t box[4] = {(cuuint32_t)kD, (cuuint32_t)(kFp8Unit / kD), 1, 1};
+        cuuint64_t strides[3] = {(cuuint64_t)kLine, (cuuint64_t)kFp8Unit, (cuuint64_t)pool->page_bytes};
+        cuuint32_t box[4] = {(cuuint32_t)kLine, (cuuint32_t)(kFp8Unit / kLine), 1, 1};
         r = encode(&pool->tmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, pool->slab, dims, strides, box, estride,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);

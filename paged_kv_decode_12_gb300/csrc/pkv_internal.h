@@ -19,8 +19,8 @@ struct pkv_pool {
     size_t page_bytes = PKV_PAGE_BYTES;
     // TMA descriptor of the slab.  BF16 pools: [num_pages][2][8][16][64] BF16,
     // 128-byte swizzle, box = one (page, KV head): its K rows then its V rows
-    // (4 KiB).  FP8 pools: the slab as [num_pages][8 heads][34 rows][64 B] (the
-    // 32 code rows and 2 scale rows of a head's unit), no swizzle, box = one
+    // (4 KiB).  FP8 pools: the slab as [num_pages][8 heads][17 lines][128 B] (a
+    // head's unit: 16 lines of codes, 1 of scales), no swizzle, box = one
     // (page, KV head) unit (2176 B).  Encoded on first use, because encoding
     // needs the CUDA driver.
     CUtensorMap tmap;  // 64-byte aligned by its own declaration
