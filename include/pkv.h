@@ -314,6 +314,13 @@ int pkv_prefill_append(const pkv_pool *pool, const uint16_t *k, const uint16_t *
  * copies, instead of after it has consumed them (helps layers that fit in one
  * wave of CTAs; can slow launches of several waves) */
 #define PKV_STEP_EARLY_TRIGGER 0x10000
+/* Grid schedule: dispatch the work units largest first (page count, then sequence,
+ * chunk, KV head) instead of in (KV head, sequence, chunk) order.  The block scheduler
+ * places CTAs in index order wherever there is room, so the largest units start first
+ * and small ones fill the gaps, which balances the SMs when a ragged batch fits in one
+ * wave.  Which CTA computes which unit is all that changes: results are identical.
+ * B <= 1024; not with PKV_STEP_PERSISTENT / PKV_STEP_WS (PKV_ERR_INVALID_ARG). */
+#define PKV_STEP_SORTED 0x20000
 
 /* Bytes of device workspace pkv_decode_step needs (a per-(sequence, KV head)
  * counter array and two work-distribution counters, followed by the chunk
@@ -347,7 +354,8 @@ size_t pkv_decode_step_workspace_bytes(int B, int max_blocks, int pages_per_chun
  * FP8 pools: the step runs as the quantizing append followed by the FP8 split
  * (and merge) kernels -- two or three launches in stream order, same results as
  * the separate calls; PKV_STEP_PERSISTENT / PKV_STEP_WS / PKV_STEP_RING /
- * PKV_STEP_EARLY_TRIGGER and the SIMT variant return PKV_ERR_UNSUPPORTED. */
+ * PKV_STEP_EARLY_TRIGGER / PKV_STEP_SORTED and the SIMT variant return
+ * PKV_ERR_UNSUPPORTED. */
 int pkv_decode_step(const pkv_pool *pool, const uint16_t *k_new, const uint16_t *v_new, uint16_t *q,
                     const int32_t *bt_dev, int max_blocks, const int32_t *seq_lens_dev, int B,
                     const float *rope_table, int max_pos, float scale, int pages_per_chunk, void *workspace,

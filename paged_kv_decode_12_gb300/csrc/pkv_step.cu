@@ -62,11 +62,14 @@ struct StepArgs {
     uint16_t *out;           // [B][32][64]
     int32_t *err;
     int early_trigger;       // grid schedule: allow the next launch as soon as the copies are issued
+    int sorted;              // grid schedule: units dispatched largest first (PKV_STEP_SORTED)
 };
 
 constexpr int kStepStages = 4;       // persistent schedule ring depth
 constexpr int kDefaultGridRing = 4;  // grid schedule ring depth unless the options choose one
 constexpr int kMaxPersistentBatch = 512;
+constexpr int kMaxSortedBatch = 1024;
+static_assert(kMaxPagesPerChunk + 1 + kWarps + 5 <= kWarps * kScratchFloats, "sorted-order scratch");
 
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void allow_dependent_launch() { asm volatile("griddepcontrol.launch_dependents;" ::); }
@@ -95,6 +98,167 @@ __device__ __forceinline__ float bf16_value(uint16_t h) { return __uint_as_float
 __device__ __forceinline__ bool length_ok(const StepArgs &a, int L)
 {
     return L >= 1 && L <= a.max_blocks * kPage && L <= a.max_pos;
+}
+
+// ------------------------------------------------------------------ sorted unit order
+
+// A sequence's work units per KV head: nfull chunks of pages_per_chunk pages and,
+// if rem > 0, a last chunk of rem pages; an invalid length has one empty unit.
+struct SeqUnits {
+    int nfull, rem;
+    bool valid;
+};
+
+__device__ __forceinline__ SeqUnits seq_units(const StepArgs &a, int L)
+{
+    SeqUnits u;
+    u.valid = length_ok(a, L);
+    if (!u.valid) {
+        u.nfull = 0;
+        u.rem = 0;
+        return u;
+    }
+    const int ppc = a.pages_per_chunk;
+    const int np = (L + kPage - 1) / kPage, nch = (np + ppc - 1) / ppc, rem = np - (nch - 1) * ppc;
+    u.nfull = rem == ppc ? nch : nch - 1;
+    u.rem = rem == ppc ? 0 : rem;
+    return u;
+}
+
+// Units of size s of one sequence (s = pages_per_chunk: full chunks; 0 < s < pages_per_chunk:
+// a last chunk; s = 0: the empty unit of an invalid length), all KV heads.
+__device__ __forceinline__ int units_of_size(const SeqUnits &u, int s, int ppc)
+{
+    if (!u.valid)
+        return s == 0 ? kHkv : 0;
+    if (s == ppc)
+        return kHkv * u.nfull;
+    return (s != 0 && u.rem == s) ? kHkv : 0;
+}
+
+// Exclusive prefix sum over the CTA's kThreads threads; `total` receives the sum.
+__device__ __forceinline__ int cta_exclusive_scan(int v, int *wsum, int &total)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(kFull, x, off);
+        if (lane >= off)
+            x += y;
+    }
+    if (lane == 31)
+        wsum[warp] = x;
+    __syncthreads();
+    int before = 0;
+    total = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        const int t = wsum[w];
+        before += w < warp ? t : 0;
+        total += t;
+    }
+    __syncthreads();
+    return before + x - v;
+}
+
+// Sorted dispatch (PKV_STEP_SORTED): the CTA with linear index lin takes the lin-th
+// unit in decreasing order of page count (ties by sequence, then chunk, then KV
+// head).  The block scheduler places CTAs in index order on whichever SM has room,
+// so the largest units are placed first and the small ones fill the gaps (greedy
+// largest-first list scheduling), instead of the grid order's mix.  The order only
+// decides which CTA computes which unit: every unit's arithmetic and the chunk-order
+// merge are unchanged, so results are identical to the unsorted grid.  All threads
+// call it (it uses barriers); `scratch` holds kMaxPagesPerChunk + 1 + kWarps + 5 ints.
+// Returns false (for the whole CTA) if lin is past the last unit.
+__device__ bool sorted_unit(const StepArgs &a, int B, int lin, int *scratch, int &b, int &g, int &c)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int ppc = a.pages_per_chunk;
+    int *hist = scratch;                            // [ppc + 1] units per size
+    int *wsum = scratch + kMaxPagesPerChunk + 1;    // [kWarps]
+    int *res = wsum + kWarps;                       // size, rank, b, g, c
+    for (int i = tid; i <= ppc; i += kThreads)
+        hist[i] = 0;
+    __syncthreads();
+    const int per = (B + kThreads - 1) / kThreads;  // contiguous sequences per thread
+    const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
+    for (int bb = b0; bb < b1; ++bb) {
+        const SeqUnits u = seq_units(a, a.seq_lens[bb]);
+        if (!u.valid) {
+            atomicAdd(&hist[0], kHkv);
+        } else {
+            if (u.nfull)
+                atomicAdd(&hist[ppc], kHkv * u.nfull);
+            if (u.rem)
+                atomicAdd(&hist[u.rem], kHkv);
+        }
+    }
+    __syncthreads();
+    if (warp == 0) {  // which size bucket holds rank lin, sizes in decreasing order
+        constexpr int kPer = (kMaxPagesPerChunk + 1 + 31) / 32;
+        int cnt[kPer];
+        int sum = 0;
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+            const int k = lane * kPer + i;  // k-th largest size, ppc - k
+            cnt[i] = k <= ppc ? hist[ppc - k] : 0;
+            sum += cnt[i];
+        }
+        int x = sum;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(kFull, x, off);
+            if (lane >= off)
+                x += y;
+        }
+        const int total = __shfl_sync(kFull, x, 31);
+        int start = x - sum;
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+            if (lin >= start && lin < start + cnt[i]) {
+                res[0] = ppc - (lane * kPer + i);
+                res[1] = lin - start;
+            }
+            start += cnt[i];
+        }
+        if (lane == 0 && lin >= total)
+            res[0] = -1;
+    }
+    __syncthreads();
+    const int s = res[0], r = res[1];
+    if (s < 0)
+        return false;
+    int mine = 0;
+    for (int bb = b0; bb < b1; ++bb)
+        mine += units_of_size(seq_units(a, a.seq_lens[bb]), s, ppc);
+    int total;
+    const int before = cta_exclusive_scan(mine, wsum, total);
+    if (r >= before && r < before + mine) {
+        int acc = before;
+        for (int bb = b0; bb < b1; ++bb) {
+            const SeqUnits u = seq_units(a, a.seq_lens[bb]);
+            const int n = units_of_size(u, s, ppc);
+            if (r < acc + n) {
+                const int i = r - acc;
+                res[2] = bb;
+                if (u.valid && s == ppc) {  // full chunks 0 .. nfull-1
+                    res[3] = i % kHkv;
+                    res[4] = i / kHkv;
+                } else {                    // the last chunk, or the empty unit of an invalid length
+                    res[3] = i;
+                    res[4] = u.valid ? u.nfull : 0;
+                }
+                break;
+            }
+            acc += n;
+        }
+    }
+    __syncthreads();
+    b = res[2];
+    g = res[3];
+    c = res[4];
+    return true;
 }
 
 __device__ __forceinline__ int chunks_of(const StepArgs &a, int L)
@@ -235,8 +399,13 @@ __global__ void __launch_bounds__(kThreads) decode_step_kernel(const __grid_cons
     int *ticket = reinterpret_cast<int *>(new_kv + 2 * kD);
 
     // chunk index slowest: every first chunk is dispatched before any later one, so the
-    // CTAs left empty by short sequences come last
-    const int g = blockIdx.x, b = blockIdx.y, c = blockIdx.z;
+    // CTAs left empty by short sequences come last; or the sorted order
+    int g = blockIdx.x, b = blockIdx.y, c = blockIdx.z;
+    if (a.sorted) {
+        const int lin = blockIdx.x + kHkv * (blockIdx.y + gridDim.y * blockIdx.z);
+        if (!sorted_unit(a, gridDim.y, lin, reinterpret_cast<int *>(sm.scratch), b, g, c))
+            return;
+    }
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int j0 = c * a.pages_per_chunk;
     // the length and this chunk's table entries are fetched together (one round trip):
@@ -964,7 +1133,8 @@ int fp8_step(const pkv_pool *pool, const uint16_t *k_new, const uint16_t *v_new,
 {
     const int variant = options & 0xff;
     if (variant == PKV_DECODE_SIMT ||
-        (options & (PKV_STEP_PERSISTENT | PKV_STEP_WS | PKV_STEP_RING_MASK | PKV_STEP_EARLY_TRIGGER)))
+        (options &
+         (PKV_STEP_PERSISTENT | PKV_STEP_WS | PKV_STEP_RING_MASK | PKV_STEP_EARLY_TRIGGER | PKV_STEP_SORTED)))
         return PKV_ERR_UNSUPPORTED;
     const int max_chunks = (max_blocks + ppc - 1) / ppc;
     const size_t counters_bytes = align256(((size_t)B * kHkv + 2) * sizeof(int));
@@ -1007,11 +1177,13 @@ extern "C" int pkv_decode_step(const pkv_pool *pool, const uint16_t *k_new, cons
     const int variant = options & 0xff;
     if (variant < PKV_DECODE_DEFAULT || variant > PKV_DECODE_MMA ||
         (options & ~(0xff | PKV_STEP_NO_PDL | PKV_STEP_GRID | PKV_STEP_PERSISTENT | PKV_STEP_WS |
-                     PKV_STEP_RING_MASK | PKV_STEP_EARLY_TRIGGER)) ||
+                     PKV_STEP_RING_MASK | PKV_STEP_EARLY_TRIGGER | PKV_STEP_SORTED)) ||
         (!!(options & PKV_STEP_GRID) + !!(options & PKV_STEP_PERSISTENT) + !!(options & PKV_STEP_WS) > 1))
         return PKV_ERR_INVALID_ARG;
     if ((options & (PKV_STEP_PERSISTENT | PKV_STEP_WS)) && B > kMaxPersistentBatch)
         return PKV_ERR_INVALID_ARG;
+    if ((options & PKV_STEP_SORTED) && ((options & (PKV_STEP_PERSISTENT | PKV_STEP_WS)) || B > kMaxSortedBatch))
+        return PKV_ERR_INVALID_ARG;  // the sorted order is a grid-schedule option, up to 1024 sequences
     const uintptr_t align = reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new) |
                             reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out) |
                             reinterpret_cast<uintptr_t>(rope_table) | reinterpret_cast<uintptr_t>(workspace);
@@ -1052,6 +1224,7 @@ extern "C" int pkv_decode_step(const pkv_pool *pool, const uint16_t *k_new, cons
     a.out = out;
     a.err = dev_err_flag;
     a.early_trigger = (options & PKV_STEP_EARLY_TRIGGER) ? 1 : 0;
+    a.sorted = (options & PKV_STEP_SORTED) ? 1 : 0;
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
     const bool pdl = !(options & PKV_STEP_NO_PDL);
     // the grid schedule is the measured default; the persistent one is chosen explicitly

@@ -30,7 +30,7 @@ class DecodeEngine:
                  pages_per_chunk: int = 16, variant: int = pkv.PKV_DECODE_DEFAULT, max_pos: int = wl.MAX_CONTEXT,
                  theta: float = wl.ROPE_THETA, pool_seed: int = 0, device: str = "cuda", fused: bool = True,
                  pdl: bool = True, schedule: str = "auto", ring: int = 0, early_trigger: bool = False,
-                 kv: str = "bf16"):
+                 kv: str = "bf16", sorted_units: bool = False):
         if kv not in ("bf16", "fp8"):
             raise ValueError(f"kv must be 'bf16' or 'fp8', not {kv!r}")
         self.kv = kv
@@ -56,8 +56,9 @@ class DecodeEngine:
         self.step_ws = torch.zeros(self.step_ws_bytes, dtype=torch.uint8, device=self.device)
         self.fused = fused
         self.step_options = (variant | (0 if pdl else pkv.PKV_STEP_NO_PDL) | SCHEDULES[schedule]
-                             | pkv.PKV_STEP_RING(ring) | (pkv.PKV_STEP_EARLY_TRIGGER if early_trigger else 0))
-        if kv == "fp8" and (schedule in ("persistent", "ws") or ring or early_trigger):
+                             | pkv.PKV_STEP_RING(ring) | (pkv.PKV_STEP_EARLY_TRIGGER if early_trigger else 0)
+                             | (pkv.PKV_STEP_SORTED if sorted_units else 0))
+        if kv == "fp8" and (schedule in ("persistent", "ws") or ring or early_trigger or sorted_units):
             raise ValueError("FP8 pools run the step as append + split kernels: no schedule, ring or trigger "
                              "options")
         self.bt = None

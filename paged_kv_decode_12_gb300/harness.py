@@ -38,7 +38,7 @@ class DeviceWorkload:
 def setup(name: str, seed: int = wl.DEFAULT_SEED, pages_per_chunk: int = 16,
           variant: int = pkv.PKV_DECODE_DEFAULT, layers: int | None = None, device: str = "cuda",
           fused: bool = True, pdl: bool = True, schedule: str = "auto", ring: int = 0,
-          early_trigger: bool = False, kv: str = "bf16") -> DeviceWorkload:
+          early_trigger: bool = False, kv: str = "bf16", sorted_units: bool = False) -> DeviceWorkload:
     """Build the named workload on the GPU: pool filled with N(0,1) BF16 (plus the
     key outliers of ``b64``) or, with ``kv="fp8"``, with FP8 pages drawn by
     ``workloads.fill_fp8_pages_``; block tables from the library's seeded
@@ -48,7 +48,7 @@ def setup(name: str, seed: int = wl.DEFAULT_SEED, pages_per_chunk: int = 16,
         w = dataclasses.replace(w, layers=layers, pool_pages=w.pool_pages * layers // w.layers)
     eng = DecodeEngine(w.pool_pages, w.layers, w.batch, w.max_blocks, pages_per_chunk, variant, pool_seed=seed,
                        device=device, fused=fused, pdl=pdl, schedule=schedule, ring=ring,
-                       early_trigger=early_trigger, kv=kv)
+                       early_trigger=early_trigger, kv=kv, sorted_units=sorted_units)
     if kv == "fp8":
         codes, scales = eng.fp8_views()
         wl.fill_fp8_pages_(codes, scales, seed, w.key_outlier_frac)

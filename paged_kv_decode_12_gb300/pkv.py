@@ -46,6 +46,7 @@ PKV_STEP_PERSISTENT = 0x400
 PKV_STEP_WS = 0x800
 PKV_STEP_RING_MASK = 0xF000
 PKV_STEP_EARLY_TRIGGER = 0x10000
+PKV_STEP_SORTED = 0x20000
 
 
 def PKV_STEP_RING(n: int) -> int:

@@ -217,3 +217,16 @@ def test_fp8_pool_rejects_unsupported_options_before_any_cuda_call():
                                 dummy, None, 0, options=opt)
         assert e.value.status == pkv.PKV_ERR_UNSUPPORTED, hex(opt)
     pkv.pkv_pool_destroy(p)
+
+
+def test_grid_schedule_options_validation_before_any_cuda_call():
+    p = make_pool(8)
+    dummy = FAKE_SLAB
+    ws = pkv.pkv_decode_step_workspace_bytes(1025, 128, 16)
+    for B, opt in ((1025, pkv.PKV_STEP_SORTED), (4, pkv.PKV_STEP_SORTED | pkv.PKV_STEP_PERSISTENT),
+                   (4, pkv.PKV_STEP_SORTED | pkv.PKV_STEP_WS)):
+        with pytest.raises(pkv.PkvError) as e:
+            pkv.pkv_decode_step(p, dummy, dummy, dummy, dummy, 128, dummy, B, dummy, 2048, 0.125, 16, dummy, ws,
+                                dummy, None, 0, options=opt)
+        assert e.value.status == pkv.PKV_ERR_INVALID_ARG, (B, hex(opt))
+    pkv.pkv_pool_destroy(p)

@@ -26,13 +26,15 @@ def native():
     pkv.lib()
 
 
-SCHEDULES = ["grid", "persistent", "ws"]
+# "sorted": the grid schedule with units dispatched largest first (PKV_STEP_SORTED)
+SCHEDULES = ["grid", "persistent", "ws", "sorted"]
 
 
 def fused_run(c, chunk=16, variant=pkv.PKV_DECODE_DEFAULT, pdl=True, seq_lens_override=None, repeats=1,
               schedule="auto", ring=0):
-    eng = DecodeEngine(c["num_pages"], 1, c["B"], c["max_blocks"], chunk, variant, pdl=pdl, schedule=schedule,
-                       ring=ring)
+    sorted_units = schedule == "sorted"
+    eng = DecodeEngine(c["num_pages"], 1, c["B"], c["max_blocks"], chunk, variant, pdl=pdl,
+                       schedule="grid" if sorted_units else schedule, ring=ring, sorted_units=sorted_units)
     eng.slab.copy_(torch.from_numpy(c["pool"].view(np.uint8)).cuda())
     eng.set_tables(c["bt"][None])
     lens = c["seq_lens"] if seq_lens_override is None else np.asarray(seq_lens_override, np.int32)
@@ -122,8 +124,29 @@ def test_persistent_many_units_per_cta():
     lens = rng.integers(1, 300, size=300)
     c = make_case(35, lens, max_blocks=64)
     g = fused_run(c, chunk=2, schedule="grid")
-    for schedule in ("persistent", "ws"):
+    for schedule in ("persistent", "ws", "sorted"):
         p = fused_run(c, chunk=2, schedule=schedule, repeats=2)
         assert p["status"] == pkv.PKV_OK and np.all(p["counters"] == 0)
         assert np.array_equal(p["out"], g["out"]) and np.array_equal(p["pool"], g["pool"])
         assert np.array_equal(p["q"], g["q"])
+
+
+@pytest.mark.parametrize("chunk", [1, 5, 32])
+def test_sorted_order_with_invalid_lengths_and_ring(chunk):
+    # every unit size class (full chunks, several last-chunk sizes, an invalid length
+    # at both ends) in one launch; the sorted order must still cover each unit once
+    rng = np.random.default_rng(37)
+    lens = np.concatenate([[2048, 1, 16, 17], rng.integers(1, 2048, size=60)]).astype(np.int32)
+    c = make_case(37, lens, max_blocks=128)
+    g = fused_run(c, chunk=chunk, schedule="grid")
+    for ring, sched in ((0, "sorted"), (2, "sorted"), (3, "sorted")):
+        s_ = fused_run(c, chunk=chunk, schedule=sched, ring=ring, repeats=2)
+        assert s_["status"] == pkv.PKV_OK and np.all(s_["counters"] == 0)
+        assert np.array_equal(s_["out"], g["out"]) and np.array_equal(s_["pool"], g["pool"])
+        assert np.array_equal(s_["q"], g["q"])
+    bad = fused_run(c, chunk=chunk, schedule="sorted", seq_lens_override=np.where(np.arange(lens.size) % 7 == 3, 0,
+                                                                                    lens))
+    assert bad["flag"] & pkv.PKV_DEVERR_LENGTH and np.all(bad["counters"] == 0)
+    zero = np.arange(lens.size) % 7 == 3
+    assert np.all(bad["out"][zero] == 0)
+    assert np.array_equal(bad["out"][~zero], g["out"][~zero])
