@@ -39,17 +39,27 @@ def _stale(outputs, inputs) -> bool:
     return min(os.path.getmtime(o) for o in outputs) < newest_in
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
+TIMELINE_LIB = os.path.join(HERE, "libpkv_timeline.so")
+
+
+def build(force: bool = False, verbose: bool = False, extra_flags=None, timeline: bool = False) -> str:
+    """Compile every source and link the library; returns its path.  With ``timeline``
+    the sources are compiled with -DPKV_TIMELINE into libpkv_timeline.so (the per-CTA
+    timeline of include/pkv_timeline.h), in a build folder of their own."""
     nvcc = _nvcc()
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    lib_path = TIMELINE_LIB if timeline else LIB
+    build_dir = os.path.join(BUILD_DIR, "timeline") if timeline else BUILD_DIR
+    os.makedirs(build_dir, exist_ok=True)
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh"))]
     headers.append(os.path.join(INCLUDE, "pkv.h"))
     srcs = [os.path.join(CSRC, s) for s in SOURCES]
-    objs = [os.path.join(BUILD_DIR, os.path.basename(s) + ".o") for s in srcs]
-    if not force and not _stale([LIB], srcs + headers + [__file__]):
-        return LIB
+    objs = [os.path.join(build_dir, os.path.basename(s) + ".o") for s in srcs]
+    if not force and not _stale([lib_path], srcs + headers + [__file__]):
+        return lib_path
     common = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "--expt-relaxed-constexpr"]
     common += list(extra_flags or [])
+    if timeline:
+        common += ["-DPKV_TIMELINE"]
     if verbose:
         common += ["-Xptxas", "-v"]
 
@@ -67,14 +77,14 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
 
     with concurrent.futures.ThreadPoolExecutor(max_workers=len(srcs)) as ex:
         list(ex.map(compile_one, zip(srcs, objs)))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     link = [nvcc] + ARCH + ["-shared", "-cudart", "shared", "-o", tmp] + objs + [
         "-Xlinker", "-rpath," + _cuda_lib_dir(nvcc)]
     if verbose:
         print(" ".join(link), file=sys.stderr)
     subprocess.run(link, check=True)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

@@ -173,6 +173,7 @@ __device__ __forceinline__ int cta_exclusive_scan(int v, int *wsum, int &total)
 // Returns false (for the whole CTA) if lin is past the last unit.
 __device__ bool sorted_unit(const StepArgs &a, int B, int lin, int *scratch, int &b, int &g, int &c)
 {
+    constexpr int kPer = kMaxSortedBatch / kThreads;  // sequences per thread, at most
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int ppc = a.pages_per_chunk;
     int *hist = scratch;                            // [ppc + 1] units per size
@@ -180,28 +181,35 @@ __device__ bool sorted_unit(const StepArgs &a, int B, int lin, int *scratch, int
     int *res = wsum + kWarps;                       // size, rank, b, g, c
     for (int i = tid; i <= ppc; i += kThreads)
         hist[i] = 0;
+    // this thread's contiguous run of sequences, read once (one memory round trip)
+    const int per = (B + kThreads - 1) / kThreads;
+    const int b0 = min(B, tid * per), nb = min(B, b0 + per) - b0;
+    SeqUnits u[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i)
+        u[i] = seq_units(a, i < nb ? a.seq_lens[b0 + i] : 0);
     __syncthreads();
-    const int per = (B + kThreads - 1) / kThreads;  // contiguous sequences per thread
-    const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
-    for (int bb = b0; bb < b1; ++bb) {
-        const SeqUnits u = seq_units(a, a.seq_lens[bb]);
-        if (!u.valid) {
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+        if (i >= nb)
+            break;
+        if (!u[i].valid) {
             atomicAdd(&hist[0], kHkv);
         } else {
-            if (u.nfull)
-                atomicAdd(&hist[ppc], kHkv * u.nfull);
-            if (u.rem)
-                atomicAdd(&hist[u.rem], kHkv);
+            if (u[i].nfull)
+                atomicAdd(&hist[ppc], kHkv * u[i].nfull);
+            if (u[i].rem)
+                atomicAdd(&hist[u[i].rem], kHkv);
         }
     }
     __syncthreads();
     if (warp == 0) {  // which size bucket holds rank lin, sizes in decreasing order
-        constexpr int kPer = (kMaxPagesPerChunk + 1 + 31) / 32;
-        int cnt[kPer];
+        constexpr int kBuckets = (kMaxPagesPerChunk + 1 + 31) / 32;
+        int cnt[kBuckets];
         int sum = 0;
 #pragma unroll
-        for (int i = 0; i < kPer; ++i) {
-            const int k = lane * kPer + i;  // k-th largest size, ppc - k
+        for (int i = 0; i < kBuckets; ++i) {
+            const int k = lane * kBuckets + i;  // k-th largest size, ppc - k
             cnt[i] = k <= ppc ? hist[ppc - k] : 0;
             sum += cnt[i];
         }
@@ -215,9 +223,9 @@ __device__ bool sorted_unit(const StepArgs &a, int B, int lin, int *scratch, int
         const int total = __shfl_sync(kFull, x, 31);
         int start = x - sum;
 #pragma unroll
-        for (int i = 0; i < kPer; ++i) {
+        for (int i = 0; i < kBuckets; ++i) {
             if (lin >= start && lin < start + cnt[i]) {
-                res[0] = ppc - (lane * kPer + i);
+                res[0] = ppc - (lane * kBuckets + i);
                 res[1] = lin - start;
             }
             start += cnt[i];
@@ -230,26 +238,26 @@ __device__ bool sorted_unit(const StepArgs &a, int B, int lin, int *scratch, int
     if (s < 0)
         return false;
     int mine = 0;
-    for (int bb = b0; bb < b1; ++bb)
-        mine += units_of_size(seq_units(a, a.seq_lens[bb]), s, ppc);
+#pragma unroll
+    for (int i = 0; i < kPer; ++i)
+        mine += i < nb ? units_of_size(u[i], s, ppc) : 0;
     int total;
     const int before = cta_exclusive_scan(mine, wsum, total);
     if (r >= before && r < before + mine) {
         int acc = before;
-        for (int bb = b0; bb < b1; ++bb) {
-            const SeqUnits u = seq_units(a, a.seq_lens[bb]);
-            const int n = units_of_size(u, s, ppc);
-            if (r < acc + n) {
-                const int i = r - acc;
-                res[2] = bb;
-                if (u.valid && s == ppc) {  // full chunks 0 .. nfull-1
-                    res[3] = i % kHkv;
-                    res[4] = i / kHkv;
-                } else {                    // the last chunk, or the empty unit of an invalid length
-                    res[3] = i;
-                    res[4] = u.valid ? u.nfull : 0;
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+            const int n = i < nb ? units_of_size(u[i], s, ppc) : 0;
+            if (n > 0 && r >= acc && r < acc + n) {
+                const int k = r - acc;
+                res[2] = b0 + i;
+                if (u[i].valid && s == ppc) {  // full chunks 0 .. nfull-1
+                    res[3] = k % kHkv;
+                    res[4] = k / kHkv;
+                } else {                       // the last chunk, or the empty unit of an invalid length
+                    res[3] = k;
+                    res[4] = u[i].valid ? u[i].nfull : 0;
                 }
-                break;
             }
             acc += n;
         }
@@ -385,6 +393,65 @@ __device__ __forceinline__ void finish_unit(const StepArgs &a, Warp &w, float *s
         a.counters[b * kHkv + g] = 0;
 }
 
+// ------------------------------------------------------------------ timeline (PKV_TIMELINE builds)
+
+#ifdef PKV_TIMELINE
+// Per-CTA timeline of the grid schedule, compiled only into libraries built with
+// -DPKV_TIMELINE: globaltimer stamps (ns) at entry, after the unit is known, after
+// the dependency wait, after the page loop and at the end, and (SM, sequence, chunk,
+// pages) per CTA linear index; CTAs without a unit store SM -1.  Every launch
+// overwrites the records of its linear indices.
+constexpr int kTimelineMax = 16384;
+__device__ unsigned long long g_timeline_stamps[kTimelineMax * 5];
+__device__ int g_timeline_meta[kTimelineMax * 4];
+
+__device__ __forceinline__ unsigned long long timeline_now()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+struct Timeline {
+    unsigned long long t[4];
+    int lin;
+    bool rec;
+    __device__ __forceinline__ void begin()
+    {
+        t[0] = timeline_now();
+        lin = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+        rec = threadIdx.x == 0 && lin < kTimelineMax;
+    }
+    __device__ __forceinline__ void stamp(int i) { t[i] = timeline_now(); }
+    __device__ __forceinline__ void none() const
+    {
+        if (rec)
+            g_timeline_meta[lin * 4] = -1;
+    }
+    __device__ __forceinline__ void end(int b, int c, int pages) const
+    {
+        if (!rec)
+            return;
+        unsigned sm;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(sm));
+        for (int i = 0; i < 4; ++i)
+            g_timeline_stamps[lin * 5 + i] = t[i];
+        g_timeline_stamps[lin * 5 + 4] = timeline_now();
+        g_timeline_meta[lin * 4 + 0] = (int)sm;
+        g_timeline_meta[lin * 4 + 1] = b;
+        g_timeline_meta[lin * 4 + 2] = c;
+        g_timeline_meta[lin * 4 + 3] = pages;
+    }
+};
+#else
+struct Timeline {  // compiled out
+    __device__ __forceinline__ void begin() {}
+    __device__ __forceinline__ void stamp(int) {}
+    __device__ __forceinline__ void none() const {}
+    __device__ __forceinline__ void end(int, int, int) const {}
+};
+#endif
+
 // ------------------------------------------------------------------ grid schedule
 
 constexpr int kGridExtraBytes = kGroup * kD * 2 + 2 * kD * 2 + 16;  // rotated q rows, new K/V rows, ticket
@@ -397,15 +464,20 @@ __global__ void __launch_bounds__(kThreads) decode_step_kernel(const __grid_cons
     uint16_t *q_rot = reinterpret_cast<uint16_t *>(sm.extra);  // [4][64] rotated query rows
     uint16_t *new_kv = q_rot + kGroup * kD;                     // [2][64] rotated key row, value row
     int *ticket = reinterpret_cast<int *>(new_kv + 2 * kD);
+    Timeline tl;
+    tl.begin();
 
     // chunk index slowest: every first chunk is dispatched before any later one, so the
     // CTAs left empty by short sequences come last; or the sorted order
     int g = blockIdx.x, b = blockIdx.y, c = blockIdx.z;
     if (a.sorted) {
         const int lin = blockIdx.x + kHkv * (blockIdx.y + gridDim.y * blockIdx.z);
-        if (!sorted_unit(a, gridDim.y, lin, reinterpret_cast<int *>(sm.scratch), b, g, c))
+        if (!sorted_unit(a, gridDim.y, lin, reinterpret_cast<int *>(sm.scratch), b, g, c)) {
+            tl.none();
             return;
+        }
     }
+    tl.stamp(1);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int j0 = c * a.pages_per_chunk;
     // the length and this chunk's table entries are fetched together (one round trip):
@@ -421,12 +493,15 @@ __global__ void __launch_bounds__(kThreads) decode_step_kernel(const __grid_cons
             grid_dependency_wait();
             write_zero_unit(a, b, g);
         }
+        tl.none();
         return;
     }
     const int npages = (L + kPage - 1) / kPage;
     const int nchunks = chunks_of(a, L);
-    if (c >= nchunks)
+    if (c >= nchunks) {
+        tl.none();
         return;
+    }
     const bool last_chunk = c == nchunks - 1;
     const int jn = min(npages - j0, a.pages_per_chunk);
     const int nmine = warp < jn ? (jn - warp + kWarps - 1) / kWarps : 0;
@@ -444,6 +519,7 @@ __global__ void __launch_bounds__(kThreads) decode_step_kernel(const __grid_cons
         allow_dependent_launch();
 
     grid_dependency_wait();  // q, k_new, v_new and every output belong to the dependency chain
+    tl.stamp(2);
 
     const int pos = L - 1, slot = pos % kPage;
     unit_rows(a, b, g, pos, last_chunk, q_rot, new_kv);
@@ -465,10 +541,12 @@ __global__ void __launch_bounds__(kThreads) decode_step_kernel(const __grid_cons
             lane == 0 && a.err)
             atomicOr(a.err, PKV_DEVERR_TIMEOUT);
     }
+    tl.stamp(3);
     if (!a.early_trigger)
         allow_dependent_launch();
     // the stages are free now: they hold the combine area
     finish_unit(a, w, reinterpret_cast<float *>(sm.stages), ticket, q_rot, b, g, c, nchunks);
+    tl.end(b, c, jn);
 }
 
 
@@ -1242,3 +1320,18 @@ extern "C" int pkv_decode_step(const pkv_pool *pool, const uint16_t *k_new, cons
     return variant == PKV_DECODE_SIMT ? launch_grid_depth<SimtWarp>(tmap, a, B, s, pdl, depth)
                                       : launch_grid_depth<MmaWarp>(tmap, a, B, s, pdl, depth);
 }
+
+#ifdef PKV_TIMELINE
+extern "C" int pkv_timeline_read(uint64_t *stamps, int32_t *meta, int n)
+{
+    using namespace pkv;
+    if (!stamps || !meta || n < 1)
+        return PKV_ERR_INVALID_ARG;
+    if (n > kTimelineMax)
+        n = kTimelineMax;
+    if (cudaMemcpyFromSymbol(stamps, g_timeline_stamps, (size_t)n * 5 * sizeof(uint64_t)) != cudaSuccess ||
+        cudaMemcpyFromSymbol(meta, g_timeline_meta, (size_t)n * 4 * sizeof(int32_t)) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    return n;
+}
+#endif

@@ -15,7 +15,8 @@ import os
 import numpy as np
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "libpkv.so")
+# PKV_LIBRARY selects another build of the same ABI (e.g. libpkv_timeline.so)
+LIB_PATH = os.environ.get("PKV_LIBRARY") or os.path.join(HERE, "libpkv.so")
 
 PKV_PAGE_SIZE = 16
 PKV_NUM_Q_HEADS = 32
