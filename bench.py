@@ -62,6 +62,7 @@ DEFAULT_RING = {"b256": 4, "b64": 2, "b8": 2, "trace": 2}   # TMA stages per war
 # Largest-first unit dispatch (PKV_STEP_SORTED): measured +5 % on the ragged one-wave
 # layers (b64, b8), -3 % on b256 where every unit has the same size.
 DEFAULT_SORTED = {"b256": False, "b64": True, "b8": True, "trace": False}
+DEFAULT_RING_FP8 = {"b256": 2, "b64": 2, "b8": 2, "trace": 2}  # units of 2176 B per warp (FP8 pages), measured
 L2_BYTES = 129 * 10**6
 
 
@@ -452,7 +453,7 @@ def run_pkv(args):
         roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                     "traffic": measured_traffic(args.config, args.path, variant_name, args.pages_per_chunk,
                                                 args.ring, args.kv),
-                    "kernel": ("FP8-page decode step: quantizing append + FP8 split kernel + merge launches"
+                    "kernel": ("fused decode step kernel over FP8 pages (append + quantize + attention + merge)"
                                if args.kv == "fp8" else
                                f"fused decode step kernel (append + attention + merge), variant {variant_name}"
                                if args.path == "fused" else
@@ -560,10 +561,9 @@ def main(argv=None):
     if args.pages_per_chunk is None:
         args.pages_per_chunk = DEFAULT_CHUNK[args.config]
     if args.ring is None:
-        args.ring = DEFAULT_RING[args.config] if args.kv == "bf16" else 0
+        args.ring = DEFAULT_RING[args.config] if args.kv == "bf16" else DEFAULT_RING_FP8[args.config]
     if args.sorted is None:
-        args.sorted = (DEFAULT_SORTED[args.config] and args.kv == "bf16" and not args.unsorted
-                       and args.schedule in ("auto", "grid"))
+        args.sorted = DEFAULT_SORTED[args.config] and not args.unsorted and args.schedule in ("auto", "grid")
     elif args.unsorted:
         raise SystemExit("--sorted and --unsorted exclude each other")
     if args.impl == "reference":

@@ -351,10 +351,11 @@ size_t pkv_decode_step_workspace_bytes(int B, int max_blocks, int pages_per_chun
  * preceding kernel on the stream write those three (block tables of different
  * layers must not share pages -- pkv_block_tables_build never does).
  * Device checks as pkv_decode_attention, plus seq_len > max_pos.
- * FP8 pools: the step runs as the quantizing append followed by the FP8 split
- * (and merge) kernels -- two or three launches in stream order, same results as
- * the separate calls; PKV_STEP_PERSISTENT / PKV_STEP_WS / PKV_STEP_RING /
- * PKV_STEP_EARLY_TRIGGER / PKV_STEP_SORTED and the SIMT variant return
+ * FP8 pools: the same single launch on the grid schedule (options PKV_STEP_RING,
+ * PKV_STEP_EARLY_TRIGGER, PKV_STEP_SORTED and PKV_STEP_NO_PDL apply; a ring stage is
+ * one 2176-byte unit): the new token's rotated key row and value row are quantized
+ * as pkv_append_rope quantizes them, and results are bit-identical to the separate
+ * calls.  PKV_STEP_PERSISTENT / PKV_STEP_WS and the SIMT variant return
  * PKV_ERR_UNSUPPORTED. */
 int pkv_decode_step(const pkv_pool *pool, const uint16_t *k_new, const uint16_t *v_new, uint16_t *q,
                     const int32_t *bt_dev, int max_blocks, const int32_t *seq_lens_dev, int B,

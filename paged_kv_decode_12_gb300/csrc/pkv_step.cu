@@ -36,6 +36,7 @@
 #include <cuda_bf16.h>
 
 #include "pkv_device.cuh"
+#include "pkv_fp8.cuh"
 
 namespace pkv {
 namespace {
@@ -549,6 +550,184 @@ __global__ void __launch_bounds__(kThreads) decode_step_kernel(const __grid_cons
     tl.end(b, c, jn);
 }
 
+
+
+// ------------------------------------------------------------------ FP8 pages, grid schedule
+
+// The fused step over FP8 pages: the same unit, prologue, dependency wait, query
+// rotation, ticket and merge as decode_step_kernel, with the FP8 unit copy and the
+// Fp8MmaWarp page policy.  The new token's rotated key row and value row are
+// quantized once per (sequence, KV head) by the unit of the last chunk -- warp 0 the
+// key, warp 1 the value, with the FP8 append's arithmetic -- stored into their page
+// slot, and patched into the staged copy of that page.
+template <int STAGES>
+struct Fp8StepSmem {
+    static constexpr int kStagesBytes = kWarps * STAGES * kFp8Unit;
+    static constexpr int kBarsBytes = kWarps * STAGES * 8;
+    static constexpr int kSortInts = kMaxPagesPerChunk + 1 + kWarps + 5;
+    static constexpr int kExtraBytes = kGroup * kD * 2 + 2 * kD * 2 + 2 * kD + 16 + 16 + kSortInts * 4;
+    static constexpr int kBytes = 128 + kStagesBytes + kBarsBytes + kExtraBytes;  // incl. alignment slack
+    static_assert(kStagesBytes >= kWarps * kStateFloats * 4, "the combine reuses the stages");
+    uint8_t *stages;
+    uint64_t *bars;
+    uint16_t *q_rot;      // [4][64] rotated query rows (BF16)
+    uint16_t *new_kv;     // [2][64] rotated key row, value row (BF16)
+    uint8_t *new_codes;   // [2][64] their E4M3 codes
+    float *new_scales;    // [2] their row scales
+    int *ticket;
+    int *sort_scratch;
+
+    __device__ __forceinline__ explicit Fp8StepSmem(uint8_t *raw)
+    {
+        uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(raw) + 127) & ~uintptr_t(127));
+        stages = base;
+        bars = reinterpret_cast<uint64_t *>(base + kStagesBytes);
+        uint8_t *e = base + kStagesBytes + kBarsBytes;
+        q_rot = reinterpret_cast<uint16_t *>(e);
+        new_kv = q_rot + kGroup * kD;
+        new_codes = reinterpret_cast<uint8_t *>(new_kv + 2 * kD);
+        new_scales = reinterpret_cast<float *>(new_codes + 2 * kD);
+        ticket = reinterpret_cast<int *>(new_scales + 4);
+        sort_scratch = ticket + 4;
+    }
+};
+
+// Lanes 0..9 of a warp write the new token's rows into a unit (a stage or the page):
+// lanes 0-3 the K codes, 4-7 the V codes (16 bytes each), 8 and 9 the two scales.
+__device__ __forceinline__ void put_new_token_fp8(uint8_t *unit, int slot, const uint8_t *codes, const float *scales,
+                                                  int lane)
+{
+    if (lane < 8) {
+        const int part = lane >> 2, ch = lane & 3;  // part 0: K row, 1: V row
+        *reinterpret_cast<uint4 *>(unit + (part * kPage + slot) * kD + 16 * ch) =
+            reinterpret_cast<const uint4 *>(codes + part * kD)[ch];
+    } else if (lane < 10) {
+        const int part = lane - 8;
+        reinterpret_cast<float *>(unit + kFp8UnitCodes)[part * kPage + slot] = scales[part];
+    }
+}
+
+template <int STAGES>
+__global__ void __launch_bounds__(kThreads, 6) decode_step_fp8_kernel(const __grid_constant__ CUtensorMap tmap,
+                                                                   StepArgs a)
+{
+    extern __shared__ uint8_t smem_raw[];
+    Fp8StepSmem<STAGES> sm(smem_raw);
+
+    int g = blockIdx.x, b = blockIdx.y, c = blockIdx.z;
+    if (a.sorted) {
+        const int lin = blockIdx.x + kHkv * (blockIdx.y + gridDim.y * blockIdx.z);
+        if (!sorted_unit(a, gridDim.y, lin, sm.sort_scratch, b, g, c))
+            return;
+    }
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int j0 = c * a.pages_per_chunk;
+    const int jcap = min(a.max_blocks - j0, a.pages_per_chunk);
+    const int ncap = warp < jcap ? (jcap - warp + kWarps - 1) / kWarps : 0;
+    int my_page = 0;
+    if (lane < ncap)
+        my_page = a.bt[(size_t)b * a.max_blocks + j0 + warp + lane * kWarps];
+    const int L = a.seq_lens[b];
+    if (!length_ok(a, L)) {
+        if (c == 0) {
+            grid_dependency_wait();
+            write_zero_unit(a, b, g);
+        }
+        return;
+    }
+    const int npages = (L + kPage - 1) / kPage;
+    const int nchunks = chunks_of(a, L);
+    if (c >= nchunks)
+        return;
+    const bool last_chunk = c == nchunks - 1;
+    const int jn = min(npages - j0, a.pages_per_chunk);
+    const int nmine = warp < jn ? (jn - warp + kWarps - 1) / kWarps : 0;
+    const bool bad = lane < nmine && (my_page < 0 || my_page >= a.num_pages);
+    const bool any_bad = __syncthreads_or(bad);
+
+    uint64_t *my_bars = sm.bars + warp * STAGES;
+    uint8_t *my_stages = sm.stages + warp * STAGES * kFp8Unit;
+    const uint64_t policy = l2_evict_first_policy();
+    if (!any_bad) {
+        init_warp_barriers<STAGES>(my_bars, lane);
+        for (int k = 0; k < min(STAGES, nmine); ++k) {
+            const int pk = __shfl_sync(kFull, my_page, k);
+            if (lane == 0)
+                fp8::fp8_issue(&tmap, my_stages + k * kFp8Unit, &my_bars[k], g, pk, policy);
+        }
+    }
+    if (a.early_trigger)
+        allow_dependent_launch();
+
+    grid_dependency_wait();  // q, k_new, v_new and every output belong to the dependency chain
+
+    const int pos = L - 1, slot = pos % kPage;
+    unit_rows(a, b, g, pos, last_chunk, sm.q_rot, sm.new_kv);
+    __syncthreads();
+    if (last_chunk) {
+        if (warp == 0) {  // key row: lane holds dims lane, lane + 32 (rotated, BF16)
+            uint32_t c1, c2;
+            float sc;
+            fp8::quantize_pair(bf16_value(sm.new_kv[lane]), bf16_value(sm.new_kv[lane + kD / 2]), c1, c2, sc);
+            sm.new_codes[lane] = (uint8_t)c1;
+            sm.new_codes[lane + kD / 2] = (uint8_t)c2;
+            if (lane == 0)
+                sm.new_scales[0] = sc;
+        } else if (warp == 1) {  // value row: lane holds dims 2 lane, 2 lane + 1
+            const uint32_t w2 = reinterpret_cast<const uint32_t *>(sm.new_kv + kD)[lane];
+            uint32_t c0, c1;
+            float sc;
+            fp8::quantize_pair(bf16lo(w2), bf16hi(w2), c0, c1, sc);
+            reinterpret_cast<uint16_t *>(sm.new_codes + kD)[lane] = (uint16_t)(c0 | (c1 << 8));
+            if (lane == 0)
+                sm.new_scales[1] = sc;
+        }
+        __syncthreads();
+        if (!any_bad && warp == 0) {
+            const int page = a.bt[(size_t)b * a.max_blocks + npages - 1];
+            uint8_t *unit = reinterpret_cast<uint8_t *>(a.slab) + (size_t)page * kFp8PageBytes + (size_t)g * kFp8Unit;
+            put_new_token_fp8(unit, slot, sm.new_codes, sm.new_scales, lane);
+        }
+    }
+    if (any_bad && tid == 0 && a.err)
+        atomicOr(a.err, PKV_DEVERR_PAGE_RANGE);
+
+    fp8::Fp8MmaWarp w;
+    w.init(sm.q_rot, a.scale_log2, lane);
+    if (!any_bad) {
+        int k = 0;
+        for (; k < nmine; ++k) {
+            const int s = k % STAGES;
+            if (!mbar_wait_warp(&my_bars[s], (uint32_t)((k / STAGES) & 1)))
+                break;
+            const int j = j0 + warp + k * kWarps;
+            uint8_t *stage = my_stages + s * kFp8Unit;
+            if (last_chunk && j == npages - 1) {  // the copy may predate the new token's store
+                put_new_token_fp8(stage, slot, sm.new_codes, sm.new_scales, lane);
+                __syncwarp();
+            }
+            w.page(stage, min(kPage, L - j * kPage));
+            __syncwarp();
+            if (k + STAGES < nmine) {
+                const int pk = __shfl_sync(kFull, my_page, k + STAGES);
+                if (lane == 0) {
+                    fence_proxy_async_smem();
+                    fp8::fp8_issue(&tmap, stage, &my_bars[s], g, pk, policy);
+                }
+            }
+        }
+        if (k < nmine) {  // a wait gave up: let the copies in flight land (bounded), flag it
+            for (int kk = k; kk < min(nmine, k + STAGES); ++kk)
+                (void)mbar_wait_warp(&my_bars[kk % STAGES], (uint32_t)((kk / STAGES) & 1));
+            if (lane == 0 && a.err)
+                atomicOr(a.err, PKV_DEVERR_TIMEOUT);
+        }
+    }
+    if (!a.early_trigger)
+        allow_dependent_launch();
+    // the stages are free now: they hold the combine area
+    finish_unit(a, w, reinterpret_cast<float *>(sm.stages), sm.ticket, sm.q_rot, b, g, c, nchunks);
+}
 
 // ------------------------------------------------------------------ persistent schedule
 
@@ -1120,6 +1299,38 @@ int launch_grid(const CUtensorMap *tmap, const StepArgs &a, int B, cudaStream_t 
     return status_from_cuda(cudaLaunchKernelEx(&cfg, kernel, *tmap, a));
 }
 
+// FP8 pages: ring depth per warp 2..4 units (2176 B each).
+template <int STAGES>
+int launch_fp8_grid(const CUtensorMap *tmap, const StepArgs &a, int B, cudaStream_t s, bool pdl)
+{
+    auto kernel = decode_step_fp8_kernel<STAGES>;
+    constexpr int smem = Fp8StepSmem<STAGES>::kBytes;
+    static bool attr_set = false;  // set once per process (before any graph capture)
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+            return PKV_ERR_CUDA;
+        attr_set = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kHkv, B, a.max_chunks);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1] = {pdl_attribute()};
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return status_from_cuda(cudaLaunchKernelEx(&cfg, kernel, *tmap, a));
+}
+
+int launch_fp8_depth(const CUtensorMap *tmap, const StepArgs &a, int B, cudaStream_t s, bool pdl, int depth)
+{
+    switch (depth) {
+    case 2: return launch_fp8_grid<2>(tmap, a, B, s, pdl);
+    case 3: return launch_fp8_grid<3>(tmap, a, B, s, pdl);
+    default: return launch_fp8_grid<4>(tmap, a, B, s, pdl);
+    }
+}
+
 // Ring depth per warp: 2 stages (36 KB per CTA, 6 CTAs per SM), 3 (4 per SM) or 4 (3 per SM).
 template <class Warp>
 int launch_grid_depth(const CUtensorMap *tmap, const StepArgs &a, int B, cudaStream_t s, bool pdl, int depth)
@@ -1202,32 +1413,6 @@ int launch_ws(const CUtensorMap *tmap, const StepArgs &a, int B, cudaStream_t s,
     return status_from_cuda(cudaLaunchKernelEx(&cfg, kernel, *tmap, a, B, work_counter, work_counter + 1));
 }
 
-// FP8 pools: the quantizing append (pos = seq_len - 1) then the FP8 split kernel
-// and, for sequences of several chunks, the merge; the workspace's counter region
-// is left untouched.
-int fp8_step(const pkv_pool *pool, const uint16_t *k_new, const uint16_t *v_new, uint16_t *q, const int32_t *bt,
-             int max_blocks, const int32_t *seq_lens, int B, const float *rope, int max_pos, float scale, int ppc,
-             char *ws, uint16_t *out, int32_t *err, cudaStream_t s, int options)
-{
-    const int variant = options & 0xff;
-    if (variant == PKV_DECODE_SIMT ||
-        (options &
-         (PKV_STEP_PERSISTENT | PKV_STEP_WS | PKV_STEP_RING_MASK | PKV_STEP_EARLY_TRIGGER | PKV_STEP_SORTED)))
-        return PKV_ERR_UNSUPPORTED;
-    const int max_chunks = (max_blocks + ppc - 1) / ppc;
-    const size_t counters_bytes = align256(((size_t)B * kHkv + 2) * sizeof(int));
-    const size_t ml_bytes = align256((size_t)B * kHq * max_chunks * sizeof(float2));
-    float2 *part_ml = reinterpret_cast<float2 *>(ws + counters_bytes);
-    float *part_o = reinterpret_cast<float *>(ws + counters_bytes + ml_bytes);
-    int st = fp8_append_rope(pool, k_new, v_new, q, bt, max_blocks, seq_lens, -1, B, rope, max_pos, err, s);
-    if (st == PKV_OK)
-        st = fp8_decode_split(pool, q, bt, max_blocks, seq_lens, B, scale * 1.4426950408889634f, ppc, part_ml,
-                              part_o, max_chunks, out, err, s);
-    if (st != PKV_OK || max_chunks == 1)
-        return st;
-    return launch_decode_merge(seq_lens, max_blocks, ppc, part_ml, part_o, max_chunks, out, B, s);
-}
-
 }  // namespace
 }  // namespace pkv
 
@@ -1269,10 +1454,9 @@ extern "C" int pkv_decode_step(const pkv_pool *pool, const uint16_t *k_new, cons
         return PKV_ERR_INVALID_ARG;
     if (workspace_bytes < pkv_decode_step_workspace_bytes(B, max_blocks, pages_per_chunk))
         return PKV_ERR_WORKSPACE_TOO_SMALL;
-    if (pool->kv_format == PKV_KV_FP8)
-        return fp8_step(pool, k_new, v_new, q, bt_dev, max_blocks, seq_lens_dev, B, rope_table, max_pos, scale,
-                        pages_per_chunk, static_cast<char *>(workspace), out, dev_err_flag,
-                        static_cast<cudaStream_t>(cuda_stream), options);
+    if (pool->kv_format == PKV_KV_FP8 &&
+        (variant == PKV_DECODE_SIMT || (options & (PKV_STEP_PERSISTENT | PKV_STEP_WS))))
+        return PKV_ERR_UNSUPPORTED;  // FP8 pages: the grid schedule and the MMA policy only
     const CUtensorMap *tmap = pool_tensor_map(pool);
     if (!tmap)
         return PKV_ERR_CUDA;
@@ -1317,6 +1501,8 @@ extern "C" int pkv_decode_step(const pkv_pool *pool, const uint16_t *k_new, cons
     if (ring != 0 && (ring < 2 || ring > 4))
         return PKV_ERR_INVALID_ARG;
     const int depth = ring ? ring : kDefaultGridRing;
+    if (pool->kv_format == PKV_KV_FP8)
+        return launch_fp8_depth(tmap, a, B, s, pdl, depth);
     return variant == PKV_DECODE_SIMT ? launch_grid_depth<SimtWarp>(tmap, a, B, s, pdl, depth)
                                       : launch_grid_depth<MmaWarp>(tmap, a, B, s, pdl, depth);
 }

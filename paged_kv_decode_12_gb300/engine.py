@@ -58,8 +58,8 @@ class DecodeEngine:
         self.step_options = (variant | (0 if pdl else pkv.PKV_STEP_NO_PDL) | SCHEDULES[schedule]
                              | pkv.PKV_STEP_RING(ring) | (pkv.PKV_STEP_EARLY_TRIGGER if early_trigger else 0)
                              | (pkv.PKV_STEP_SORTED if sorted_units else 0))
-        if kv == "fp8" and (schedule in ("persistent", "ws") or ring or early_trigger or sorted_units):
-            raise ValueError("FP8 pools run the step as append + split kernels: no schedule, ring or trigger "
+        if kv == "fp8" and schedule in ("persistent", "ws"):
+            raise ValueError("FP8 pools run the fused step on the grid schedule only: no persistent or ws "
                              "options")
         self.bt = None
         self.bt_host = None

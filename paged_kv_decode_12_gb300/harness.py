@@ -75,10 +75,10 @@ def setup(name: str, seed: int = wl.DEFAULT_SEED, pages_per_chunk: int = 16,
 
 
 def kernels_per_step(dw: DeviceWorkload) -> int:
-    """Library kernel launches in one step: per layer one fused kernel, or (separate
-    path, and every FP8-page step) the append, the split kernel and, when a sequence
-    can span several chunks, the merge."""
-    if dw.eng.fused and dw.eng.kv == "bf16":
+    """Library kernel launches in one step: per layer one fused kernel (BF16 or FP8
+    pages), or (separate path) the append, the split kernel and, when a sequence can
+    span several chunks, the merge."""
+    if dw.eng.fused:
         return dw.w.layers
     merge = 1 if (dw.w.max_blocks + dw.eng.pages_per_chunk - 1) // dw.eng.pages_per_chunk > 1 else 0
     return dw.w.layers * (2 + merge)

@@ -210,8 +210,7 @@ def test_fp8_pool_rejects_unsupported_options_before_any_cuda_call():
                                          0, variant=pkv.PKV_DECODE_SIMT)
     assert e.value.status == pkv.PKV_ERR_UNSUPPORTED
     ws = pkv.pkv_decode_step_workspace_bytes(4, 128, 16)
-    for opt in (pkv.PKV_STEP_PERSISTENT, pkv.PKV_STEP_WS, pkv.PKV_STEP_RING(2), pkv.PKV_STEP_EARLY_TRIGGER,
-                pkv.PKV_DECODE_SIMT):
+    for opt in (pkv.PKV_STEP_PERSISTENT, pkv.PKV_STEP_WS, pkv.PKV_DECODE_SIMT):
         with pytest.raises(pkv.PkvError) as e:
             pkv.pkv_decode_step(p, dummy, dummy, dummy, dummy, 128, dummy, 4, dummy, 2048, 0.125, 16, dummy, ws,
                                 dummy, None, 0, options=opt)

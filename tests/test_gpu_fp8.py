@@ -231,22 +231,59 @@ def test_fp8_single_token_returns_dequantized_v():
     assert ulp_distance(gpu["out"], ref["out"]).max() <= 1
 
 
-def test_fp8_step_equals_separate_calls():
-    c = make_case(51, [5, 16, 17, 77, 130, 1])
-    outs, pools = [], []
-    for fused in (False, True):
-        eng = engine_for(c, chunk=4, fused=fused)
+def fp8_step_run(c, chunk, fused, ring=0, sorted_units=False, pdl=True, repeats=1, lens_override=None):
+    eng = DecodeEngine(c["num_pages"], 1, c["B"], c["max_blocks"], chunk, kv="fp8", fused=fused, ring=ring,
+                       sorted_units=sorted_units, pdl=pdl)
+    eng.slab.copy_(torch.from_numpy(c["pool"]).cuda())
+    eng.set_tables(c["bt"][None])
+    lens = c["seq_lens"] if lens_override is None else np.asarray(lens_override, np.int32)
+    lens_d = torch.from_numpy(lens).cuda()
+    for _ in range(repeats):
         q = dev_bf16(c["q"])[None].contiguous()
         out = torch.zeros((1, c["B"], HQ, D), dtype=torch.bfloat16, device="cuda")
-        lens_d = torch.from_numpy(c["seq_lens"]).cuda()
         eng.step(q, dev_bf16(c["k_new"])[None], dev_bf16(c["v_new"])[None], lens_d - 1, lens_d, out)
-        st, flag = eng.check_errors()
-        assert st == pkv.PKV_OK and flag == 0
-        outs.append(u16(out))
-        pools.append(eng.slab.cpu().numpy())
-        eng.close()
-    assert np.array_equal(outs[0], outs[1]) and np.array_equal(pools[0], pools[1])
-    assert_close(outs[1][0], oracle_run(c)["out_f64"])
+    st, flag = eng.check_errors()
+    counters = eng.step_ws[: (c["B"] * 8 + 2) * 4].view(torch.int32).cpu().numpy()
+    res = dict(out=u16(out)[0], q=u16(q)[0], pool=eng.slab.cpu().numpy(), status=st, flag=flag, counters=counters)
+    eng.close()
+    return res
+
+
+@pytest.mark.parametrize("chunk", [1, 4, 128])
+@pytest.mark.parametrize("ring,sorted_units", [(0, False), (2, False), (3, True)])
+def test_fp8_fused_step_equals_separate_calls(chunk, ring, sorted_units):
+    # one launch per layer (append + quantize + attention + merge) against the
+    # quantizing append and the FP8 split kernel: same pool bytes, queries, outputs
+    c = make_case(51, [5, 16, 17, 77, 130, 1, 200, 33])
+    sep = fp8_step_run(c, chunk, fused=False)
+    fus = fp8_step_run(c, chunk, fused=True, ring=ring, sorted_units=sorted_units, repeats=1)
+    assert sep["status"] == pkv.PKV_OK and fus["status"] == pkv.PKV_OK and fus["flag"] == 0
+    assert np.all(fus["counters"] == 0)
+    assert np.array_equal(sep["out"], fus["out"]) and np.array_equal(sep["pool"], fus["pool"])
+    assert np.array_equal(sep["q"], fus["q"])
+    assert_close(fus["out"], oracle_run(c)["out_f64"])
+
+
+def test_fp8_fused_step_repeats_and_without_pdl():
+    c = make_case(52, [40, 3, 129])
+    a = fp8_step_run(c, 2, fused=True)
+    b = fp8_step_run(c, 2, fused=True, pdl=False)
+    assert np.array_equal(a["out"], b["out"]) and np.array_equal(a["pool"], b["pool"])
+    r = fp8_step_run(c, 2, fused=True, repeats=3)   # the counters stay usable across calls
+    assert r["status"] == pkv.PKV_OK and np.all(r["counters"] == 0)
+
+
+def test_fp8_fused_step_device_checks():
+    c = make_case(53, [40, 20, 70])
+    z = fp8_step_run(c, 4, fused=True, lens_override=[40, 0, 70])
+    assert z["flag"] & pkv.PKV_DEVERR_LENGTH and np.all(z["out"][1] == 0) and np.all(z["counters"] == 0)
+    ref = fp8_step_run(c, 4, fused=False)
+    assert np.array_equal(z["out"][[0, 2]], ref["out"][[0, 2]])
+    bad = dict(c, bt=c["bt"].copy())
+    bad["bt"][2, 1] = c["num_pages"] + 3
+    f = fp8_step_run(bad, 4, fused=True)
+    assert f["flag"] & pkv.PKV_DEVERR_PAGE_RANGE and np.all(f["counters"] == 0)
+    assert np.array_equal(f["out"][:2], ref["out"][:2])
 
 
 def test_fp8_bad_page_id_sets_flag():
