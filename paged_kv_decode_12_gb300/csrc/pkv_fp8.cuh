@@ -22,6 +22,7 @@ namespace fp8 {
 using namespace dev;
 
 constexpr int kFp8Tile = kPage * kD;  // 1 KiB: one (page, KV head) K or V code tile
+constexpr float kDeferLog2 = 8.f;      // softmax reference moves when a score exceeds it by 2^8
 static_assert(kFp8Unit == 2176 && kFp8Unit % 128 == 0, "stage = one unit, 128-byte aligned");
 
 // ------------------------------------------------------------------ quantization
@@ -246,20 +247,43 @@ struct Fp8MmaWarp {
         }
         const float sk0 = scales[gid], sk1 = scales[gid + 8];
         float sv0 = scales[kPage + gid], sv1 = scales[kPage + gid + 8];
-        float x[4] = {s[0] * (sk0 * hf[0]), s[1] * (sk0 * hf[1]), s[2] * (sk1 * hf[0]), s[3] * (sk1 * hf[1])};
+        // Exponents relative to the reference maxima m (log2 domain).  m moves only when a
+        // score exceeds it by more than kDeferLog2 -- then the page's maxima are reduced
+        // across the warp and O^T, l are rescaled -- so most pages need no reduction and
+        // the weights stay below 2^kDeferLog2 (m, l, o remain a valid log-sum-exp triple).
+        const float skh00 = sk0 * hf[0], skh01 = sk0 * hf[1], skh10 = sk1 * hf[0], skh11 = sk1 * hf[1];
+        float z[4] = {fmaf(s[0], skh00, -m[0]), fmaf(s[1], skh01, -m[1]), fmaf(s[2], skh10, -m[0]),
+                      fmaf(s[3], skh11, -m[1])};
         if (gid >= nvalid) {
-            x[0] = x[1] = -INFINITY;
+            z[0] = z[1] = -INFINITY;
             sv0 = 0.f;
         }
         if (gid + 8 >= nvalid) {
-            x[2] = x[3] = -INFINITY;
+            z[2] = z[3] = -INFINITY;
             sv1 = 0.f;
         }
-        float pm0 = fmaxf(x[0], x[2]), pm1 = fmaxf(x[1], x[3]);
+        float al0 = 1.f, al1 = 1.f;
+        if (__any_sync(kFull, fmaxf(fmaxf(z[0], z[1]), fmaxf(z[2], z[3])) > kDeferLog2)) {
+            float x[4] = {s[0] * skh00, s[1] * skh01, s[2] * skh10, s[3] * skh11};
+            if (gid >= nvalid)
+                x[0] = x[1] = -INFINITY;
+            if (gid + 8 >= nvalid)
+                x[2] = x[3] = -INFINITY;
+            float pm0 = fmaxf(x[0], x[2]), pm1 = fmaxf(x[1], x[3]);
 #pragma unroll
-        for (int off = 4; off <= 16; off <<= 1) {
-            pm0 = fmaxf(pm0, __shfl_xor_sync(kFull, pm0, off));
-            pm1 = fmaxf(pm1, __shfl_xor_sync(kFull, pm1, off));
+            for (int off = 4; off <= 16; off <<= 1) {
+                pm0 = fmaxf(pm0, __shfl_xor_sync(kFull, pm0, off));
+                pm1 = fmaxf(pm1, __shfl_xor_sync(kFull, pm1, off));
+            }
+            const float mn0 = fmaxf(m[0], pm0), mn1 = fmaxf(m[1], pm1);
+            al0 = ex2_approx(m[0] - mn0);  // 0 on the first page (m = -inf)
+            al1 = ex2_approx(m[1] - mn1);
+            m[0] = mn0;
+            m[1] = mn1;
+            z[0] = x[0] - mn0;
+            z[1] = x[1] - mn1;
+            z[2] = x[2] - mn0;
+            z[3] = x[3] - mn1;
         }
         // raise sref when a V scale of this page exceeds it (rare after the first pages)
         float grow = 1.f;
@@ -273,14 +297,10 @@ struct Fp8MmaWarp {
             sref = smax;
             sinv = inv;
         }
-        const float mn0 = fmaxf(m[0], pm0), mn1 = fmaxf(m[1], pm1);
-        const float al0 = ex2_approx(m[0] - mn0), al1 = ex2_approx(m[1] - mn1);
-        const float p0 = ex2_approx(x[0] - mn0), p1 = ex2_approx(x[1] - mn1);
-        const float p2 = ex2_approx(x[2] - mn0), p3 = ex2_approx(x[3] - mn1);
+        const float p0 = ex2_approx(z[0]), p1 = ex2_approx(z[1]);
+        const float p2 = ex2_approx(z[2]), p3 = ex2_approx(z[3]);
         l[0] = fmaf(l[0], al0, p0 + p2);
         l[1] = fmaf(l[1], al1, p1 + p3);
-        m[0] = mn0;
-        m[1] = mn1;
         // ---- P''^T as the B operand (FP16): p * scale_v / sref, transposed
         const float r0 = sv0 * sinv, r1 = sv1 * sinv;
         const uint32_t b0 = movmatrix_trans(pack_f16x2(p0 * r0, p1 * r0));  // tokens 2tig, 2tig+1 ; head gid
