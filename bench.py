@@ -314,15 +314,15 @@ def run_trace(args):
     seed = replica_seed(args.seed, rank)
     options = (VARIANTS[args.variant] | pkv.PKV_STEP_RING(args.ring) | (pkv.PKV_STEP_NO_PDL if args.no_pdl else 0)
                | (pkv.PKV_STEP_SORTED if args.sorted else 0))
-    pages = args.pool_mib * 2**20 // pkv.PKV_PAGE_BYTES
+    pages = args.pool_mib * 2**20 // (pkv.PKV_PAGE_BYTES_FP8 if args.kv == "fp8" else pkv.PKV_PAGE_BYTES)
     reqs = wl.trace_schedule(seed=seed, steps=steps)
     # warm-up: a short trace on a small runner (kernel attributes, tensor maps)
     warm = TraceRunner(pool_pages=4096, layers=16, max_batch=8, seed=seed + 1,
-                       pages_per_chunk=args.pages_per_chunk, options=options)
+                       pages_per_chunk=args.pages_per_chunk, options=options, kv=args.kv)
     warm.run(wl.trace_schedule(seed=seed + 1, steps=max(args.warmup, 3), arrival_rate=2.0), max(args.warmup, 3))
     warm.close()
     runner = TraceRunner(pool_pages=pages, layers=16, max_batch=192, static=args.static, seed=seed,
-                         pages_per_chunk=args.pages_per_chunk, options=options)
+                         pages_per_chunk=args.pages_per_chunk, options=options, kv=args.kv)
     uuid = str(getattr(torch.cuda.get_device_properties(local), "uuid", "") or "")
     sampler = ClockSampler(uuid if uuid.startswith("GPU-") else (f"GPU-{uuid}" if uuid else str(local)))
     sampler.start()
@@ -338,8 +338,10 @@ def run_trace(args):
     value = res.kv_bytes * world / gpu_s / 1e9
     line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * gpu_s / max(res.decode_steps, 1),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if args.kv == "bf16" else "fp8e4m3 KV, f16 MMA, f32 softmax", "data": "synthetic",
             "config": {"workload": f"trace: {CONFIG_TEXT['trace']}", "layers": 16, "pool_mib": args.pool_mib,
+                       "kv_pages": args.kv,
                        "pages_per_chunk": args.pages_per_chunk, "ring": args.ring, "kernel_variant": args.variant,
                        "batching": "static" if args.static else "continuous", "requests": len(reqs),
                        "seed": args.seed, "l2": "KV per step far above L2 once the batch has grown; no flush"},

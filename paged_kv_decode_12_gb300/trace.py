@@ -41,13 +41,19 @@ class TraceResult:
 class TraceRunner:
     def __init__(self, pool_pages: int, layers: int = 16, max_batch: int = 192, max_blocks: int = wl.MAX_BLOCKS,
                  max_context: int = wl.MAX_CONTEXT, static: bool = False, seed: int = wl.DEFAULT_SEED,
-                 pages_per_chunk: int = 32, options: int = pkv.PKV_STEP_RING(2), device: str = "cuda"):
+                 pages_per_chunk: int = 32, options: int = pkv.PKV_STEP_RING(2), device: str = "cuda",
+                 kv: str = "bf16"):
         self.device = torch.device(device)
         self.layers, self.max_batch, self.max_blocks, self.max_context = layers, max_batch, max_blocks, max_context
         self.pages_per_chunk, self.options, self.seed = pages_per_chunk, options, seed
         self.scale = 1.0 / math.sqrt(wl.HEAD_DIM)
-        self.slab = torch.zeros(pool_pages * pkv.PKV_PAGE_BYTES, dtype=torch.uint8, device=self.device)
-        self.pool = pkv.pkv_pool_create(self.slab, self.slab.numel(), seed=seed)
+        self.kv = kv
+        self.page_bytes = pkv.PKV_PAGE_BYTES_FP8 if kv == "fp8" else pkv.PKV_PAGE_BYTES
+        self.slab = torch.zeros(pool_pages * self.page_bytes, dtype=torch.uint8, device=self.device)
+        if kv == "fp8":  # prompts are quantized by the prefill, decode tokens by the step
+            self.pool = pkv.pkv_pool_create_fp8(self.slab, self.slab.numel(), seed=seed)
+        else:
+            self.pool = pkv.pkv_pool_create(self.slab, self.slab.numel(), seed=seed)
         self.num_pages = pool_pages
         self.sched = pkv.pkv_sched_create(self.pool, layers, max_blocks, max_context, max_batch,
                                           pkv.PKV_SCHED_STATIC if static else pkv.PKV_SCHED_CONTINUOUS)
@@ -60,7 +66,10 @@ class TraceRunner:
         def draw(shape, s):
             return wl.fill_bf16_normal_(torch.empty(shape, dtype=torch.bfloat16, device=self.device), s)
 
-        self.q = draw((layers, max_batch, wl.NUM_Q_HEADS, wl.HEAD_DIM), seed + 1)
+        # q is rotated in place by every step: each step starts from the unrotated draw q0,
+        # as a real step starts from freshly projected queries
+        self.q0 = draw((layers, max_batch, wl.NUM_Q_HEADS, wl.HEAD_DIM), seed + 1)
+        self.q = self.q0.clone()
         self.k_new = draw((layers, max_batch, wl.NUM_KV_HEADS, wl.HEAD_DIM), seed + 2)
         self.v_new = draw((layers, max_batch, wl.NUM_KV_HEADS, wl.HEAD_DIM), seed + 3)
         self.out = torch.zeros((layers, max_batch, wl.NUM_Q_HEADS, wl.HEAD_DIM), dtype=torch.bfloat16,
@@ -69,6 +78,7 @@ class TraceRunner:
         self.lens = torch.zeros(max_batch, dtype=torch.int32, device=self.device)
         self.prompt_bt = torch.full((layers, max_blocks), -1, dtype=torch.int32, device=self.device)
         self._prompt_seed = seed + 100
+        self.prompt_seeds = {}  # request id -> (seed of its prompt K/V draw, prompt length)
 
     def close(self):
         if self.sched is not None:
@@ -79,15 +89,21 @@ class TraceRunner:
             self.pool = None
 
     # ------------------------------------------------------------------ pieces
-    def prefill(self, bt_rows: np.ndarray, prompt_len: int):
-        """Fill one prompt's pages in every layer with seeded N(0,1) K/V."""
-        self.prompt_bt.copy_(torch.from_numpy(bt_rows))
-        self._prompt_seed += 1
+    def prompt_kv(self, seed: int, prompt_len: int):
+        """The seeded N(0,1) prompt K and V of every layer, [layers][prompt_len][8][64] BF16."""
         g = torch.Generator(device=self.device)
-        g.manual_seed(self._prompt_seed)
+        g.manual_seed(seed)
         shape = (self.layers, prompt_len, wl.NUM_KV_HEADS, wl.HEAD_DIM)
         k = torch.randn(shape, generator=g, device=self.device, dtype=torch.float32).to(torch.bfloat16)
         v = torch.randn(shape, generator=g, device=self.device, dtype=torch.float32).to(torch.bfloat16)
+        return k, v
+
+    def prefill(self, bt_rows: np.ndarray, prompt_len: int, rid: int = -1):
+        """Fill one prompt's pages in every layer with seeded N(0,1) K/V."""
+        self.prompt_bt.copy_(torch.from_numpy(bt_rows))
+        self._prompt_seed += 1
+        self.prompt_seeds[rid] = (self._prompt_seed, prompt_len)
+        k, v = self.prompt_kv(self._prompt_seed, prompt_len)
         pkv.pkv_prefill_append(self.pool, k, v, self.prompt_bt, self.max_blocks, self.layers, 0, prompt_len,
                                self.rope, self.max_context, self.err)
 
@@ -106,7 +122,7 @@ class TraceRunner:
         for r in requests:
             by_step.setdefault(r.arrival_step, []).append(r)
         gpu_ms, kv_bytes, tokens, decode_steps, sizes = 0.0, 0, 0, 0, []
-        per_token = wl.kv_bytes_per_token(self.layers)
+        per_token = wl.kv_bytes_per_token(self.layers, kv=self.kv)
         t0 = time.perf_counter()
         for step in range(steps):
             for r in by_step.get(step, []):
@@ -117,7 +133,7 @@ class TraceRunner:
                         raise
             ids, plens, bt_rows = pkv.pkv_sched_admit(self.sched, self.max_batch, self.layers, self.max_blocks)
             for i in range(ids.size):
-                self.prefill(bt_rows[i], int(plens[i]))
+                self.prefill(bt_rows[i], int(plens[i]), int(ids[i]))
             ids, lens, bt = pkv.pkv_sched_decode_batch(self.sched, self.max_batch, self.layers, self.max_blocks)
             B = ids.size
             sizes.append(B)
@@ -125,6 +141,7 @@ class TraceRunner:
                 continue
             self.lens[:B].copy_(torch.from_numpy(lens))
             self.bt[:, :B].copy_(torch.from_numpy(bt))
+            self.q[:, :B].copy_(self.q0[:, :B])
             if before_step:
                 before_step(step, ids, lens, bt)
             start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)

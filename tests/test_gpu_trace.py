@@ -4,8 +4,9 @@ continuous-batching trace.
 * pkv_prefill_append writes exactly the oracle's bytes (positions bit-exact, V
   bit-exact, K within 1 BF16 ulp), the oracle's append applied token by token;
 * during a trace (admission by page budget, prefill, lazy pages, retirement),
-  sampled outputs of several steps match the oracle computed on a snapshot of the
-  sequence's pages taken just before the step.
+  sampled outputs of several steps match the oracle, which rebuilds the sequence's
+  pages from the raw seeded inputs (prompt draw, each step's new K/V row), for BF16
+  and FP8 pages.
 """
 import math
 
@@ -68,44 +69,56 @@ def test_prefill_fill_matches_oracle(start, T):
     pkv.pkv_pool_destroy(p)
 
 
-def test_trace_steps_match_oracle():
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_trace_steps_match_oracle(kv):
+    # The oracle rebuilds each sampled sequence's pages from the raw seeded inputs that
+    # went into them -- the prompt K/V draw of its admission and the new K/V row of every
+    # step since -- and decodes with the step's unrotated query; nothing the CUDA path
+    # wrote is read back as an oracle input.
     layers, max_batch = 2, 24
-    runner = TraceRunner(pool_pages=3000, layers=layers, max_batch=max_batch, pages_per_chunk=4, seed=5)
+    runner = TraceRunner(pool_pages=3000, layers=layers, max_batch=max_batch, pages_per_chunk=4, seed=5, kv=kv)
+    fp8 = kv == "fp8"
     reqs = wl.trace_schedule(seed=5, steps=60, arrival_rate=0.8, prompt_lo=8, prompt_hi=200, out_lo=4, out_hi=60)
     rng = np.random.default_rng(9)
     check_steps = {3, 17, 31, 45, 59}
+    k_new, v_new, q0 = u16(runner.k_new), u16(runner.v_new), u16(runner.q0)
+    history = {}   # request id -> [(position, batch slot)] of its decode tokens so far
     pending = {}
 
     def before(step, ids, lens, bt):
-        if step not in check_steps:
-            return
-        picks = []
-        for _ in range(4):
-            b = int(rng.integers(ids.size))
-            layer = int(rng.integers(layers))
-            h = int(rng.integers(wl.NUM_Q_HEADS))
-            L = int(lens[b])
-            npg = math.ceil(L / PS)
-            pages = torch.from_numpy(bt[layer, b, :npg].astype(np.int64)).cuda()
-            pool_view = runner.slab.view(torch.bfloat16).view(runner.num_pages, 2, HKV, PS, D)
-            picks.append(dict(b=b, layer=layer, h=h, L=L, npg=npg, mini=u16(pool_view[pages]).reshape(-1).copy(),
-                              q=u16(runner.q[layer, b]).copy(), k=u16(runner.k_new[layer, b]).copy(),
-                              v=u16(runner.v_new[layer, b]).copy()))
-        pending[step] = picks
+        for b, rid in enumerate(ids.tolist()):
+            history.setdefault(rid, []).append((int(lens[b]) - 1, b))
+        if step in check_steps:
+            pending[step] = [(int(rng.integers(ids.size)), int(rng.integers(layers)), int(rng.integers(wl.NUM_Q_HEADS)),
+                              ids.copy(), lens.copy()) for _ in range(4)]
+
+    def oracle_out(rid, L, layer, b, h):
+        seed, plen = runner.prompt_seeds[rid]
+        kp, vp = runner.prompt_kv(seed, plen)
+        k = np.concatenate([u16(kp)[layer], np.stack([k_new[layer, s] for _, s in history[rid]])])
+        v = np.concatenate([u16(vp)[layer], np.stack([v_new[layer, s] for _, s in history[rid]])])
+        assert k.shape[0] == L and [p for p, _ in history[rid]] == list(range(plen, L))
+        npg = math.ceil(L / PS)
+        g = oracle.geom(npg)
+        row = np.full((1, runner.max_blocks), -1, dtype=np.int32)
+        row[0, :npg] = np.arange(npg)
+        mini = np.zeros(npg * oracle.FP8_PAGE_BYTES, np.uint8) if fp8 else ph.new_pool(npg)
+        append = oracle.append_fp8 if fp8 else oracle.append
+        for pos in range(L - 1):
+            append(mini, g, row, [pos], k[pos][None], v[pos][None])
+        q = q0[layer, b][None].copy()
+        append(mini, g, row, [L - 1], k[L - 1][None], v[L - 1][None], q)
+        decode_one = oracle.decode_one_fp8 if fp8 else oracle.decode_one
+        return decode_one(mini, g, row[0], L, q[0, h], h // 4, runner.scale)
 
     def after(step, ids, lens, bt):
         if step not in pending:
             return
         torch.cuda.synchronize()
         out = u16(runner.out)
-        for pk in pending.pop(step):
-            g = oracle.geom(pk["npg"])
-            row = np.full((1, runner.max_blocks), -1, dtype=np.int32)
-            row[0, :pk["npg"]] = np.arange(pk["npg"])
-            q = pk["q"][None].copy()
-            oracle.append(pk["mini"], g, row, [pk["L"] - 1], pk["k"][None], pk["v"][None], q)
-            ref = oracle.decode_one(pk["mini"], g, row[0], pk["L"], q[0, pk["h"]], pk["h"] // 4, runner.scale)
-            assert_close(out[pk["layer"], pk["b"], pk["h"]], ref)
+        for b, layer, h, ids_, lens_ in pending.pop(step):
+            ref = oracle_out(int(ids_[b]), int(lens_[b]), layer, b, h)
+            assert_close(out[layer, b, h], ref)
 
     res = runner.run(reqs, 60, before, after)
     assert not pending
