@@ -493,21 +493,21 @@ def run_pkv(args):
 
 def measure_e2e(dw, args, world, device):
     """Same metric through DecodeEngine.run_host: every step copies q, k_new, v_new,
-    positions and lengths from pinned host memory and the output back, on the stream."""
+    positions and lengths (packed, one copy) from pinned host memory and the output back,
+    on the stream."""
     import torch
 
     from paged_kv_decode_12_gb300 import harness
 
-    host_in = harness.host_pinned_inputs(dw)
-    dev_in = {"q": dw.q, "k_new": dw.k_new, "v_new": dw.v_new, "pos": dw.pos, "seq_lens": dw.seq_lens}
+    io = harness.host_pinned_inputs(dw)
     out_host = torch.empty(dw.out.shape, dtype=dw.out.dtype).pin_memory()
     n = max(1, min(args.steps, args.e2e_steps))
     for _ in range(2):
-        dw.eng.run_host(host_in, dev_in, dw.out, out_host)
+        dw.eng.run_host(io, dw.out, out_host)
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
         for _ in range(n):
-            dw.eng.run_host(host_in, dev_in, dw.out, out_host)
+            dw.eng.run_host(io, dw.out, out_host)
     g.replay()
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -516,11 +516,12 @@ def measure_e2e(dw, args, world, device):
     end.record()
     torch.cuda.synchronize()
     ms = reduce_max(start.elapsed_time(end), world, device)
-    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    h2d = io.bytes
     d2h = out_host.numel() * out_host.element_size()
     return {"value": dw.w.kv_bytes_per_step(dw.eng.kv) * n * world / (ms / 1e3) / 1e9, "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n, "ms_per_step": ms / n,
-            "path": "DecodeEngine.run_host (pinned host in/out, copies on the kernels' stream, CUDA graph)"}
+            "path": "DecodeEngine.run_host (packed pinned host inputs: one H2D copy, one D2H copy of the output, "
+                    "on the kernels' stream, CUDA graph)"}
 
 
 def main(argv=None):

@@ -145,14 +145,36 @@ class DecodeEngine:
             if layer_hook:
                 layer_hook(layer, "after")
 
-    def run_host(self, host_in: dict, dev_in: dict, out_dev, out_host, stream=None) -> None:
-        """End-to-end step: copy q, k_new, v_new, pos, seq_lens from pinned host tensors into the
-        device tensors, run the step, copy the output back to pinned host memory."""
-        for k in ("q", "k_new", "v_new", "pos", "seq_lens"):
-            dev_in[k].copy_(host_in[k], non_blocking=True)
-        self.step(dev_in["q"], dev_in["k_new"], dev_in["v_new"], dev_in["pos"], dev_in["seq_lens"], out_dev,
-                  stream)
+    def run_host(self, io: "PackedIO", out_dev, out_host, stream=None) -> None:
+        """End-to-end step: one copy of the step's inputs (q, k_new, v_new, pos, seq_lens, packed
+        back to back in pinned host memory) to the device, the step, one copy of the output back
+        to pinned host memory; all on the kernels' stream."""
+        io.dev.copy_(io.host, non_blocking=True)
+        d = io.d
+        self.step(d["q"], d["k_new"], d["v_new"], d["pos"], d["seq_lens"], out_dev, stream)
         out_host.copy_(out_dev, non_blocking=True)
 
     def check_errors(self):
         return pkv.pkv_check_device_error(self.err)
+
+
+class PackedIO:
+    """A step's inputs packed back to back (256-byte aligned) in one pinned host buffer and one
+    device buffer of the same layout, so that the end-to-end step moves them with one copy.
+    ``h[name]`` / ``d[name]`` are host / device views with the tensors' shapes and dtypes."""
+
+    def __init__(self, tensors: dict, device):
+        offsets, off = {}, 0
+        for name, t in tensors.items():
+            offsets[name] = off
+            off += (t.numel() * t.element_size() + 255) // 256 * 256
+        self.host = torch.empty(off, dtype=torch.uint8).pin_memory()
+        self.dev = torch.empty(off, dtype=torch.uint8, device=device)
+        self.bytes = sum(t.numel() * t.element_size() for t in tensors.values())
+        self.h, self.d = {}, {}
+        for name, t in tensors.items():
+            n = t.numel() * t.element_size()
+            o = offsets[name]
+            self.h[name] = self.host[o:o + n].view(t.dtype).view(t.shape)
+            self.d[name] = self.dev[o:o + n].view(t.dtype).view(t.shape)
+            self.h[name].copy_(t.cpu())

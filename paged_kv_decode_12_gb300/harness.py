@@ -131,10 +131,13 @@ def warm(dw: DeviceWorkload, n: int = 2) -> None:
     torch.cuda.synchronize()
 
 
-def host_pinned_inputs(dw: DeviceWorkload) -> dict:
-    """Pinned host copies of one step's inputs (for the end-to-end measurement)."""
-    return {k: getattr(dw, k if k != "q" else "q0").cpu().pin_memory()
-            for k in ("q", "k_new", "v_new", "pos", "seq_lens")}
+def host_pinned_inputs(dw: DeviceWorkload):
+    """One step's inputs (the unrotated q, k_new, v_new, pos, seq_lens) packed in pinned host
+    memory, with a device buffer of the same layout (for the end-to-end measurement)."""
+    from .engine import PackedIO
+
+    return PackedIO({"q": dw.q0, "k_new": dw.k_new, "v_new": dw.v_new, "pos": dw.pos, "seq_lens": dw.seq_lens},
+                    dw.eng.device)
 
 
 def sample_units(w: wl.Workload, n: int, seed: int) -> list:

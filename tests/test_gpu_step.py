@@ -150,3 +150,22 @@ def test_sorted_order_with_invalid_lengths_and_ring(chunk):
     zero = np.arange(lens.size) % 7 == 3
     assert np.all(bad["out"][zero] == 0)
     assert np.array_equal(bad["out"][~zero], g["out"][~zero])
+
+
+def test_run_host_equals_device_step():
+    # the end-to-end form (packed pinned inputs, one copy each way) computes the same step
+    from paged_kv_decode_12_gb300 import harness
+
+    dw = harness.setup("tiny", pages_per_chunk=1, ring=2)
+    pool0 = dw.eng.slab.clone()
+    dw.step()
+    torch.cuda.synchronize()
+    ref = u16(dw.out)
+    dw.eng.slab.copy_(pool0)
+    io = harness.host_pinned_inputs(dw)
+    out_host = torch.empty(dw.out.shape, dtype=dw.out.dtype).pin_memory()
+    dw.eng.run_host(io, dw.out, out_host)
+    torch.cuda.synchronize()
+    assert np.array_equal(u16(out_host), ref)
+    assert io.bytes == sum(t.numel() * t.element_size() for t in (dw.q0, dw.k_new, dw.v_new, dw.pos, dw.seq_lens))
+    dw.eng.close()
