@@ -357,9 +357,14 @@ int oracle_decode_contiguous(const double *K, const double *V, int S, const int3
  *  - one FP32 scale per (token, KV head) row of 64 values: scale = amax / 448
  *    (FP32 division; 1 for an all-zero row), code = E4M3(x / scale) with x / scale
  *    an FP32 division; the row's input is the BF16 value the BF16 path would store;
- *  - page = kv_heads units, one per KV head, each the codes [2 (K,V)][page_size]
- *    [head_dim] (1 byte each) followed by the scales [2][page_size] FP32:
- *    8 x (2048 + 128) = 17408 bytes for 8 x 16 x 64.                                */
+ *  - page = kv_heads units, one per KV head, each the K codes [page_size][head_dim]
+ *    (1 byte each, row-major), the V codes (same bytes, stored token-pair
+ *    interleaved, below), then the scales [2 (K,V)][page_size] FP32:
+ *    8 x (2048 + 128) = 17408 bytes for 8 x 16 x 64;
+ *  - V codes: slots 2p and 2p+1 share a 2 x head_dim byte line; in it, dims
+ *    8c .. 8c+7 of both slots form 16-byte chunk c (byte 2 (dim % 8) + slot % 2),
+ *    stored at chunk position c XOR (2p mod head_dim/8) (head_dim/8 a power of two).
+ *    Where each byte goes is storage only: every value is the same code.            */
 
 uint8_t oracle_e4m3_from_double(double x)
 {
@@ -428,8 +433,13 @@ static int64_t fp8_unit_bytes(const oracle_pool_geom *g)
 /* byte offset of a code / of a row's scale inside the FP8 pool */
 int64_t oracle_fp8_code_offset(const oracle_pool_geom *g, int page, int kv, int head, int slot, int dim)
 {
-    int64_t row = (int64_t)kv * g->page_size + slot;
-    return (int64_t)page * oracle_fp8_page_bytes(g) + head * fp8_unit_bytes(g) + row * g->head_dim + dim;
+    int64_t unit = (int64_t)page * oracle_fp8_page_bytes(g) + head * fp8_unit_bytes(g);
+    if (kv == 0)
+        return unit + (int64_t)slot * g->head_dim + dim;
+    int pair = slot / 2, chunks = g->head_dim / 8;
+    int chunk = (dim / 8) ^ ((2 * pair) % chunks);
+    return unit + (int64_t)g->page_size * g->head_dim + (int64_t)pair * 2 * g->head_dim + chunk * 16 +
+           2 * (dim % 8) + slot % 2;
 }
 
 int64_t oracle_fp8_scale_offset(const oracle_pool_geom *g, int page, int kv, int head, int slot)

@@ -78,15 +78,7 @@ def fp8_pool(num_pages):
     return np.full(num_pages * PAGE, 0xA5, dtype=np.uint8)
 
 
-UNIT = PAGE // HKV            # one KV head's codes [2][16][64] then scales [2][16]
-
-
-def fp8_views(pool):
-    """(codes [pages][2][heads][16][64], scales [pages][2][heads][16]) as views of ``pool``."""
-    units = pool.reshape(-1, HKV, UNIT)
-    codes = units[:, :, :CODES // HKV].reshape(-1, HKV, 2, PS, D).transpose(0, 2, 1, 3, 4)
-    scales = units[:, :, CODES // HKV:].view(np.float32).reshape(-1, HKV, 2, PS).transpose(0, 2, 1, 3)
-    return codes, scales
+UNIT = PAGE // HKV            # one KV head's codes (K rows, interleaved V rows) then scales [2][16]
 
 
 def test_fp8_decode_equals_contiguous_dequantized():
@@ -95,7 +87,7 @@ def test_fp8_decode_equals_contiguous_dequantized():
     num_pages = ph.pages_needed(lens) + 2
     bt = wl.permutation_block_tables(rng, lens, num_pages, 8)
     pool = fp8_pool(num_pages)
-    codes_v, scales_v = fp8_views(pool)
+    pv = ph.Fp8Pages(pool)
     S = int(lens.max())
     K = np.zeros((len(lens), HKV, S, D))
     V = np.zeros((len(lens), HKV, S, D))
@@ -105,8 +97,7 @@ def test_fp8_decode_equals_contiguous_dequantized():
             for kv, dst in ((0, K), (1, V)):
                 for h in range(HKV):
                     c, s = oracle.quantize_row_fp8(wl.bf16_normal_host(rng, (D,)))
-                    codes_v[page, kv, h, slot] = c
-                    scales_v[page, kv, h, slot] = s
+                    pv.set_row(page, kv, h, slot, c, s)
                     dst[b, h, t] = oracle.e4m3_to_f64(c) * float(s)
     q = wl.bf16_normal_host(rng, (len(lens), HQ, D))
     _, paged = oracle.decode_fp8(pool, oracle.geom(num_pages), bt, lens, q, 1 / 8)
@@ -133,7 +124,8 @@ def test_fp8_append_matches_bf16_append_then_quantize():
     oracle.append(ref, g, bt, lens - 1, k_new, v_new, q_bf16)
     assert np.array_equal(q_fp8, q_bf16)
     assert np.count_nonzero(pool != before) <= 3 * (2 * HKV * D + 2 * HKV * 4)
-    codes_v, scales_v = fp8_views(pool)
+    pv = ph.Fp8Pages(pool)
+    codes_v, scales_v = pv.codes(), pv.scales
     R = ph.pool_view(ref)
     for b in range(3):
         page, slot = bt[b, (lens[b] - 1) // PS], (lens[b] - 1) % PS
@@ -141,7 +133,12 @@ def test_fp8_append_matches_bf16_append_then_quantize():
             for kv in (0, 1):
                 c, s = oracle.quantize_row_fp8(R[page, kv, h, slot])
                 assert np.array_equal(codes_v[page, kv, h, slot], c) and scales_v[page, kv, h, slot] == s
-    # head-major page: head 2's unit starts at 2 * 2176; V row 3 of it at 16 rows of 64 + 3 rows
-    assert oracle.fp8_code_offset(g, 1, 1, 2, 3, 4) == PAGE + 2 * UNIT + (PS + 3) * D + 4
+    # head-major page: head 2's unit starts at 2 * 2176; K row 3 at 3 rows of 64; V slot 3 is the
+    # odd slot of pair 1 (line 1 of 128 bytes), dim 4 in chunk 0, stored at chunk 0 ^ 2 = 2
+    assert oracle.fp8_code_offset(g, 1, 0, 2, 3, 4) == PAGE + 2 * UNIT + 3 * D + 4
+    assert oracle.fp8_code_offset(g, 1, 1, 2, 3, 4) == PAGE + 2 * UNIT + PS * D + 1 * 128 + 2 * 16 + 2 * 4 + 1
+    assert oracle.fp8_code_offset(g, 0, 1, 0, 14, 63) == PS * D + 7 * 128 + (7 ^ 6) * 16 + 2 * 7 + 0
     assert oracle.fp8_scale_offset(g, 1, 1, 2, 3) == PAGE + 2 * UNIT + 2 * PS * D + (PS + 3) * 4
-    assert UNIT == 2176 and oracle.fp8_code_offset(g, 0, 1, 7, 15, 63) + 1 + 2 * PS * 4 == PAGE
+    assert UNIT == 2176
+    unit_codes = {oracle.fp8_code_offset(g, 0, kv, 7, s, d) for kv in (0, 1) for s in range(PS) for d in range(D)}
+    assert unit_codes == set(range(7 * UNIT, 7 * UNIT + 2 * PS * D))   # the codes fill their 2 KiB exactly
