@@ -115,9 +115,11 @@ int pkv_pool_create(void *dev_slab, size_t slab_bytes, int page_size, int num_kv
  * section 5.1:
  * keep the KV cache in low precision and dequantize before attention; the scheme
  * is this library's reading).  A page is 17408 bytes: 8 units of 2176 bytes, one
- * per KV head, each the codes [2 (K,V)][16 slots][64 dims] (one byte each, E4M3
- * without infinities, largest 448) followed by the row scales [2][16] FP32, so that
- * one (page, KV head) is one contiguous copy.  A row of 64 values x is stored
+ * per KV head, each the K codes [16 slots][64 dims], the V codes (1024 bytes: slots
+ * 2p and 2p+1 share line p of 128 bytes, in which dims 8c..8c+7 of both form 16-byte
+ * chunk c -- byte 2 (dim % 8) + slot % 2 -- stored at chunk position c XOR (2p mod 8))
+ * and the row scales [2 (K,V)][16] FP32; codes are E4M3 without infinities (largest
+ * 448), one byte each.  One (page, KV head) is one contiguous copy.  A row of 64 values x is stored
  * as scale = amax|x| / 448 (FP32; 1 for an all-zero row) and codes
  * E4M3_rne_satfinite(x / scale) (FP32 division); x is the BF16 value the BF16 path
  * would store (the rotated key, or the value).  Every entry point below accepts

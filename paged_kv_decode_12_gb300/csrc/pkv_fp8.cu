@@ -73,8 +73,9 @@ __device__ __forceinline__ void store_value_row_fp8(uint8_t *page, int h, int sl
     quantize_pair(bf16lo(w), bf16hi(w), c0, c1, scale);
     const uint32_t c = c0 | (c1 << 8);
     uint8_t *unit = page + (size_t)h * kFp8Unit;
-    uint8_t *row = unit + (kPage + slot) * kD;
-    reinterpret_cast<uint16_t *>(row)[lane] = (uint16_t)c;
+    uint8_t *vt = unit + kFp8Tile;  // token-pair interleaved V codes
+    vt[v_code_offset(slot, 2 * lane)] = (uint8_t)c;
+    vt[v_code_offset(slot, 2 * lane + 1)] = (uint8_t)(c >> 8);
     if (lane == 0)
         reinterpret_cast<float *>(unit + kFp8UnitCodes)[kPage + slot] = scale;
 }

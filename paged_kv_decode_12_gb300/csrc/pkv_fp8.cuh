@@ -51,6 +51,16 @@ __device__ __forceinline__ float bf16_round(float x)
     return __bfloat162float(__float2bfloat16_rn(x));
 }
 
+// Byte offset, inside a unit's V code tile, of the code of (slot, dim): slots 2p and 2p+1
+// share a 128-byte line; dims 8c..8c+7 of both form 16-byte chunk c (byte 2 (dim % 8) +
+// slot % 2), stored at chunk position c ^ (2p % 8), so that the decode's 16-byte reads of
+// one chunk by the lanes of a quarter warp fall in distinct bank groups.
+__device__ __forceinline__ int v_code_offset(int slot, int dim)
+{
+    const int pair = slot >> 1;
+    return pair * 2 * kD + (((dim >> 3) ^ ((2 * pair) & 7)) << 4) + ((dim & 7) << 1) + (slot & 1);
+}
+
 // The row codes of one warp's BF16-valued pair (y1, y2) per lane (a row of 64 values
 // held as lane i: values i and i + 32, or 2i and 2i + 1): the row scale and the two
 // lanes' codes, with the arithmetic every FP8 writer uses.
@@ -163,7 +173,6 @@ struct Fp8MmaWarp {
     float o[4][4];      // O^T accumulators, in units of sref
     float m[2], l[2];
     float sref, sinv;   // largest V scale so far (warp-uniform) and its reciprocal
-    uint32_t sel_lo, sel_hi;  // byte-permute selectors pairing tokens (2tig, 2tig+1) per dim
     int lane;
 
     __device__ __forceinline__ void init(const uint16_t *qg, float scale_log2, int lane_)
@@ -221,11 +230,6 @@ struct Fp8MmaWarp {
         l[0] = l[1] = 0.f;
         sref = 0.f;
         sinv = 0.f;
-        // tokens are loaded in the order (2tig + par, 2tig + 1 - par), par = bit 0 of tig;
-        // the selectors put token 2tig's code in the low byte of each pair either way
-        const bool par = tig & 1;
-        sel_lo = par ? 0x1504u : 0x5140u;  // codes of dims +0, +1 (or +4, +5)
-        sel_hi = par ? 0x3726u : 0x7362u;  // codes of dims +2, +3 (or +6, +7)
     }
 
     // unit: the stage -- K code rows, V code rows (64 bytes each), K scales[16], V scales[16]
@@ -315,22 +319,19 @@ struct Fp8MmaWarp {
                 o[i][3] *= c1;
             }
         }
-        // ---- V code rows: dims 8gid..8gid+7 of tokens 2tig(+1), 2tig+8(+1)
+        // ---- V codes: dims 8gid..8gid+7 of token pairs tig (2tig, 2tig+1) and tig+4
+        // (2tig+8, 2tig+9), one 16-byte chunk each in the token-pair interleaved layout:
+        // word i holds dims 8gid+2i, 8gid+2i+1 of both tokens, i.e. m-tile i's rows gid, gid+8
         const uint8_t *vt = codes + kFp8Tile;
-        const int par = tig & 1;
-        const uint32_t col = (uint32_t)(8 * gid);
-        const uint2 u0 = *reinterpret_cast<const uint2 *>(vt + (2 * tig + par) * kD + col);
-        const uint2 u1 = *reinterpret_cast<const uint2 *>(vt + (2 * tig + 1 - par) * kD + col);
-        const uint2 u2 = *reinterpret_cast<const uint2 *>(vt + (2 * tig + 8 + par) * kD + col);
-        const uint2 u3 = *reinterpret_cast<const uint2 *>(vt + (2 * tig + 9 - par) * kD + col);
+        const uint32_t chunk = (uint32_t)((gid ^ (2 * tig)) << 4);
+        const uint4 u0 = *reinterpret_cast<const uint4 *>(vt + tig * 2 * kD + chunk);
+        const uint4 u1 = *reinterpret_cast<const uint4 *>(vt + (tig + 4) * 2 * kD + chunk);
+        const uint32_t w0[4] = {u0.x, u0.y, u0.z, u0.w}, w1[4] = {u1.x, u1.y, u1.z, u1.w};
         uint32_t a[4][4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const uint32_t sel = (i & 1) ? sel_hi : sel_lo;
-            const uint32_t lo = __byte_perm(i < 2 ? u0.x : u0.y, i < 2 ? u1.x : u1.y, sel);
-            const uint32_t hi = __byte_perm(i < 2 ? u2.x : u2.y, i < 2 ? u3.x : u3.y, sel);
-            e4m3x4_to_f16x2(lo, a[i][0], a[i][1]);  // dim 8gid+2i | 8gid+2i+1, tokens 2tig, 2tig+1
-            e4m3x4_to_f16x2(hi, a[i][2], a[i][3]);  // same dims, tokens 2tig+8, 2tig+9
+            e4m3x4_to_f16x2(w0[i], a[i][0], a[i][1]);  // dim 8gid+2i | 8gid+2i+1, tokens 2tig, 2tig+1
+            e4m3x4_to_f16x2(w1[i], a[i][2], a[i][3]);  // same dims, tokens 2tig+8, 2tig+9
         }
         if (nvalid < kPage) {  // zero V of slots past the sequence end (their bytes are arbitrary)
             const uint32_t mlo =

@@ -592,19 +592,19 @@ struct Fp8StepSmem {
     }
 };
 
-// Lanes 0..9 of a warp write the new token's rows into a unit (a stage or the page):
-// lanes 0-3 the K codes, 4-7 the V codes (16 bytes each), 8 and 9 the two scales.
+// A warp writes the new token's rows into a unit (a stage or the page): lanes 0-3 the
+// K codes (16 bytes each), every lane two V codes (dims 2 lane, 2 lane + 1) at their
+// interleaved positions, lanes 0 and 1 the two scales.
 __device__ __forceinline__ void put_new_token_fp8(uint8_t *unit, int slot, const uint8_t *codes, const float *scales,
                                                   int lane)
 {
-    if (lane < 8) {
-        const int part = lane >> 2, ch = lane & 3;  // part 0: K row, 1: V row
-        *reinterpret_cast<uint4 *>(unit + (part * kPage + slot) * kD + 16 * ch) =
-            reinterpret_cast<const uint4 *>(codes + part * kD)[ch];
-    } else if (lane < 10) {
-        const int part = lane - 8;
-        reinterpret_cast<float *>(unit + kFp8UnitCodes)[part * kPage + slot] = scales[part];
-    }
+    if (lane < 4)
+        *reinterpret_cast<uint4 *>(unit + slot * kD + 16 * lane) = reinterpret_cast<const uint4 *>(codes)[lane];
+    uint8_t *vt = unit + fp8::kFp8Tile;
+    vt[fp8::v_code_offset(slot, 2 * lane)] = codes[kD + 2 * lane];
+    vt[fp8::v_code_offset(slot, 2 * lane + 1)] = codes[kD + 2 * lane + 1];
+    if (lane < 2)
+        reinterpret_cast<float *>(unit + kFp8UnitCodes)[lane * kPage + slot] = scales[lane];
 }
 
 template <int STAGES>

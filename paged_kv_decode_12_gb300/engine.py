@@ -73,7 +73,8 @@ class DecodeEngine:
                                                    wl.HEAD_DIM)
 
     def fp8_views(self):
-        """(codes uint8 [pages][2][8][16][64], scales float32 [pages][2][8][16]) of an FP8 pool."""
+        """(codes uint8 [pages][2][8][16 x 64 bytes], scales float32 [pages][2][8][16]) of an FP8
+        pool; the code bytes are in storage order (K rows; V codes interleaved by token pair)."""
         if self.kv != "fp8":
             raise ValueError("fp8_views needs an FP8 pool")
         # a page is one 2176-byte unit per KV head: codes [2][16][64], then scales [2][16]

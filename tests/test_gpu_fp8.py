@@ -52,14 +52,11 @@ def dev_bf16(a: np.ndarray) -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(a).view(np.int16).copy()).view(torch.bfloat16).cuda()
 
 
-UNIT = PAGE // HKV  # one KV head's codes [2][16][64] then scales [2][16]
-
-
 def views(pool: np.ndarray):
-    """(codes [pages][2][8][16][64], scales [pages][2][8][16]) as views into ``pool``."""
-    units = pool.reshape(-1, HKV, UNIT)
-    return (units[:, :, :CODES // HKV].reshape(-1, HKV, 2, PS, D).transpose(0, 2, 1, 3, 4),
-            units[:, :, CODES // HKV:].view(np.float32).reshape(-1, HKV, 2, PS).transpose(0, 2, 1, 3))
+    """(codes [pages][2][8][16][64] (a copy, through the oracle's byte layout), scales
+    [pages][2][8][16] (a view)) of an FP8 pool."""
+    pv = ph.Fp8Pages(pool)
+    return pv.codes(), pv.scales
 
 
 def ulp_distance(a: np.ndarray, b: np.ndarray) -> np.ndarray:
@@ -80,14 +77,13 @@ def make_case(seed, seq_lens, num_pages=None, max_blocks=None):
     num_pages = num_pages or ph.pages_needed(seq_lens) + 2
     bt = wl.permutation_block_tables(rng, seq_lens, num_pages, max_blocks)
     pool = np.full(num_pages * PAGE, SENTINEL, dtype=np.uint8)
-    codes, scales = views(pool)
+    pv = ph.Fp8Pages(pool)
     for b, L in enumerate(seq_lens):
         for t in range(int(L) - 1):
             page, slot = bt[b, t // PS], t % PS
             for kv in (0, 1):
                 for h in range(HKV):
-                    codes[page, kv, h, slot], scales[page, kv, h, slot] = oracle.quantize_row_fp8(
-                        wl.bf16_normal_host(rng, (D,)))
+                    pv.set_row(page, kv, h, slot, *oracle.quantize_row_fp8(wl.bf16_normal_host(rng, (D,))))
     q = wl.bf16_normal_host(rng, (B, HQ, D))
     k_new = wl.bf16_normal_host(rng, (B, HKV, D))
     v_new = wl.bf16_normal_host(rng, (B, HKV, D))
