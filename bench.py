@@ -195,9 +195,11 @@ def measured_traffic(config: str, path: str, variant_name: str, pages_per_chunk:
 
 # --------------------------------------------------------------------------- CPU oracle sample
 
-def oracle_samples(w, n_seqs: int, seed: int):
+def oracle_samples(w, n_seqs: int, seed: int, kv: str = "bf16"):
     """Host-side synthetic inputs for ``n_seqs`` sequences of one layer of workload ``w``
-    (same length mix), each in its own small paged pool."""
+    (same length mix), each in its own small paged pool (FP8 pools: codes drawn as for the
+    GPU workloads, N(0, 128^2) converted to E4M3, row scales uniform in [0.005, 0.009])."""
+    import oracle
     from paged_kv_decode_12_gb300 import workloads as wl
 
     rng = np.random.default_rng(seed)
@@ -206,7 +208,16 @@ def oracle_samples(w, n_seqs: int, seed: int):
     for b in idx:
         L = int(w.seq_lens[b])
         npg = -(-L // wl.PAGE_SIZE)
-        pool = wl.bf16_normal_host(rng, (npg * 2 * wl.NUM_KV_HEADS * wl.PAGE_SIZE * wl.HEAD_DIM,))
+        if kv == "fp8":
+            pool = np.empty(npg * oracle.FP8_PAGE_BYTES, dtype=np.uint8)
+            units = pool.reshape(npg, wl.NUM_KV_HEADS, -1)
+            ncode = 2 * wl.PAGE_SIZE * wl.HEAD_DIM
+            units[:, :, :ncode] = oracle.e4m3_from_f64(
+                np.clip(rng.standard_normal((npg, wl.NUM_KV_HEADS, ncode)) * 128.0, -448, 448))
+            units[:, :, ncode:].view(np.float32)[:] = rng.uniform(0.005, 0.009, (npg, wl.NUM_KV_HEADS,
+                                                                                 2 * wl.PAGE_SIZE))
+        else:
+            pool = wl.bf16_normal_host(rng, (npg * 2 * wl.NUM_KV_HEADS * wl.PAGE_SIZE * wl.HEAD_DIM,))
         bt = wl.permutation_block_tables(rng, [L], npg, w.max_blocks)
         out.append(dict(L=L, npg=npg, pool=pool, bt=bt,
                         q=wl.bf16_normal_host(rng, (1, wl.NUM_Q_HEADS, wl.HEAD_DIM)),
@@ -215,31 +226,32 @@ def oracle_samples(w, n_seqs: int, seed: int):
     return out
 
 
-def oracle_run_sample(sample) -> int:
+def oracle_run_sample(sample, kv: str = "bf16") -> int:
     """One oracle pass (append + attention, all 32 heads) over each sampled sequence;
     returns the KV tokens attended."""
     import oracle
     from paged_kv_decode_12_gb300 import workloads as wl
 
+    append, decode = (oracle.append_fp8, oracle.decode_fp8) if kv == "fp8" else (oracle.append, oracle.decode)
     tokens = 0
     for s in sample:
         g = oracle.geom(s["npg"])
         q = s["q"].copy()
-        oracle.append(s["pool"], g, s["bt"], [s["L"] - 1], s["k_new"], s["v_new"], q)
-        oracle.decode(s["pool"], g, s["bt"], [s["L"]], q, 1.0 / math.sqrt(wl.HEAD_DIM))
+        append(s["pool"], g, s["bt"], [s["L"] - 1], s["k_new"], s["v_new"], q)
+        decode(s["pool"], g, s["bt"], [s["L"]], q, 1.0 / math.sqrt(wl.HEAD_DIM))
         tokens += s["L"]
     return tokens
 
 
-def cpu_baseline(w, seconds: float, seed: int) -> dict:
+def cpu_baseline(w, seconds: float, seed: int, kv: str = "bf16") -> dict:
     from paged_kv_decode_12_gb300 import workloads as wl
 
-    per_token = wl.kv_bytes_per_token(1)
-    pool = oracle_samples(w, 64, seed)
+    per_token = wl.kv_bytes_per_token(1, kv=kv)
+    pool = oracle_samples(w, 64, seed, kv)
     tokens, seqs = 0, 0
     t0 = time.perf_counter()
     while time.perf_counter() - t0 < seconds:       # cycle over the prepared sample
-        tokens += oracle_run_sample([pool[seqs % len(pool)]])
+        tokens += oracle_run_sample([pool[seqs % len(pool)]], kv)
         seqs += 1
     dt = time.perf_counter() - t0
     return {"value": tokens * per_token / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
@@ -273,15 +285,15 @@ def run_reference(args):
     w = wl.make_workload(args.config, args.seed)
     if args.layers:
         w.layers = args.layers
-    per_token = wl.kv_bytes_per_token(1)
-    sample = oracle_samples(w, args.ref_seqs, args.seed)
+    per_token = wl.kv_bytes_per_token(1, kv=args.kv)
+    sample = oracle_samples(w, args.ref_seqs, args.seed, args.kv)
     for _ in range(args.warmup):
-        oracle_run_sample(sample)
+        oracle_run_sample(sample, args.kv)
     times = []
     tokens = 0
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        tokens = oracle_run_sample(sample)
+        tokens = oracle_run_sample(sample, args.kv)
         times.append(time.perf_counter() - t0)
     dt = sum(times)
     value = tokens * per_token * args.steps / dt / 1e9
@@ -471,7 +483,7 @@ def run_pkv(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(w, args.cpu_seconds, args.seed)
+        cpu = cpu_baseline(w, args.cpu_seconds, args.seed, args.kv)
 
     line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
