@@ -162,7 +162,8 @@ class ClockSampler:
                 "samples": len(sm), "power_w_max": max(power) if power else None}
 
 
-KERNEL_SOURCES = ("pkv_device.cuh", "pkv_decode.cu", "pkv_step.cu", "pkv_fp8.cu", "pkv_host.cpp")
+# the sources the fused step kernels are built from (kernels, policies, tensor maps)
+KERNEL_SOURCES = ("pkv_device.cuh", "pkv_fp8.cuh", "pkv_step.cu", "pkv_host.cpp", "pkv_internal.h")
 
 
 def kernel_source_digest() -> str:

@@ -94,7 +94,7 @@ extern "C" int pkv_append_rope(const pkv_pool *pool, const uint16_t *k_new, cons
         return PKV_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
     if (pool->kv_format == PKV_KV_FP8)
-        return fp8_append_rope(pool, k_new, v_new, q, bt_dev, max_blocks, pos_dev, 0, B, rope_table, max_pos,
+        return fp8_append_rope(pool, k_new, v_new, q, bt_dev, max_blocks, pos_dev, B, rope_table, max_pos,
                                dev_err_flag, s);
     append_rope_kernel<<<B, kAppendThreads, 0, s>>>(reinterpret_cast<uint16_t *>(pool->slab), pool->num_pages,
                                                     k_new, v_new, q, bt_dev, max_blocks, pos_dev,

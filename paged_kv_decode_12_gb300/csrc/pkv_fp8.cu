@@ -87,11 +87,11 @@ constexpr int kAppendThreads = kHkv * 32;  // one warp per KV head
 __global__ void __launch_bounds__(kAppendThreads)
 append_rope_fp8_kernel(uint8_t *__restrict__ slab, int num_pages, const uint16_t *__restrict__ k_new,
                        const uint16_t *__restrict__ v_new, uint16_t *__restrict__ q, const int32_t *__restrict__ bt,
-                       int max_blocks, const int32_t *__restrict__ pos, int pos_offset,
+                       int max_blocks, const int32_t *__restrict__ pos,
                        const float2 *__restrict__ rope, int max_pos, int32_t *__restrict__ err)
 {
     const int b = blockIdx.x;
-    const int p = pos[b] + pos_offset;  // pos_offset -1: `pos` holds the lengths
+    const int p = pos[b];
     if (p < 0 || p >= min(max_pos, max_blocks * kPage)) {
         if (threadIdx.x == 0 && err)
             atomicOr(err, PKV_DEVERR_LENGTH);
@@ -314,11 +314,11 @@ constexpr int kFp8Stages = 4;  // 35 KiB of shared memory: six CTAs per SM
 // ------------------------------------------------------------------ launchers
 
 int fp8_append_rope(const pkv_pool *pool, const uint16_t *k_new, const uint16_t *v_new, uint16_t *q,
-                    const int32_t *bt, int max_blocks, const int32_t *pos, int pos_offset, int B, const float *rope,
+                    const int32_t *bt, int max_blocks, const int32_t *pos, int B, const float *rope,
                     int max_pos, int32_t *err, cudaStream_t s)
 {
     append_rope_fp8_kernel<<<B, kAppendThreads, 0, s>>>(reinterpret_cast<uint8_t *>(pool->slab), pool->num_pages,
-                                                        k_new, v_new, q, bt, max_blocks, pos, pos_offset,
+                                                        k_new, v_new, q, bt, max_blocks, pos,
                                                         reinterpret_cast<const float2 *>(rope), max_pos, err);
     return status_from_cuda(cudaGetLastError());
 }

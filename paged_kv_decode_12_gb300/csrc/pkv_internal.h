@@ -50,7 +50,7 @@ int launch_decode_merge(const int32_t *seq_lens, int max_blocks, int pages_per_c
 // FP8 pools: quantizing append / prefill and the dequantizing split kernel.  The
 // public entry points validate their arguments and dispatch here.
 int fp8_append_rope(const pkv_pool *pool, const uint16_t *k_new, const uint16_t *v_new, uint16_t *q,
-                    const int32_t *bt, int max_blocks, const int32_t *pos, int pos_offset, int B,
+                    const int32_t *bt, int max_blocks, const int32_t *pos, int B,
                     const float *rope, int max_pos, int32_t *err, cudaStream_t s);
 int fp8_prefill_append(const pkv_pool *pool, const uint16_t *k, const uint16_t *v, const int32_t *bt_rows,
                        int max_blocks, int layers, int start_pos, int T, const float *rope, int max_pos,
