@@ -62,7 +62,7 @@ DEFAULT_RING = {"b256": 4, "b64": 2, "b8": 2, "trace": 2}   # TMA stages per war
 # Largest-first unit dispatch (PKV_STEP_SORTED): measured +5 % on the ragged one-wave
 # layers (b64, b8), -3 % on b256 where every unit has the same size.
 DEFAULT_SORTED = {"b256": False, "b64": True, "b8": True, "trace": False}
-DEFAULT_RING_FP8 = {"b256": 4, "b64": 2, "b8": 2, "trace": 2}  # units of 2176 B per warp (FP8 pages), measured
+DEFAULT_RING_FP8 = {"b256": 3, "b64": 2, "b8": 2, "trace": 2}  # units of 2176 B per warp (FP8 pages), measured
 L2_BYTES = 129 * 10**6
 
 

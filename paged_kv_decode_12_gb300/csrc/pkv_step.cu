@@ -607,9 +607,14 @@ __device__ __forceinline__ void put_new_token_fp8(uint8_t *unit, int slot, const
         reinterpret_cast<float *>(unit + kFp8UnitCodes)[lane * kPage + slot] = scales[lane];
 }
 
+// CTAs per SM the register budget is set for.  The 3-stage ring takes 27.5 KB of shared
+// memory per CTA, so seven CTAs fit (at most 72 registers, a few spilled) and keep 7 x 4 x 3
+// units of 2176 B in flight per SM; the other rings keep six (80 registers, none spilled).
+constexpr int fp8_ctas_per_sm(int stages) { return stages == 3 ? 7 : 6; }
+
 template <int STAGES>
-__global__ void __launch_bounds__(kThreads, 6) decode_step_fp8_kernel(const __grid_constant__ CUtensorMap tmap,
-                                                                   StepArgs a)
+__global__ void __launch_bounds__(kThreads, fp8_ctas_per_sm(STAGES))
+    decode_step_fp8_kernel(const __grid_constant__ CUtensorMap tmap, StepArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
     Fp8StepSmem<STAGES> sm(smem_raw);
