@@ -46,7 +46,7 @@ if ROOT not in sys.path:
 METRIC = "paged decode attention KV GB/s (% of GB300 HBM peak) and decode steps/s"
 CONFIG_TEXT = {
     "b256": "long-context batch 256: every sequence 2048 tokens (128 pages), 16 layers, 32 Q / 8 KV heads, "
-            "head_dim 64, BF16 pool of 524288 pages (16 GiB), random page permutation",
+            "head_dim 64, pool of 524288 pages (32 KiB BF16 or 17 KiB FP8 each), random page permutation",
     "b64": "ragged batch 64: log-normal lengths (median 300, sigma 1, clipped to [1, 2048], boundary lengths "
            "1/16/17/32/33/2048 included), 16 layers, 1% of keys x8, 4096 pages per layer",
     "b8": "batch 8: lengths uniform in [1, 2048], 16 layers, 4096 pages of 32 KiB per layer",
