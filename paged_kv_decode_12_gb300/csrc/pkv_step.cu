@@ -341,6 +341,9 @@ struct ConsumerSync {
     __device__ __forceinline__ void operator()() const { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 };
 
+// Chunk counts up to which the merging unit holds every partial in registers.
+constexpr int kMergeRegs = 8;
+
 template <class Warp, class Sync = CtaSync>
 __device__ __forceinline__ void finish_unit(const StepArgs &a, Warp &w, float *state, int *ticket,
                                             const uint16_t *q_rot, int b, int g, int c, int nchunks,
@@ -374,18 +377,47 @@ __device__ __forceinline__ void finish_unit(const StepArgs &a, Warp &w, float *s
     sync();
     if (*ticket != nchunks - 1)
         return;
-    float Mx = -INFINITY;
-    for (int cc = 0; cc < nchunks; ++cc)
-        Mx = fmaxf(Mx, __ldcg(&a.part_ml[base + cc]).x);
     float ls = 0.f, r0 = 0.f, r1 = 0.f;
-    if (Mx != -INFINITY) {
-        for (int cc = 0; cc < nchunks; ++cc) {
-            const float2 ml = __ldcg(&a.part_ml[base + cc]);
-            const float f = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - Mx);
-            const float2 oc = __ldcg(reinterpret_cast<const float2 *>(a.part_o + (base + cc) * kD) + dp);
-            ls = fmaf(f, ml.y, ls);
-            r0 = fmaf(f, oc.x, r0);
-            r1 = fmaf(f, oc.y, r1);
+    const float2 *ml_row = a.part_ml + base;
+    const float2 *o_col = reinterpret_cast<const float2 *>(a.part_o + base * kD) + dp;
+    if (nchunks <= kMergeRegs) {
+        // every partial loaded before the first use: one memory round trip at the end of
+        // the sequence's critical path; the arithmetic below is the general loop's
+        float2 ml[kMergeRegs], oc[kMergeRegs];
+#pragma unroll
+        for (int cc = 0; cc < kMergeRegs; ++cc)
+            if (cc < nchunks) {
+                ml[cc] = __ldcg(ml_row + cc);
+                oc[cc] = __ldcg(o_col + cc * (kD / 2));
+            }
+        float Mx = -INFINITY;
+#pragma unroll
+        for (int cc = 0; cc < kMergeRegs; ++cc)
+            if (cc < nchunks)
+                Mx = fmaxf(Mx, ml[cc].x);
+        if (Mx != -INFINITY) {
+#pragma unroll
+            for (int cc = 0; cc < kMergeRegs; ++cc)
+                if (cc < nchunks) {
+                    const float f = (ml[cc].x == -INFINITY) ? 0.f : exp2f(ml[cc].x - Mx);
+                    ls = fmaf(f, ml[cc].y, ls);
+                    r0 = fmaf(f, oc[cc].x, r0);
+                    r1 = fmaf(f, oc[cc].y, r1);
+                }
+        }
+    } else {
+        float Mx = -INFINITY;
+        for (int cc = 0; cc < nchunks; ++cc)
+            Mx = fmaxf(Mx, __ldcg(ml_row + cc).x);
+        if (Mx != -INFINITY) {
+            for (int cc = 0; cc < nchunks; ++cc) {
+                const float2 ml = __ldcg(ml_row + cc);
+                const float f = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - Mx);
+                const float2 oc = __ldcg(o_col + cc * (kD / 2));
+                ls = fmaf(f, ml.y, ls);
+                r0 = fmaf(f, oc.x, r0);
+                r1 = fmaf(f, oc.y, r1);
+            }
         }
     }
     out_row[dp] = finish_pair(r0, r1, ls);
