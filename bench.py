@@ -55,14 +55,16 @@ CONFIG_TEXT = {
              "page fill, lazy pages",
 }
 VARIANTS = {"default": 0, "simt": 1, "mma": 2}
-# Pages per work unit, chosen per workload from a sweep of 8..128 (any fixed value keeps
-# results batch invariant: the chunking depends only on each sequence's own length).
-DEFAULT_CHUNK = {"b256": 128, "b64": 32, "b8": 16, "trace": 32}
-DEFAULT_RING = {"b256": 4, "b64": 2, "b8": 2, "trace": 2}   # TMA stages per warp (grid schedule), from the same sweep
-# Largest-first unit dispatch (PKV_STEP_SORTED): measured +5 % on the ragged one-wave
-# layers (b64, b8), -3 % on b256 where every unit has the same size.
-DEFAULT_SORTED = {"b256": False, "b64": True, "b8": True, "trace": False}
-DEFAULT_RING_FP8 = {"b256": 3, "b64": 2, "b8": 2, "trace": 2}  # units of 2176 B per warp (FP8 pages), measured
+# Per-workload launch settings (pages per unit, ring depth, sorted dispatch, micro-batch
+# chains), chosen by measurement; the full-size parity tests run the same ones.
+from paged_kv_decode_12_gb300 import launch as LAUNCH  # noqa: E402  (no torch import)
+
+DEFAULT_CHUNK = {k: v for k, v in LAUNCH.CHUNK.items() if k != "tiny"}
+DEFAULT_RING = {k: v for k, v in LAUNCH.RING.items() if k != "tiny"}
+DEFAULT_SORTED = {k: v for k, v in LAUNCH.SORTED.items() if k != "tiny"}
+DEFAULT_RING_FP8 = {k: v for k, v in LAUNCH.RING_FP8.items() if k != "tiny"}
+DEFAULT_CHAINS = {k: v for k, v in LAUNCH.CHAINS.items() if k != "tiny"}
+DEFAULT_CHAINS_FP8 = {k: v for k, v in LAUNCH.CHAINS_FP8.items() if k != "tiny"}
 L2_BYTES = 129 * 10**6
 
 
@@ -176,7 +178,7 @@ def kernel_source_digest() -> str:
 
 
 def measured_traffic(config: str, path: str, variant_name: str, pages_per_chunk: int, ring: int,
-                     kv: str = "bf16"):
+                     kv: str = "bf16", chains: int = 1):
     """DRAM bytes per attention launch from the committed ncu summary
     (profiles/decode_traffic.json), if it was taken on the current kernel source;
     else None."""
@@ -189,7 +191,8 @@ def measured_traffic(config: str, path: str, variant_name: str, pages_per_chunk:
     for e in entries:
         if (e.get("config") == config and e.get("path") == path and e.get("variant") == variant_name and
                 e.get("pages_per_chunk") == pages_per_chunk and e.get("ring", 4) == ring and
-                e.get("kv", "bf16") == kv and e.get("kernel_source_sha") == digest):
+                e.get("kv", "bf16") == kv and e.get("chains", 1) == chains and
+                e.get("kernel_source_sha") == digest):
             return e.get("dram_bytes_per_launch")
     return None
 
@@ -271,6 +274,7 @@ def config_block(w, args, variant_name: str, graph: bool) -> dict:
             "schedule": getattr(args, "schedule", "auto"), "ring": getattr(args, "ring", 0),
             "early_trigger": getattr(args, "early_trigger", False),
             "sorted_units": getattr(args, "sorted", False),
+            "chains": getattr(args, "chains", 1),
             "kv_pages": getattr(args, "kv", "bf16"),
             "kv_bytes_per_step": kv,
             "l2": f"inputs larger than L2 ({kv / 1e9:.2f} GB of KV per step vs {L2_BYTES / 1e6:.0f} MB L2), "
@@ -331,11 +335,11 @@ def run_trace(args):
     reqs = wl.trace_schedule(seed=seed, steps=steps)
     # warm-up: a short trace on a small runner (kernel attributes, tensor maps)
     warm = TraceRunner(pool_pages=4096, layers=16, max_batch=8, seed=seed + 1,
-                       pages_per_chunk=args.pages_per_chunk, options=options, kv=args.kv)
+                       pages_per_chunk=args.pages_per_chunk, options=options, kv=args.kv, chains=args.chains)
     warm.run(wl.trace_schedule(seed=seed + 1, steps=max(args.warmup, 3), arrival_rate=2.0), max(args.warmup, 3))
     warm.close()
     runner = TraceRunner(pool_pages=pages, layers=16, max_batch=192, static=args.static, seed=seed,
-                         pages_per_chunk=args.pages_per_chunk, options=options, kv=args.kv)
+                         pages_per_chunk=args.pages_per_chunk, options=options, kv=args.kv, chains=args.chains)
     uuid = str(getattr(torch.cuda.get_device_properties(local), "uuid", "") or "")
     sampler = ClockSampler(uuid if uuid.startswith("GPU-") else (f"GPU-{uuid}" if uuid else str(local)))
     sampler.start()
@@ -354,7 +358,7 @@ def run_trace(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16" if args.kv == "bf16" else "fp8e4m3 KV, f16 MMA, f32 softmax", "data": "synthetic",
             "config": {"workload": f"trace: {CONFIG_TEXT['trace']}", "layers": 16, "pool_mib": args.pool_mib,
-                       "kv_pages": args.kv,
+                       "kv_pages": args.kv, "chains": args.chains,
                        "pages_per_chunk": args.pages_per_chunk, "ring": args.ring, "kernel_variant": args.variant,
                        "batching": "static" if args.static else "continuous", "requests": len(reqs),
                        "seed": args.seed, "l2": "KV per step far above L2 once the batch has grown; no flush"},
@@ -370,7 +374,7 @@ def run_trace(args):
                     "h2d_bytes_per_step": None, "d2h_bytes_per_step": 0,
                     "path": "TraceRunner.run: scheduler, prefill, table/length uploads, one sync per step"},
             "scheduler_stats": res.stats, "cpu_baseline": None,
-            "gpu_launches": res.decode_steps * 16 + res.stats["admitted"], "clocks": clocks}
+            "gpu_launches": res.launches, "clocks": clocks}
     if rank == 0:
         print(json.dumps(line), flush=True)
     runner.close()
@@ -396,7 +400,7 @@ def run_pkv(args):
     dw = harness.setup(args.config, replica_seed(args.seed, rank), args.pages_per_chunk, VARIANTS[variant_name],
                        layers=args.layers, fused=args.path == "fused", pdl=not args.no_pdl,
                        schedule=args.schedule, ring=args.ring, early_trigger=args.early_trigger, kv=args.kv,
-                       sorted_units=args.sorted)
+                       sorted_units=args.sorted, chains=args.chains)
     w = dw.w
     harness.warm(dw, 2)
     dw.reset_q()
@@ -457,25 +461,38 @@ def run_pkv(args):
     # dominant kernel: the attention launches (split + merge), timed inside the graphs
     split_ms = [s.elapsed_time(e) for cap in timed_ev for (s, e) in cap.split_events]
     kv_step = w.kv_bytes_per_step(args.kv)
-    kv_launch = kv_step // w.layers
+    launches = harness.kernels_per_step(dw)
+    kv_launch = kv_step // launches  # average over the layers (and the micro-batch chains)
     peak, peak_src = hbm_peak()
     steps_per_s = args.steps / (elapsed_ms / 1e3)
     value = kv_step * steps_per_s * world / 1e9
     roofline = None
     if split_ms:
         avg = sum(split_ms) / len(split_ms)
-        achieved = kv_launch / (avg / 1e3) / 1e9
+        alone = kv_launch / (avg / 1e3) / 1e9
+        timing = "external events around every launch in a second pass of the same steps"
+        eff_ms, achieved = avg, alone
+        if args.chains > 1:
+            # the chains' launches overlap on the GPU, and an event between two launches of
+            # one chain would serialise them: a launch's duration comes from the timed region
+            # (every launch in it is this kernel), the serialised per-launch figure is kept
+            eff_ms = (elapsed_ms / args.steps) * args.chains / launches
+            achieved = kv_launch / (eff_ms / 1e3) / 1e9
+            timing = ("micro-batch chains overlap their launches: duration per launch = step time x chains / "
+                      "launches per step, from the timed region (every launch in it is this kernel); "
+                      "launch_alone: " + timing + ", the chains one after another")
         roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                     "traffic": measured_traffic(args.config, args.path, variant_name, args.pages_per_chunk,
-                                                args.ring, args.kv),
+                                                args.ring, args.kv, args.chains),
                     "kernel": ("fused decode step kernel over FP8 pages (append + quantize + attention + merge)"
                                if args.kv == "fp8" else
                                f"fused decode step kernel (append + attention + merge), variant {variant_name}"
                                if args.path == "fused" else
                                f"paged decode attention launch (split + merge), variant {variant_name}"),
-                    "timing": "external events around every launch in a second pass of the same steps",
-                    "algorithmic_bytes_per_launch": kv_launch, "avg_launch_us": avg * 1e3,
+                    "timing": timing, "algorithmic_bytes_per_launch": kv_launch, "avg_launch_us": eff_ms * 1e3,
                     "launches_timed": len(split_ms), "peak_source": f"{peak_src} hbm_gbs (burst copy)"}
+        if args.chains > 1:
+            roofline["launch_alone"] = {"achieved": alone, "frac": alone / peak, "avg_launch_us": avg * 1e3}
 
     # end to end through the public API with pinned host buffers
     e2e = None
@@ -495,7 +512,7 @@ def run_pkv(args):
             "tokens_per_s": w.batch * steps_per_s * world,
             "attended_kv_tokens_per_s": float(w.seq_lens.sum()) * w.layers * steps_per_s * world,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": harness.kernels_per_step(dw) * args.steps, "clocks": clocks}
+            "gpu_launches": launches * args.steps, "clocks": clocks}
     if rank == 0:
         print(json.dumps(line), flush=True)
     dw.eng.close()
@@ -563,6 +580,11 @@ def main(argv=None):
                     help="fused path: one CTA per unit, or persistent CTAs walking the units")
     ap.add_argument("--ring", type=int, default=None, choices=[2, 3, 4],
                     help="grid schedule: TMA stages per warp (default: the measured best for the workload)")
+    ap.add_argument("--chains", type=int, default=None,
+                    help="fused path: micro-batch chains, each a per-layer launch chain over a contiguous row "
+                         "group on its own stream (default: per workload, BF16 "
+                         + ", ".join(f"{k} {v}" for k, v in DEFAULT_CHAINS.items()) + "; FP8 "
+                         + ", ".join(f"{k} {v}" for k, v in DEFAULT_CHAINS_FP8.items()) + ")")
     ap.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
                     help="KV page format: BF16 (the engine's) or FP8 E4M3 with per-row scales")
     ap.add_argument("--seed", type=int, default=12)
@@ -582,6 +604,11 @@ def main(argv=None):
         args.sorted = DEFAULT_SORTED[args.config] and not args.unsorted and args.schedule in ("auto", "grid")
     elif args.unsorted:
         raise SystemExit("--sorted and --unsorted exclude each other")
+    if args.chains is None:
+        args.chains = (1 if args.path != "fused" else
+                       (DEFAULT_CHAINS if args.kv == "bf16" else DEFAULT_CHAINS_FP8)[args.config])
+    elif args.chains > 1 and args.path != "fused":
+        raise SystemExit("--chains > 1 runs the fused path only")
     if args.impl == "reference":
         return run_reference(args)
     if args.config == "trace":

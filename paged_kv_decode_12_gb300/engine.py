@@ -10,6 +10,13 @@ every step of the computation runs in libpkv's kernels.
 
 ``run_host`` is the end-to-end form: inputs come from pinned host memory and
 the result goes back to it, with the copies on the same stream as the kernels.
+
+Micro-batch chains (``chains=K``, fused path): the batch rows are cut into K
+contiguous groups, each group runs its own chain of per-layer fused launches on
+its own stream (forked from and joined back to the caller's stream), so one
+group's layer tail overlaps another group's streaming.  Layer order is kept
+inside every group; sequences never interact, so every output byte is the same
+as with one chain.
 """
 from __future__ import annotations
 
@@ -30,9 +37,13 @@ class DecodeEngine:
                  pages_per_chunk: int = 16, variant: int = pkv.PKV_DECODE_DEFAULT, max_pos: int = wl.MAX_CONTEXT,
                  theta: float = wl.ROPE_THETA, pool_seed: int = 0, device: str = "cuda", fused: bool = True,
                  pdl: bool = True, schedule: str = "auto", ring: int = 0, early_trigger: bool = False,
-                 kv: str = "bf16", sorted_units: bool = False):
+                 kv: str = "bf16", sorted_units: bool = False, chains: int = 1):
         if kv not in ("bf16", "fp8"):
             raise ValueError(f"kv must be 'bf16' or 'fp8', not {kv!r}")
+        if not 1 <= chains <= batch:
+            raise ValueError(f"chains must be in [1, batch], not {chains}")
+        if chains > 1 and not fused:
+            raise ValueError("micro-batch chains run the fused step only")
         self.kv = kv
         self.device = torch.device(device)
         self.layers, self.batch, self.max_blocks = layers, batch, max_blocks
@@ -63,6 +74,12 @@ class DecodeEngine:
                              "options")
         self.bt = None
         self.bt_host = None
+        self.chains = chains
+        self.chain_bounds = chain_bounds(batch, chains)
+        # each chain has its own stream and its own step workspace (counters start at zero)
+        self.chain_streams = [torch.cuda.Stream(device=self.device) for _ in range(chains)] if chains > 1 else []
+        self.chain_ws = [torch.zeros(self.step_ws_bytes, dtype=torch.uint8, device=self.device)
+                         for _ in range(chains)] if chains > 1 else []
 
     # ------------------------------------------------------------------ setup
     def pool_view(self) -> torch.Tensor:
@@ -85,9 +102,11 @@ class DecodeEngine:
         return codes, scales
 
     def build_tables(self, seq_lens) -> np.ndarray:
-        """Allocate pages for every (layer, sequence) and upload the block tables."""
+        """Allocate pages for every (layer, sequence) and upload the block tables; the
+        micro-batch chains (if any) are cut to balance their pages."""
         bt = pkv.pkv_block_tables_build(self.pool, self.layers, seq_lens, self.max_blocks)
         self.set_tables(bt)
+        self.chain_bounds = chain_bounds(self.batch, self.chains, seq_lens)
         return bt
 
     def set_tables(self, bt_host: np.ndarray) -> None:
@@ -116,11 +135,45 @@ class DecodeEngine:
                                          self.scale, self.pages_per_chunk, self.workspace, self.ws_bytes, out,
                                          self.err, stream, self.variant if variant is None else variant)
 
-    def fused_layer(self, layer: int, q, k_new, v_new, seq_lens_dev, out, stream=None) -> None:
-        """Append + attention of one layer in one launch (positions are seq_lens - 1)."""
-        pkv.pkv_decode_step(self.pool, k_new, v_new, q, self.bt[layer], self.max_blocks, seq_lens_dev, self.batch,
-                            self.rope, self.max_pos, self.scale, self.pages_per_chunk, self.step_ws,
-                            self.step_ws_bytes, out, self.err, stream, self.step_options)
+    def fused_layer(self, layer: int, q, k_new, v_new, seq_lens_dev, out, stream=None, rows=None,
+                    workspace=None) -> None:
+        """Append + attention of one layer in one launch (positions are seq_lens - 1); with
+        ``rows=(r0, r1)`` for the batch rows r0..r1-1 only (contiguous slices of every argument)."""
+        r0, r1 = rows if rows is not None else (0, self.batch)
+        pkv.pkv_decode_step(self.pool, k_new[r0:r1], v_new[r0:r1], q[r0:r1], self.bt[layer, r0:r1], self.max_blocks,
+                            seq_lens_dev[r0:r1], r1 - r0, self.rope, self.max_pos, self.scale, self.pages_per_chunk,
+                            self.step_ws if workspace is None else workspace, self.step_ws_bytes, out[r0:r1],
+                            self.err, stream, self.step_options)
+
+    def _step_chains(self, q, k_new, v_new, seq_lens_dev, out, stream=None, layer_hook=None) -> None:
+        """The fused step as micro-batch chains.  Each chain waits for the caller's stream,
+        runs its layers on its own stream, and the caller's stream waits for every chain.
+        With a ``layer_hook`` the chains run one after another on the caller's stream
+        instead, so that the hook's events bracket one launch each."""
+        groups = list(zip(self.chain_bounds[:-1], self.chain_bounds[1:]))
+        if layer_hook is not None:
+            for k, rows in enumerate(groups):
+                for layer in range(self.layers):
+                    layer_hook(layer, "before")
+                    self.fused_layer(layer, q[layer], k_new[layer], v_new[layer], seq_lens_dev, out[layer], stream,
+                                     rows, self.chain_ws[k])
+                    layer_hook(layer, "after")
+            return
+        cur = torch.cuda.current_stream(self.device) if stream is None else stream
+        fork = torch.cuda.Event()
+        fork.record(cur)
+        joins = []
+        for k, rows in enumerate(groups):
+            s = self.chain_streams[k]
+            s.wait_event(fork)
+            for layer in range(self.layers):
+                self.fused_layer(layer, q[layer], k_new[layer], v_new[layer], seq_lens_dev, out[layer], s, rows,
+                                 self.chain_ws[k])
+            done = torch.cuda.Event()
+            done.record(s)
+            joins.append(done)
+        for done in joins:
+            cur.wait_event(done)
 
     def step(self, q, k_new, v_new, pos_dev, seq_lens_dev, out, stream=None, layer_hook=None) -> None:
         """One decode step over all layers.
@@ -131,6 +184,9 @@ class DecodeEngine:
         pkv_append_rope at pos_dev then pkv_decode_attention.
         ``layer_hook(layer, phase)`` (optional) is called around each attention launch.
         """
+        if self.fused and self.chains > 1:
+            self._step_chains(q, k_new, v_new, seq_lens_dev, out, stream, layer_hook)
+            return
         for layer in range(self.layers):
             if self.fused:
                 if layer_hook:
@@ -157,6 +213,29 @@ class DecodeEngine:
 
     def check_errors(self):
         return pkv.pkv_check_device_error(self.err)
+
+
+def chain_bounds(batch: int, chains: int, seq_lens=None) -> list:
+    """Row bounds [0 = r_0 < r_1 < ... < r_K = batch] of K contiguous micro-batch chains.
+    Without lengths the rows are split evenly; with them, r_k is the cut whose running page
+    count is nearest to k/K of the total (every chain keeps at least one row)."""
+    if not 1 <= chains <= batch:
+        raise ValueError(f"chains must be in [1, batch], not {chains}")
+    if seq_lens is None or chains == 1:
+        return [int(x) for x in np.linspace(0, batch, chains + 1).round().astype(int)]
+    pages = (np.asarray(seq_lens, dtype=np.int64).clip(min=0) + wl.PAGE_SIZE - 1) // wl.PAGE_SIZE
+    cum = np.cumsum(pages)
+    total = int(cum[-1]) if batch else 0
+    bounds = [0]
+    for k in range(1, chains):
+        target = total * k / chains
+        i = int(np.searchsorted(cum, target, side="left"))  # first row whose running count reaches it
+        r = i + 1 if i == 0 or abs(cum[min(i, batch - 1)] - target) <= abs(cum[i - 1] - target) else i
+        r = max(r, bounds[-1] + 1)          # at least one row per chain
+        r = min(r, batch - (chains - k))    # leave a row for every later chain
+        bounds.append(r)
+    bounds.append(batch)
+    return bounds
 
 
 class PackedIO:

@@ -38,17 +38,19 @@ class DeviceWorkload:
 def setup(name: str, seed: int = wl.DEFAULT_SEED, pages_per_chunk: int = 16,
           variant: int = pkv.PKV_DECODE_DEFAULT, layers: int | None = None, device: str = "cuda",
           fused: bool = True, pdl: bool = True, schedule: str = "auto", ring: int = 0,
-          early_trigger: bool = False, kv: str = "bf16", sorted_units: bool = False) -> DeviceWorkload:
+          early_trigger: bool = False, kv: str = "bf16", sorted_units: bool = False,
+          chains: int = 1) -> DeviceWorkload:
     """Build the named workload on the GPU: pool filled with N(0,1) BF16 (plus the
     key outliers of ``b64``) or, with ``kv="fp8"``, with FP8 pages drawn by
     ``workloads.fill_fp8_pages_``; block tables from the library's seeded
-    allocator, per-layer q / k_new / v_new draws, positions = lengths - 1."""
+    allocator, per-layer q / k_new / v_new draws, positions = lengths - 1.
+    ``chains`` > 1 runs the fused step as that many micro-batch chains (see engine)."""
     w = wl.make_workload(name, seed)
     if layers is not None and layers != w.layers:
         w = dataclasses.replace(w, layers=layers, pool_pages=w.pool_pages * layers // w.layers)
     eng = DecodeEngine(w.pool_pages, w.layers, w.batch, w.max_blocks, pages_per_chunk, variant, pool_seed=seed,
                        device=device, fused=fused, pdl=pdl, schedule=schedule, ring=ring,
-                       early_trigger=early_trigger, kv=kv, sorted_units=sorted_units)
+                       early_trigger=early_trigger, kv=kv, sorted_units=sorted_units, chains=chains)
     if kv == "fp8":
         codes, scales = eng.fp8_views()
         wl.fill_fp8_pages_(codes, scales, seed, w.key_outlier_frac)
@@ -76,10 +78,10 @@ def setup(name: str, seed: int = wl.DEFAULT_SEED, pages_per_chunk: int = 16,
 
 def kernels_per_step(dw: DeviceWorkload) -> int:
     """Library kernel launches in one step: per layer one fused kernel (BF16 or FP8
-    pages), or (separate path) the append, the split kernel and, when a sequence can
-    span several chunks, the merge."""
+    pages) per micro-batch chain, or (separate path) the append, the split kernel and,
+    when a sequence can span several chunks, the merge."""
     if dw.eng.fused:
-        return dw.w.layers
+        return dw.w.layers * dw.eng.chains
     merge = 1 if (dw.w.max_blocks + dw.eng.pages_per_chunk - 1) // dw.eng.pages_per_chunk > 1 else 0
     return dw.w.layers * (2 + merge)
 

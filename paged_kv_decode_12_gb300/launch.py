@@ -1,0 +1,34 @@
+"""Launch configuration of the fused decode step per workload and KV page format.
+
+These are the settings the benchmark times and the full-size parity tests run:
+pages per work unit, TMA ring depth per warp, largest-first unit dispatch and the
+number of micro-batch chains.  Each was chosen by measurement on GB300. The fixed
+chunking keeps results batch invariant, because it depends only on each sequence's
+own length. None of the settings changes a result bit.
+"""
+from __future__ import annotations
+
+# pages per work unit (swept over 8..128 per workload)
+CHUNK = {"tiny": 1, "b256": 128, "b64": 32, "b8": 16, "trace": 32}
+# TMA stages per warp on the grid schedule, BF16 pages (4 KiB each)
+RING = {"tiny": 2, "b256": 3, "b64": 2, "b8": 2, "trace": 2}
+# TMA stages per warp, FP8 pages (units of 2176 B)
+RING_FP8 = {"tiny": 2, "b256": 3, "b64": 2, "b8": 2, "trace": 2}
+# largest-first unit dispatch (PKV_STEP_SORTED): a gain on a ragged one-wave layer run as
+# one launch (b8); with micro-batch chains the grid order is faster (b64), and on b256
+# every unit has the same size
+SORTED = {"tiny": True, "b256": False, "b64": False, "b8": True, "trace": False}
+# micro-batch chains: independent per-layer launch chains over contiguous row groups,
+# each on its own stream, so that one group's layer tail overlaps another's streaming
+# (the trace launches eagerly from the host each step, where more launches cost more
+# than the overlap gains)
+CHAINS = {"tiny": 2, "b256": 2, "b64": 16, "b8": 1, "trace": 1}
+CHAINS_FP8 = {"tiny": 2, "b256": 2, "b64": 8, "b8": 1, "trace": 1}
+
+
+def config(name: str, kv: str = "bf16") -> dict:
+    """Keyword arguments of ``harness.setup`` for workload ``name`` with ``kv`` pages."""
+    if kv not in ("bf16", "fp8"):
+        raise ValueError(f"kv must be 'bf16' or 'fp8', not {kv!r}")
+    return {"pages_per_chunk": CHUNK[name], "ring": (RING if kv == "bf16" else RING_FP8)[name],
+            "sorted_units": SORTED[name], "chains": (CHAINS if kv == "bf16" else CHAINS_FP8)[name], "kv": kv}

@@ -36,13 +36,14 @@ class TraceResult:
     tokens: int                    # decode tokens produced (one per active sequence per step)
     batch_sizes: list
     stats: dict
+    launches: int = 0              # library kernel launches (decode steps of every layer and chain, prefills)
 
 
 class TraceRunner:
     def __init__(self, pool_pages: int, layers: int = 16, max_batch: int = 192, max_blocks: int = wl.MAX_BLOCKS,
                  max_context: int = wl.MAX_CONTEXT, static: bool = False, seed: int = wl.DEFAULT_SEED,
                  pages_per_chunk: int = 32, options: int = pkv.PKV_STEP_RING(2), device: str = "cuda",
-                 kv: str = "bf16"):
+                 kv: str = "bf16", chains: int = 1):
         self.device = torch.device(device)
         self.layers, self.max_batch, self.max_blocks, self.max_context = layers, max_batch, max_blocks, max_context
         self.pages_per_chunk, self.options, self.seed = pages_per_chunk, options, seed
@@ -62,6 +63,13 @@ class TraceRunner:
         self.err = torch.zeros(1, dtype=torch.int32, device=self.device)
         self.ws_bytes = pkv.pkv_decode_step_workspace_bytes(max_batch, max_blocks, pages_per_chunk)
         self.ws = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=self.device)
+        # micro-batch chains (see engine.chain_bounds): per chain a stream and a workspace
+        if chains < 1:
+            raise ValueError(f"chains must be >= 1, not {chains}")
+        self.chains = chains
+        self.chain_streams = [torch.cuda.Stream(device=self.device) for _ in range(chains)] if chains > 1 else []
+        self.chain_ws = [torch.zeros(self.ws_bytes, dtype=torch.uint8, device=self.device)
+                         for _ in range(chains)] if chains > 1 else []
 
         def draw(shape, s):
             return wl.fill_bf16_normal_(torch.empty(shape, dtype=torch.bfloat16, device=self.device), s)
@@ -77,6 +85,7 @@ class TraceRunner:
         self.bt = torch.full((layers, max_batch, max_blocks), -1, dtype=torch.int32, device=self.device)
         self.lens = torch.zeros(max_batch, dtype=torch.int32, device=self.device)
         self.prompt_bt = torch.full((layers, max_blocks), -1, dtype=torch.int32, device=self.device)
+        self.launches = 0
         self._prompt_seed = seed + 100
         self.prompt_seeds = {}  # request id -> (seed of its prompt K/V draw, prompt length)
 
@@ -106,13 +115,39 @@ class TraceRunner:
         k, v = self.prompt_kv(self._prompt_seed, prompt_len)
         pkv.pkv_prefill_append(self.pool, k, v, self.prompt_bt, self.max_blocks, self.layers, 0, prompt_len,
                                self.rope, self.max_context, self.err)
+        self.launches += 1
 
-    def decode(self, B: int):
+    def _layers(self, r0: int, r1: int, ws, stream=None):
+        self.launches += self.layers
         for layer in range(self.layers):
-            pkv.pkv_decode_step(self.pool, self.k_new[layer, :B], self.v_new[layer, :B], self.q[layer, :B],
-                                self.bt[layer, :B], self.max_blocks, self.lens, B, self.rope, self.max_context,
-                                self.scale, self.pages_per_chunk, self.ws, self.ws_bytes, self.out[layer, :B],
-                                self.err, None, self.options)
+            pkv.pkv_decode_step(self.pool, self.k_new[layer, r0:r1], self.v_new[layer, r0:r1],
+                                self.q[layer, r0:r1], self.bt[layer, r0:r1], self.max_blocks, self.lens[r0:r1],
+                                r1 - r0, self.rope, self.max_context, self.scale, self.pages_per_chunk, ws,
+                                self.ws_bytes, self.out[layer, r0:r1], self.err, stream, self.options)
+
+    def decode(self, B: int, lens_host=None):
+        """All layers of one decode step over the first B batch rows; with chains, as
+        micro-batch chains cut by the rows' page counts (``lens_host``)."""
+        k = min(self.chains, B)
+        if k <= 1:
+            self._layers(0, B, self.ws)
+            return
+        from .engine import chain_bounds
+
+        bounds = chain_bounds(B, k, lens_host)
+        cur = torch.cuda.current_stream(self.device)
+        fork = torch.cuda.Event()
+        fork.record(cur)
+        joins = []
+        for i in range(k):
+            s = self.chain_streams[i]
+            s.wait_event(fork)
+            self._layers(bounds[i], bounds[i + 1], self.chain_ws[i], s)
+            done = torch.cuda.Event()
+            done.record(s)
+            joins.append(done)
+        for done in joins:
+            cur.wait_event(done)
 
     # ------------------------------------------------------------------ trace
     def run(self, requests, steps: int, before_step=None, after_step=None) -> TraceResult:
@@ -122,6 +157,7 @@ class TraceRunner:
         for r in requests:
             by_step.setdefault(r.arrival_step, []).append(r)
         gpu_ms, kv_bytes, tokens, decode_steps, sizes = 0.0, 0, 0, 0, []
+        self.launches = 0
         per_token = wl.kv_bytes_per_token(self.layers, kv=self.kv)
         t0 = time.perf_counter()
         for step in range(steps):
@@ -146,7 +182,7 @@ class TraceRunner:
                 before_step(step, ids, lens, bt)
             start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             start.record()
-            self.decode(B)
+            self.decode(B, lens)
             end.record()
             if after_step:
                 after_step(step, ids, lens, bt)
@@ -158,4 +194,4 @@ class TraceRunner:
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
         return TraceResult(steps, decode_steps, gpu_ms, wall, kv_bytes, tokens, sizes,
-                           pkv.pkv_sched_get_stats(self.sched))
+                           pkv.pkv_sched_get_stats(self.sched), self.launches)

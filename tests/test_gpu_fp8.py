@@ -21,7 +21,7 @@ import pytest
 import torch
 
 import oracle
-from paged_kv_decode_12_gb300 import harness, pkv
+from paged_kv_decode_12_gb300 import harness, launch, pkv
 from paged_kv_decode_12_gb300 import workloads as wl
 from paged_kv_decode_12_gb300.engine import DecodeEngine
 from tests import paged_helpers as ph
@@ -304,7 +304,7 @@ def test_fp8_zero_length_sets_flag_and_zeros():
 
 @pytest.mark.parametrize("name", ["b64", "b256"])
 def test_fp8_full_size_sampled(name):
-    dw = harness.setup(name, pages_per_chunk=32 if name == "b64" else 128, kv="fp8")
+    dw = harness.setup(name, **launch.config(name, "fp8"))  # the benchmark's launch configuration
     harness.warm(dw, 1)
     dw.reset_q()
     cap = harness.capture_steps(dw, 1)

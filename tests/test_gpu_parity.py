@@ -16,7 +16,7 @@ import pytest
 import torch
 
 import oracle
-from paged_kv_decode_12_gb300 import harness, pkv
+from paged_kv_decode_12_gb300 import harness, launch, pkv
 from paged_kv_decode_12_gb300 import workloads as wl
 from paged_kv_decode_12_gb300.engine import DecodeEngine
 from tests import paged_helpers as ph
@@ -252,7 +252,7 @@ def test_append_position_out_of_range_sets_flag():
 
 @pytest.mark.parametrize("name", ["tiny", "b8", "b64", "b256"])
 def test_full_size_sampled(name):
-    dw = harness.setup(name)
+    dw = harness.setup(name, **launch.config(name))  # the benchmark's launch configuration
     harness.warm(dw, 1)
     dw.reset_q()
     cap = harness.capture_steps(dw, 1)

@@ -69,14 +69,15 @@ def test_prefill_fill_matches_oracle(start, T):
     pkv.pkv_pool_destroy(p)
 
 
-@pytest.mark.parametrize("kv", ["bf16", "fp8"])
-def test_trace_steps_match_oracle(kv):
+@pytest.mark.parametrize("kv,chains", [("bf16", 1), ("fp8", 1), ("bf16", 3)])
+def test_trace_steps_match_oracle(kv, chains):
     # The oracle rebuilds each sampled sequence's pages from the raw seeded inputs that
     # went into them -- the prompt K/V draw of its admission and the new K/V row of every
     # step since -- and decodes with the step's unrotated query; nothing the CUDA path
     # wrote is read back as an oracle input.
     layers, max_batch = 2, 24
-    runner = TraceRunner(pool_pages=3000, layers=layers, max_batch=max_batch, pages_per_chunk=4, seed=5, kv=kv)
+    runner = TraceRunner(pool_pages=3000, layers=layers, max_batch=max_batch, pages_per_chunk=4, seed=5, kv=kv,
+                         chains=chains)
     fp8 = kv == "fp8"
     reqs = wl.trace_schedule(seed=5, steps=60, arrival_rate=0.8, prompt_lo=8, prompt_hi=200, out_lo=4, out_hi=60)
     rng = np.random.default_rng(9)
