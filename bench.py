@@ -178,7 +178,7 @@ def kernel_source_digest() -> str:
 
 
 def measured_traffic(config: str, path: str, variant_name: str, pages_per_chunk: int, ring: int,
-                     kv: str = "bf16", chains: int = 1):
+                     kv: str = "bf16", chains: int = 1, sorted_units: bool = False):
     """DRAM bytes per attention launch from the committed ncu summary
     (profiles/decode_traffic.json), if it was taken on the current kernel source;
     else None."""
@@ -192,6 +192,7 @@ def measured_traffic(config: str, path: str, variant_name: str, pages_per_chunk:
         if (e.get("config") == config and e.get("path") == path and e.get("variant") == variant_name and
                 e.get("pages_per_chunk") == pages_per_chunk and e.get("ring", 4) == ring and
                 e.get("kv", "bf16") == kv and e.get("chains", 1) == chains and
+                e.get("sorted_units", False) == sorted_units and
                 e.get("kernel_source_sha") == digest):
             return e.get("dram_bytes_per_launch")
     return None
@@ -476,14 +477,14 @@ def run_pkv(args):
             # the chains' launches overlap on the GPU, and an event between two launches of
             # one chain would serialise them: a launch's duration comes from the timed region
             # (every launch in it is this kernel), the serialised per-launch figure is kept
-            eff_ms = (elapsed_ms / args.steps) * args.chains / launches
+            eff_ms = (elapsed_ms / args.steps) / launches
             achieved = kv_launch / (eff_ms / 1e3) / 1e9
-            timing = ("micro-batch chains overlap their launches: duration per launch = step time x chains / "
-                      "launches per step, from the timed region (every launch in it is this kernel); "
-                      "launch_alone: " + timing + ", the chains one after another")
+            timing = ("micro-batch chains overlap their launches: GPU time per launch = step time / launches per "
+                      "step, from the timed region (every launch in it is this kernel); launch_alone: "
+                      + timing + ", the chains one after another")
         roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                     "traffic": measured_traffic(args.config, args.path, variant_name, args.pages_per_chunk,
-                                                args.ring, args.kv, args.chains),
+                                                args.ring, args.kv, args.chains, args.sorted),
                     "kernel": ("fused decode step kernel over FP8 pages (append + quantize + attention + merge)"
                                if args.kv == "fp8" else
                                f"fused decode step kernel (append + attention + merge), variant {variant_name}"
