@@ -8,8 +8,10 @@ own length. None of the settings changes a result bit.
 """
 from __future__ import annotations
 
-# pages per work unit (swept over 8..128 per workload)
-CHUNK = {"tiny": 1, "b256": 128, "b64": 32, "b8": 16, "trace": 32}
+# pages per work unit (swept over 8..128 per workload; b64 together with its chains:
+# with 8 chains a launch holds 8 sequences, and 20-page units shorten each unit's
+# serial chain of page round trips)
+CHUNK = {"tiny": 1, "b256": 128, "b64": 20, "b8": 16, "trace": 32}
 # TMA stages per warp on the grid schedule, BF16 pages (4 KiB each)
 RING = {"tiny": 2, "b256": 3, "b64": 2, "b8": 2, "trace": 2}
 # TMA stages per warp, FP8 pages (units of 2176 B)
