@@ -1,0 +1,57 @@
+"""bench.py's argument resolution (CPU only): the per-workload launch settings it
+fills in are the ones in paged_kv_decode_12_gb300/launch.py, explicit flags win, and
+combinations the path does not run are refused before any GPU work."""
+import pytest
+
+import bench
+from paged_kv_decode_12_gb300 import launch
+
+
+@pytest.fixture
+def captured(monkeypatch):
+    seen = {}
+
+    def grab(name):
+        def run(args):
+            seen["arm"], seen["args"] = name, args
+            return 0
+        return run
+
+    monkeypatch.setattr(bench, "run_pkv", grab("pkv"))
+    monkeypatch.setattr(bench, "run_trace", grab("trace"))
+    monkeypatch.setattr(bench, "run_reference", grab("reference"))
+    return seen
+
+
+@pytest.mark.parametrize("config", ["b256", "b64", "b8"])
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_defaults_follow_launch_table(captured, config, kv):
+    assert bench.main(["--config", config, "--kv", kv]) == 0
+    a, want = captured["args"], launch.config(config, kv)
+    assert captured["arm"] == "pkv"
+    assert (a.pages_per_chunk, a.ring, a.sorted, a.chains) == \
+        (want["pages_per_chunk"], want["ring"], want["sorted_units"], want["chains"])
+
+
+def test_explicit_flags_win(captured):
+    bench.main(["--chains", "1", "--ring", "4", "--pages-per-chunk", "64", "--unsorted"])
+    a = captured["args"]
+    assert (a.chains, a.ring, a.pages_per_chunk, a.sorted) == (1, 4, 64, False)
+    bench.main(["--config", "b64", "--sorted"])
+    assert captured["args"].sorted is True
+
+
+def test_separate_path_runs_one_chain(captured):
+    bench.main(["--path", "separate"])
+    assert captured["args"].chains == 1
+    with pytest.raises(SystemExit):
+        bench.main(["--path", "separate", "--chains", "2"])
+    with pytest.raises(SystemExit):
+        bench.main(["--sorted", "--unsorted"])
+
+
+def test_trace_and_reference_arms(captured):
+    bench.main(["--config", "trace"])
+    assert captured["arm"] == "trace" and captured["args"].chains == launch.CHAINS["trace"]
+    bench.main(["--impl", "reference", "--config", "b64"])
+    assert captured["arm"] == "reference" and captured["args"].chains == launch.CHAINS["b64"]
