@@ -410,23 +410,22 @@ def run_pkv(args):
     per_graph = max(1, min(args.steps, args.steps_per_graph))
     warm_cap = harness.capture_steps(dw, max(1, min(args.warmup, per_graph)))
 
-    def capture_all(instrumented):
-        caps, left = [], args.steps
-        while left > 0:
-            n = min(per_graph, left)
-            caps.append(harness.capture_steps(dw, n, time_attention=instrumented))
-            left -= n
-        return caps
-
-    # the step time comes from plain graphs: a timing event between two launches
-    # would turn their programmatic (overlapping) dependency into a full one
-    timed = capture_all(False)
-    timed_ev = capture_all(True) if ext else []
+    # The timed steps replay one captured graph of per_graph steps (plus one graph for the
+    # remainder): a serving loop replays the same graph every step, and many distinct graph
+    # instances of thousands of nodes each (micro-batch chains) cost the device time to
+    # switch between.  The step time comes from these plain graphs: a timing event between
+    # two launches would turn their programmatic (overlapping) dependency into a full one.
+    n_full, rem = divmod(args.steps, per_graph)
+    timed = [harness.capture_steps(dw, per_graph)] * n_full
+    if rem:
+        timed.append(harness.capture_steps(dw, rem))
+    # per-launch durations: one instrumented graph of the same per_graph steps
+    timed_ev = [harness.capture_steps(dw, per_graph, time_attention=True)] if ext else []
     torch.cuda.synchronize()
 
     # every timed graph is launched once before the timed region: the first launch of an
-    # instantiated graph also uploads it to the device (thousands of nodes with many chains)
-    for cap in timed:
+    # instantiated graph also uploads it to the device
+    for cap in {id(c): c for c in timed}.values():
         cap.graph.replay()
     torch.cuda.synchronize()
     # warm-up: W steps
@@ -456,7 +455,7 @@ def run_pkv(args):
         torch.distributed.barrier()
     clocks = sampler.stop(t0, t1)
     elapsed_ms = reduce_max(start.elapsed_time(end), world, device)
-    # second pass, same steps: per-launch durations of the attention kernel
+    # second pass, per_graph more steps: per-launch durations of the attention kernel
     for cap in timed_ev:
         cap.graph.replay()
     torch.cuda.synchronize()
@@ -477,7 +476,7 @@ def run_pkv(args):
     if split_ms:
         avg = sum(split_ms) / len(split_ms)
         alone = kv_launch / (avg / 1e3) / 1e9
-        timing = "external events around every launch in a second pass of the same steps"
+        timing = f"external events around every launch in a second pass of {per_graph} steps"
         eff_ms, achieved = avg, alone
         if args.chains > 1:
             # the chains' launches overlap on the GPU, and an event between two launches of

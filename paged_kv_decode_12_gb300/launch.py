@@ -22,10 +22,9 @@ RING_FP8 = {"tiny": 2, "b256": 3, "b64": 2, "b8": 2, "trace": 2}
 SORTED = {"tiny": True, "b256": False, "b64": False, "b8": True, "trace": False}
 # micro-batch chains: independent per-layer launch chains over contiguous row groups,
 # each on its own stream, so that one group's layer tail overlaps another's streaming.
-# Every chain adds a launch per layer: past 8 chains on b64 the host's graph launches
-# (cost grows with the node count) no longer stay ahead of the GPU, and the trace
-# launches eagerly from the host each step, where more launches cost more than the
-# overlap gains
+# Every chain adds a launch per layer: past 8 chains b64 gains nothing in multi-step
+# graphs and loses at one step per graph, and the trace launches eagerly from the host
+# each step, where more launches cost more than the overlap gains
 CHAINS = {"tiny": 2, "b256": 2, "b64": 8, "b8": 1, "trace": 1}
 CHAINS_FP8 = {"tiny": 2, "b256": 2, "b64": 8, "b8": 1, "trace": 1}
 
