@@ -181,7 +181,8 @@ class DecodeEngine:
         q: [layers][B][32][64] bf16 (rotated in place), k_new, v_new: [layers][B][8][64] bf16,
         pos_dev, seq_lens_dev: [B] int32, out: [layers][B][32][64] bf16.  The fused path
         (default) appends at seq_lens - 1 and ignores pos_dev; the separate path launches
-        pkv_append_rope at pos_dev then pkv_decode_attention.
+        pkv_append_rope at pos_dev then pkv_decode_attention.  ``stream`` is a
+        torch.cuda.Stream or None (the current stream).
         ``layer_hook(layer, phase)`` (optional) is called around each attention launch.
         """
         if self.fused and self.chains > 1:
