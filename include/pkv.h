@@ -364,6 +364,28 @@ int pkv_decode_step(const pkv_pool *pool, const uint16_t *k_new, const uint16_t 
                     const float *rope_table, int max_pos, float scale, int pages_per_chunk, void *workspace,
                     size_t workspace_bytes, uint16_t *out, int32_t *dev_err_flag, void *cuda_stream, int options);
 
+/* Every layer of one decode step: pkv_decode_step for layer l = 0 .. layers-1, in
+ * that order, on the one stream.  The pages put each layer of the model after the
+ * previous one; in the samir-vllm README summary the decode loop runs the layers in
+ * turn, and this call keeps that order.  It exists so that a host loop issues one call
+ * per step instead of one per layer (the per-call host work is the same as
+ * pkv_decode_step's, done here in native code).
+ *   Layer l's arguments are the given base pointers plus l times a layer stride, in
+ *   elements: k_new and v_new + l * kv_layer_stride (BF16 elements), q and out +
+ *   l * q_layer_stride (BF16 elements), bt_dev + l * bt_layer_stride (int32
+ *   entries).  A stride of 0 reuses the same array for every layer.  seq_lens_dev,
+ *   rope_table, workspace, dev_err_flag, options and the stream are shared by all
+ *   layers; the layers run one after another, so sharing the workspace is allowed.
+ *   Layouts, ownership, validation and device checks are pkv_decode_step's.
+ * Errors: layers < 1 or a negative stride -> PKV_ERR_INVALID_ARG before anything is
+ * launched.  Otherwise the first failing layer's status is returned and no later
+ * layer is launched.  Earlier layers have then been launched and run. */
+int pkv_decode_step_layers(const pkv_pool *pool, int layers, const uint16_t *k_new, const uint16_t *v_new,
+                           uint16_t *q, const int32_t *bt_dev, int max_blocks, const int32_t *seq_lens_dev, int B,
+                           const float *rope_table, int max_pos, float scale, int pages_per_chunk, void *workspace,
+                           size_t workspace_bytes, uint16_t *out, int32_t *dev_err_flag, void *cuda_stream,
+                           int options, int64_t kv_layer_stride, int64_t q_layer_stride, int64_t bt_layer_stride);
+
 /* Size of the library's static scratch used by pkv_decode_attention_noalloc. */
 #define PKV_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20) /* 32 MiB */
 

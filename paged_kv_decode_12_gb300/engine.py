@@ -145,6 +145,23 @@ class DecodeEngine:
                             self.step_ws if workspace is None else workspace, self.step_ws_bytes, out[r0:r1],
                             self.err, stream, self.step_options)
 
+    def fused_layers(self, q, k_new, v_new, seq_lens_dev, out, stream=None, rows=None, workspace=None) -> None:
+        """Every layer's fused launch for batch rows ``rows`` (default: all) in one library
+        call (``pkv_decode_step_layers``): q, k_new, v_new, out are [layers][B][...] with
+        contiguous rows; a layer's arrays are the layer-0 rows plus the tensors' layer stride."""
+        r0, r1 = rows if rows is not None else (0, self.batch)
+        ws = self.step_ws if workspace is None else workspace
+        if k_new.stride(0) != v_new.stride(0) or q.stride(0) != out.stride(0):
+            for layer in range(self.layers):  # layer strides the one call cannot express
+                self.fused_layer(layer, q[layer], k_new[layer], v_new[layer], seq_lens_dev, out[layer], stream,
+                                 rows, ws)
+            return
+        pkv.pkv_decode_step_layers(self.pool, self.layers, k_new[0, r0:r1], v_new[0, r0:r1], q[0, r0:r1],
+                                   self.bt[0, r0:r1], self.max_blocks, seq_lens_dev[r0:r1], r1 - r0, self.rope,
+                                   self.max_pos, self.scale, self.pages_per_chunk, ws, self.step_ws_bytes,
+                                   out[0, r0:r1], self.err, stream, self.step_options, k_new.stride(0),
+                                   q.stride(0), self.bt.stride(0))
+
     def _step_chains(self, q, k_new, v_new, seq_lens_dev, out, stream=None, layer_hook=None) -> None:
         """The fused step as micro-batch chains.  Each chain waits for the caller's stream,
         runs its layers on its own stream, and the caller's stream waits for every chain.
@@ -166,9 +183,7 @@ class DecodeEngine:
         for k, rows in enumerate(groups):
             s = self.chain_streams[k]
             s.wait_event(fork)
-            for layer in range(self.layers):
-                self.fused_layer(layer, q[layer], k_new[layer], v_new[layer], seq_lens_dev, out[layer], s, rows,
-                                 self.chain_ws[k])
+            self.fused_layers(q, k_new, v_new, seq_lens_dev, out, s, rows, self.chain_ws[k])
             done = torch.cuda.Event()
             done.record(s)
             joins.append(done)
@@ -187,6 +202,9 @@ class DecodeEngine:
         """
         if self.fused and self.chains > 1:
             self._step_chains(q, k_new, v_new, seq_lens_dev, out, stream, layer_hook)
+            return
+        if self.fused and layer_hook is None:
+            self.fused_layers(q, k_new, v_new, seq_lens_dev, out, stream)
             return
         for layer in range(self.layers):
             if self.fused:

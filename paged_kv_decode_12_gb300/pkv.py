@@ -58,7 +58,7 @@ EXPORTED = (
     "pkv_pool_create", "pkv_pool_destroy", "pkv_pool_alloc", "pkv_pool_free", "pkv_pool_info",
     "pkv_block_tables_build", "pkv_rope_table_init", "pkv_append_rope", "pkv_decode_workspace_bytes",
     "pkv_decode_attention", "pkv_decode_attention_variant", "pkv_decode_attention_noalloc",
-    "pkv_decode_step_workspace_bytes", "pkv_decode_step", "pkv_check_device_error",
+    "pkv_decode_step_workspace_bytes", "pkv_decode_step", "pkv_decode_step_layers", "pkv_check_device_error",
     "pkv_status_string", "pkv_version",
 )
 
@@ -104,6 +104,9 @@ def lib():
     L.pkv_decode_step_workspace_bytes.restype = ctypes.c_size_t
     L.pkv_decode_step.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _vp, _i32, ctypes.c_float, _i32, _vp,
                                   ctypes.c_size_t, _vp, _vp, _vp, _i32]
+    L.pkv_decode_step_layers.argtypes = [_vp, _i32, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _vp, _i32, ctypes.c_float,
+                                         _i32, _vp, ctypes.c_size_t, _vp, _vp, _vp, _i32, ctypes.c_int64,
+                                         ctypes.c_int64, ctypes.c_int64]
     L.pkv_check_device_error.argtypes = [_vp, _i32p, _vp]
     L.pkv_status_string.argtypes = [_i32]
     L.pkv_status_string.restype = ctypes.c_char_p
@@ -255,6 +258,19 @@ def pkv_decode_step(pool, k_new, v_new, q, bt_dev, max_blocks: int, seq_lens_dev
                                  _ptr(seq_lens_dev), B, _ptr(rope_table), max_pos, float(scale), pages_per_chunk,
                                  _ptr(workspace), int(workspace_bytes), _ptr(out), _ptr(dev_err_flag),
                                  _stream(stream), int(options)), "pkv_decode_step")
+
+
+def pkv_decode_step_layers(pool, layers: int, k_new, v_new, q, bt_dev, max_blocks: int, seq_lens_dev, B: int,
+                           rope_table, max_pos: int, scale: float, pages_per_chunk: int, workspace,
+                           workspace_bytes: int, out, dev_err_flag=None, stream=None,
+                           options: int = PKV_DECODE_DEFAULT, kv_layer_stride: int = 0, q_layer_stride: int = 0,
+                           bt_layer_stride: int = 0) -> None:
+    """pkv_decode_step for every layer in one call; strides in elements (see include/pkv.h)."""
+    _check(lib().pkv_decode_step_layers(pool, int(layers), _ptr(k_new), _ptr(v_new), _ptr(q), _ptr(bt_dev),
+                                        max_blocks, _ptr(seq_lens_dev), B, _ptr(rope_table), max_pos, float(scale),
+                                        pages_per_chunk, _ptr(workspace), int(workspace_bytes), _ptr(out),
+                                        _ptr(dev_err_flag), _stream(stream), int(options), int(kv_layer_stride),
+                                        int(q_layer_stride), int(bt_layer_stride)), "pkv_decode_step_layers")
 
 
 PKV_NOALLOC_SCRATCH_BYTES = 32 << 20

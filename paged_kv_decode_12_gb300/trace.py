@@ -86,6 +86,15 @@ class TraceRunner:
         self.lens = torch.zeros(max_batch, dtype=torch.int32, device=self.device)
         self.prompt_bt = torch.full((layers, max_blocks), -1, dtype=torch.int32, device=self.device)
         self.launches = 0
+        # every decode call gets its arguments as addresses computed from these bases and row
+        # strides (no tensor views per call: the trace launches from the host every step)
+        kv_row, q_row = wl.NUM_KV_HEADS * wl.HEAD_DIM * 2, wl.NUM_Q_HEADS * wl.HEAD_DIM * 2
+        self._base = dict(k=self.k_new.data_ptr(), v=self.v_new.data_ptr(), q=self.q.data_ptr(),
+                          bt=self.bt.data_ptr(), lens=self.lens.data_ptr(), out=self.out.data_ptr(),
+                          rope=self.rope.data_ptr(), err=self.err.data_ptr())
+        self._stride = dict(kv=kv_row, q=q_row, bt=max_blocks * 4)
+        self._fork = torch.cuda.Event() if chains > 1 else None
+        self._joins = [torch.cuda.Event() for _ in range(chains)] if chains > 1 else []
         self._prompt_seed = seed + 100
         self.prompt_seeds = {}  # request id -> (seed of its prompt K/V draw, prompt length)
 
@@ -118,12 +127,19 @@ class TraceRunner:
         self.launches += 1
 
     def _layers(self, r0: int, r1: int, ws, stream=None):
+        """Every layer of one decode step for batch rows r0..r1-1 (contiguous slices of the
+        per-layer [max_batch] arrays, passed as addresses)."""
         self.launches += self.layers
-        for layer in range(self.layers):
-            pkv.pkv_decode_step(self.pool, self.k_new[layer, r0:r1], self.v_new[layer, r0:r1],
-                                self.q[layer, r0:r1], self.bt[layer, r0:r1], self.max_blocks, self.lens[r0:r1],
-                                r1 - r0, self.rope, self.max_context, self.scale, self.pages_per_chunk, ws,
-                                self.ws_bytes, self.out[layer, r0:r1], self.err, stream, self.options)
+        a, st = self._base, self._stride
+        ws_ptr, lens = ws.data_ptr(), a["lens"] + 4 * r0
+        stream = torch.cuda.current_stream(self.device).cuda_stream if stream is None else stream.cuda_stream
+        # one library call for all layers: layer l's rows are r0.. of layer l's [max_batch] arrays
+        pkv.pkv_decode_step_layers(self.pool, self.layers, a["k"] + r0 * st["kv"], a["v"] + r0 * st["kv"],
+                                   a["q"] + r0 * st["q"], a["bt"] + r0 * st["bt"], self.max_blocks, lens, r1 - r0,
+                                   a["rope"], self.max_context, self.scale, self.pages_per_chunk, ws_ptr,
+                                   self.ws_bytes, a["out"] + r0 * st["q"], a["err"], stream, self.options,
+                                   self.max_batch * st["kv"] // 2, self.max_batch * st["q"] // 2,
+                                   self.max_batch * st["bt"] // 4)
 
     def decode(self, B: int, lens_host=None):
         """All layers of one decode step over the first B batch rows; with chains, as
@@ -136,18 +152,14 @@ class TraceRunner:
 
         bounds = chain_bounds(B, k, lens_host)
         cur = torch.cuda.current_stream(self.device)
-        fork = torch.cuda.Event()
-        fork.record(cur)
-        joins = []
+        self._fork.record(cur)
         for i in range(k):
             s = self.chain_streams[i]
-            s.wait_event(fork)
+            s.wait_event(self._fork)
             self._layers(bounds[i], bounds[i + 1], self.chain_ws[i], s)
-            done = torch.cuda.Event()
-            done.record(s)
-            joins.append(done)
-        for done in joins:
-            cur.wait_event(done)
+            self._joins[i].record(s)
+        for i in range(k):
+            cur.wait_event(self._joins[i])
 
     # ------------------------------------------------------------------ trace
     def run(self, requests, steps: int, before_step=None, after_step=None) -> TraceResult:

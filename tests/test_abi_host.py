@@ -229,3 +229,25 @@ def test_grid_schedule_options_validation_before_any_cuda_call():
                                 dummy, None, 0, options=opt)
         assert e.value.status == pkv.PKV_ERR_INVALID_ARG, (B, hex(opt))
     pkv.pkv_pool_destroy(p)
+
+
+def test_step_layers_validation_before_any_cuda_call():
+    p = make_pool(8)
+    dummy = FAKE_SLAB
+    ws = pkv.pkv_decode_step_workspace_bytes(4, 128, 16)
+    args = (dummy, dummy, dummy, dummy, 128, dummy, 4, dummy, 2048, 0.125, 16, dummy, ws, dummy, None, 0)
+    bad = [dict(layers=0), dict(layers=2, kv_layer_stride=-512), dict(layers=2, q_layer_stride=-1),
+           dict(layers=2, bt_layer_stride=-128), dict(layers=2, kv_layer_stride=3),   # 6-byte layer step
+           dict(layers=2, q_layer_stride=4100)]
+    for kw in bad:
+        layers = kw.pop("layers")
+        with pytest.raises(pkv.PkvError) as e:
+            pkv.pkv_decode_step_layers(p, layers, *args, **kw)
+        assert e.value.status == pkv.PKV_ERR_INVALID_ARG, kw
+    # layer 0 is validated as pkv_decode_step validates it: a bad batch launches nothing
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.pkv_decode_step_layers(p, 16, dummy, dummy, dummy, dummy, 128, dummy, 0, dummy, 2048, 0.125, 16, dummy,
+                                   ws, dummy, None, 0, kv_layer_stride=4 * 512, q_layer_stride=4 * 2048,
+                                   bt_layer_stride=4 * 128)
+    assert e.value.status == pkv.PKV_ERR_INVALID_ARG
+    pkv.pkv_pool_destroy(p)

@@ -169,3 +169,27 @@ def test_run_host_equals_device_step():
     assert np.array_equal(u16(out_host), ref)
     assert io.bytes == sum(t.numel() * t.element_size() for t in (dw.q0, dw.k_new, dw.v_new, dw.pos, dw.seq_lens))
     dw.eng.close()
+
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_step_layers_call_matches_per_layer_calls(kv):
+    # pkv_decode_step_layers (one call for every layer, the engine's step) against one
+    # pkv_decode_step call per layer on the same inputs: every byte equal
+    from paged_kv_decode_12_gb300 import harness
+
+    res = []
+    for per_layer in (False, True):
+        dw = harness.setup("b8", layers=4, pages_per_chunk=16, ring=2, kv=kv)
+        dw.reset_q()
+        if per_layer:
+            for layer in range(dw.w.layers):
+                dw.eng.fused_layer(layer, dw.q[layer], dw.k_new[layer], dw.v_new[layer], dw.seq_lens, dw.out[layer])
+        else:
+            dw.step()
+        torch.cuda.synchronize()
+        st, flag = dw.eng.check_errors()
+        assert st == pkv.PKV_OK and flag == 0
+        res.append((dw.out.cpu().clone(), dw.q.cpu().clone(), dw.eng.slab.cpu().clone()))
+        dw.eng.close()
+    for a, b in zip(*res):
+        assert torch.equal(a, b)
