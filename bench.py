@@ -528,22 +528,22 @@ def run_pkv(args):
 
 
 def measure_e2e(dw, args, world, device):
-    """Same metric through DecodeEngine.run_host: every step copies q, k_new, v_new,
-    positions and lengths (packed, one copy) from pinned host memory and the output back,
-    on the stream."""
+    """Same metric through DecodeEngine.run_host_steps: every step copies q, k_new, v_new,
+    positions and lengths (packed, one copy) from pinned host memory and its output back,
+    double-buffered so that the copies of the neighbouring steps overlap the step's compute."""
     import torch
 
     from paged_kv_decode_12_gb300 import harness
 
     io = harness.host_pinned_inputs(dw)
     out_host = torch.empty(dw.out.shape, dtype=dw.out.dtype).pin_memory()
-    n = max(1, min(args.steps, args.e2e_steps))
-    for _ in range(2):
-        dw.eng.run_host(io, dw.out, out_host)
+    outs = (dw.out, torch.empty_like(dw.out))
+    n = max(2, min(args.steps, args.e2e_steps))
+    dw.eng.run_host_steps(io, outs, out_host, 2)
+    torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
-        for _ in range(n):
-            dw.eng.run_host(io, dw.out, out_host)
+        dw.eng.run_host_steps(io, outs, out_host, n)
     g.replay()
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -556,8 +556,9 @@ def measure_e2e(dw, args, world, device):
     d2h = out_host.numel() * out_host.element_size()
     return {"value": dw.w.kv_bytes_per_step(dw.eng.kv) * n * world / (ms / 1e3) / 1e9, "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n, "ms_per_step": ms / n,
-            "path": "DecodeEngine.run_host (packed pinned host inputs: one H2D copy, one D2H copy of the output, "
-                    "on the kernels' stream, CUDA graph)"}
+            "path": "DecodeEngine.run_host_steps (per step: one H2D copy of the packed pinned inputs and one D2H "
+                    "copy of the output, double-buffered on two copy streams so that they overlap the "
+                    "neighbouring steps' compute; CUDA graph)"}
 
 
 def main(argv=None):

@@ -230,6 +230,52 @@ class DecodeEngine:
         self.step(d["q"], d["k_new"], d["v_new"], d["pos"], d["seq_lens"], out_dev, stream)
         out_host.copy_(out_dev, non_blocking=True)
 
+    def run_host_steps(self, io: "PackedIO", out_devs, out_host, steps: int, stream=None) -> None:
+        """``steps`` end-to-end steps, each with its own copy of the inputs from pinned host
+        memory and its own copy of the output back, double-buffered: step s reads device
+        input buffer s % 2 and writes ``out_devs[s % 2]``.  Host-to-device copies run on one
+        copy stream and device-to-host copies on another, so that step s+1's inputs arrive
+        and step s-1's output leaves while step s computes.  A buffer is refilled only after
+        the step that used it has finished, and an output buffer is rewritten only after its
+        copy to the host has finished.  ``out_host`` receives the outputs in step order and
+        ends holding the last step's."""
+        cur = torch.cuda.current_stream(self.device) if stream is None else stream
+        if not hasattr(self, "_h2d"):
+            self._h2d, self._d2h = torch.cuda.Stream(device=self.device), torch.cuda.Stream(device=self.device)
+        devs = (io.d, io.second())
+        raws = (io.dev, io.dev2)
+        start = torch.cuda.Event()
+        start.record(cur)
+        self._h2d.wait_event(start)
+        self._d2h.wait_event(start)
+        ready = [torch.cuda.Event() for _ in range(steps)]
+        done = [torch.cuda.Event() for _ in range(steps)]
+        sent = [torch.cuda.Event() for _ in range(steps)]
+
+        def upload(s):
+            if s >= 2:
+                self._h2d.wait_event(done[s - 2])      # the step that last read this buffer
+            with torch.cuda.stream(self._h2d):
+                raws[s % 2].copy_(io.host, non_blocking=True)
+            ready[s].record(self._h2d)
+
+        upload(0)
+        for s in range(steps):
+            if s + 1 < steps:
+                upload(s + 1)
+            cur.wait_event(ready[s])
+            if s >= 2:
+                cur.wait_event(sent[s - 2])            # this output buffer has left for the host
+            d = devs[s % 2]
+            self.step(d["q"], d["k_new"], d["v_new"], d["pos"], d["seq_lens"], out_devs[s % 2], cur)
+            done[s].record(cur)
+            self._d2h.wait_event(done[s])
+            with torch.cuda.stream(self._d2h):
+                out_host.copy_(out_devs[s % 2], non_blocking=True)
+            sent[s].record(self._d2h)
+        cur.wait_event(sent[steps - 1])
+        cur.wait_event(ready[steps - 1])
+
     def check_errors(self):
         return pkv.pkv_check_device_error(self.err)
 
@@ -269,11 +315,22 @@ class PackedIO:
             off += (t.numel() * t.element_size() + 255) // 256 * 256
         self.host = torch.empty(off, dtype=torch.uint8).pin_memory()
         self.dev = torch.empty(off, dtype=torch.uint8, device=device)
+        self.dev2 = None
         self.bytes = sum(t.numel() * t.element_size() for t in tensors.values())
+        self._layout = {name: (offsets[name], t.numel() * t.element_size(), t.dtype, t.shape)
+                        for name, t in tensors.items()}
         self.h, self.d = {}, {}
-        for name, t in tensors.items():
-            n = t.numel() * t.element_size()
-            o = offsets[name]
-            self.h[name] = self.host[o:o + n].view(t.dtype).view(t.shape)
-            self.d[name] = self.dev[o:o + n].view(t.dtype).view(t.shape)
-            self.h[name].copy_(t.cpu())
+        for name, (o, n, dtype, shape) in self._layout.items():
+            self.h[name] = self.host[o:o + n].view(dtype).view(shape)
+            self.d[name] = self.dev[o:o + n].view(dtype).view(shape)
+            self.h[name].copy_(tensors[name].cpu())
+        self.d2 = None
+
+    def second(self) -> dict:
+        """Views of a second device buffer of the same layout (allocated on first use),
+        for double-buffered steps."""
+        if self.dev2 is None:
+            self.dev2 = torch.empty_like(self.dev)
+            self.d2 = {name: self.dev2[o:o + n].view(dtype).view(shape)
+                       for name, (o, n, dtype, shape) in self._layout.items()}
+        return self.d2

@@ -193,3 +193,40 @@ def test_step_layers_call_matches_per_layer_calls(kv):
         dw.eng.close()
     for a, b in zip(*res):
         assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("chains", [1, 2])
+def test_run_host_steps_double_buffered(chains):
+    # the double-buffered end-to-end steps compute what the plain step computes: every
+    # step's output reaches the host, and the last one stays there
+    from paged_kv_decode_12_gb300 import harness
+
+    dw = harness.setup("tiny", pages_per_chunk=1, ring=2, chains=chains)
+    pool0 = dw.eng.slab.clone()
+    dw.step()
+    torch.cuda.synchronize()
+    ref = u16(dw.out)
+    io = harness.host_pinned_inputs(dw)
+    out_host = torch.empty(dw.out.shape, dtype=dw.out.dtype).pin_memory()
+    outs = (dw.out, torch.empty_like(dw.out))
+    for steps in (1, 2, 5):
+        dw.eng.slab.copy_(pool0)
+        out_host.zero_()
+        for o in outs:
+            o.zero_()
+        dw.eng.run_host_steps(io, outs, out_host, steps)
+        torch.cuda.synchronize()
+        assert np.array_equal(u16(out_host), ref), steps
+        if steps >= 2:
+            assert np.array_equal(u16(outs[0]), ref) and np.array_equal(u16(outs[1]), ref)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        dw.eng.run_host_steps(io, outs, out_host, 3)
+    dw.eng.slab.copy_(pool0)
+    out_host.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(u16(out_host), ref)
+    st, flag = dw.eng.check_errors()
+    assert st == pkv.PKV_OK and flag == 0
+    dw.eng.close()
