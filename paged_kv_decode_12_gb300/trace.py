@@ -169,6 +169,7 @@ class TraceRunner:
         for r in requests:
             by_step.setdefault(r.arrival_step, []).append(r)
         gpu_ms, kv_bytes, tokens, decode_steps, sizes = 0.0, 0, 0, 0, []
+        timed = []
         self.launches = 0
         per_token = wl.kv_bytes_per_token(self.layers, kv=self.kv)
         t0 = time.perf_counter()
@@ -198,12 +199,14 @@ class TraceRunner:
             end.record()
             if after_step:
                 after_step(step, ids, lens, bt)
-            end.synchronize()
-            gpu_ms += start.elapsed_time(end)
+            # the events are read after the trace: the host schedules the next step while
+            # this one runs (every device-side use of a buffer is ordered on the stream)
+            timed.append((start, end))
             kv_bytes += int(lens.astype(np.int64).sum()) * per_token
             tokens += B
             decode_steps += 1
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
+        gpu_ms = sum(a.elapsed_time(b) for a, b in timed)
         return TraceResult(steps, decode_steps, gpu_ms, wall, kv_bytes, tokens, sizes,
                            pkv.pkv_sched_get_stats(self.sched), self.launches)
