@@ -320,8 +320,8 @@ def run_trace(args):
     """The continuous-batching trace: the scheduler admits by page budget, prompts are
     filled into pages, and every step runs the fused decode step of all layers on the
     live batch.  value = KV bytes attended / summed device time of the decode steps;
-    e2e = the same bytes / wall-clock time of the whole trace (scheduling, prefill,
-    uploads and a host synchronisation per step included)."""
+    e2e = the same bytes / wall-clock time of the whole trace (scheduling, prefill and
+    uploads included; the host schedules step s+1 while step s runs)."""
     import torch
 
     from paged_kv_decode_12_gb300 import pkv, workloads as wl
@@ -374,7 +374,7 @@ def run_trace(args):
                          "peak_source": f"{peak_src} hbm_gbs (burst copy)"},
             "e2e": {"value": res.kv_bytes * world / wall_s / 1e9, "unit": "GB/s",
                     "h2d_bytes_per_step": None, "d2h_bytes_per_step": 0,
-                    "path": "TraceRunner.run: scheduler, prefill, table/length uploads, one sync per step"},
+                    "path": "TraceRunner.run: scheduler, prefill, table/length uploads; the host schedules the next step while the GPU runs the current one"},
             "scheduler_stats": res.stats, "cpu_baseline": None,
             "gpu_launches": res.launches, "clocks": clocks}
     if rank == 0:
