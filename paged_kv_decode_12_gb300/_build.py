@@ -19,7 +19,8 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libpkv.so")
 BUILD_DIR = os.path.join(ROOT, "_build")
 
-SOURCES = ["pkv_host.cpp", "pkv_sched.cpp", "pkv_append.cu", "pkv_decode.cu", "pkv_step.cu", "pkv_fp8.cu"]
+SOURCES = ["pkv_host.cpp", "pkv_sched.cpp", "pkv_layers.cpp", "pkv_append.cu", "pkv_decode.cu", "pkv_step.cu",
+           "pkv_fp8.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
