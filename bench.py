@@ -272,9 +272,8 @@ def config_block(w, args, variant_name: str, graph: bool) -> dict:
             "seq_len_max": int(w.seq_lens.max()), "seq_len_mean": float(w.seq_lens.mean()),
             "pages_per_chunk": args.pages_per_chunk, "kernel_variant": variant_name, "cuda_graph": graph,
             "path": getattr(args, "path", "fused"), "pdl": not getattr(args, "no_pdl", False),
-            "schedule": getattr(args, "schedule", "auto"), "ring": getattr(args, "ring", 0),
-            "early_trigger": getattr(args, "early_trigger", False),
-            "sorted_units": getattr(args, "sorted", False),
+            "ring": getattr(args, "ring", 0), "sorted_units": getattr(args, "sorted", False),
+            "split_merge": getattr(args, "split_merge", False),
             "chains": getattr(args, "chains", 1),
             "steps_per_graph": getattr(args, "steps_per_graph", None) if graph else None,
             "kv_pages": getattr(args, "kv", "bf16"),
@@ -400,9 +399,8 @@ def run_pkv(args):
 
     variant_name = args.variant
     dw = harness.setup(args.config, replica_seed(args.seed, rank), args.pages_per_chunk, VARIANTS[variant_name],
-                       layers=args.layers, fused=args.path == "fused", pdl=not args.no_pdl,
-                       schedule=args.schedule, ring=args.ring, early_trigger=args.early_trigger, kv=args.kv,
-                       sorted_units=args.sorted, chains=args.chains)
+                       layers=args.layers, fused=args.path == "fused", pdl=not args.no_pdl, ring=args.ring,
+                       kv=args.kv, sorted_units=args.sorted, chains=args.chains, split_merge=args.split_merge)
     w = dw.w
     harness.warm(dw, 2)
     dw.reset_q()
@@ -467,7 +465,7 @@ def run_pkv(args):
     # dominant kernel: the attention launches (split + merge), timed inside the graphs
     split_ms = [s.elapsed_time(e) for cap in timed_ev for (s, e) in cap.split_events]
     kv_step = w.kv_bytes_per_step(args.kv)
-    launches = harness.kernels_per_step(dw)
+    launches = harness.attention_launches_per_step(dw)
     kv_launch = kv_step // launches  # average over the layers (and the micro-batch chains)
     peak, peak_src = hbm_peak()
     steps_per_s = args.steps / (elapsed_ms / 1e3)
@@ -518,7 +516,7 @@ def run_pkv(args):
             "tokens_per_s": w.batch * steps_per_s * world,
             "attended_kv_tokens_per_s": float(w.seq_lens.sum()) * w.layers * steps_per_s * world,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": launches * args.steps, "clocks": clocks}
+            "gpu_launches": harness.kernels_per_step(dw) * args.steps, "clocks": clocks}
     if rank == 0:
         print(json.dumps(line), flush=True)
     dw.eng.close()
@@ -573,18 +571,16 @@ def main(argv=None):
                          + ", ".join(f"{k} {v}" for k, v in DEFAULT_CHUNK.items()) + ")")
     ap.add_argument("--variant", choices=sorted(VARIANTS), default="default")
     ap.add_argument("--path", choices=["fused", "separate"], default="fused",
-                    help="one fused kernel per layer, or append + split + merge launches")
+                    help="one fused kernel per layer, or pkv_append_rope + pkv_decode_attention launches")
+    ap.add_argument("--split-merge", action="store_true",
+                    help="separate path: the two-kernel attention form (split kernel + LSE merge kernel)")
     ap.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
-    ap.add_argument("--early-trigger", action="store_true",
-                    help="let the next layer's launch begin once a CTA has issued its page copies")
     ap.add_argument("--sorted", action="store_true", default=None,
                     help="grid schedule: dispatch work units largest first (PKV_STEP_SORTED; default: per workload, "
                          + ", ".join(f"{k} {v}" for k, v in DEFAULT_SORTED.items()) + ")")
     ap.add_argument("--unsorted", action="store_true", help="grid schedule: dispatch units in grid order")
     ap.add_argument("--pool-mib", type=int, default=16384, help="trace: KV pool size (the engine's default is 128)")
     ap.add_argument("--static", action="store_true", help="trace: static batching instead of continuous")
-    ap.add_argument("--schedule", choices=["auto", "grid", "persistent", "ws"], default="auto",
-                    help="fused path: one CTA per unit, or persistent CTAs walking the units")
     ap.add_argument("--ring", type=int, default=None, choices=[2, 3, 4],
                     help="grid schedule: TMA stages per warp (default: the measured best for the workload)")
     ap.add_argument("--chains", type=int, default=None,
@@ -608,14 +604,13 @@ def main(argv=None):
     if args.ring is None:
         args.ring = DEFAULT_RING[args.config] if args.kv == "bf16" else DEFAULT_RING_FP8[args.config]
     if args.sorted is None:
-        args.sorted = DEFAULT_SORTED[args.config] and not args.unsorted and args.schedule in ("auto", "grid")
+        args.sorted = DEFAULT_SORTED[args.config] and not args.unsorted and not args.split_merge
     elif args.unsorted:
         raise SystemExit("--sorted and --unsorted exclude each other")
+    if args.split_merge and args.path != "separate":
+        raise SystemExit("--split-merge selects the separate path's two-kernel attention (--path separate)")
     if args.chains is None:
-        args.chains = (1 if args.path != "fused" else
-                       (DEFAULT_CHAINS if args.kv == "bf16" else DEFAULT_CHAINS_FP8)[args.config])
-    elif args.chains > 1 and args.path != "fused":
-        raise SystemExit("--chains > 1 runs the fused path only")
+        args.chains = (DEFAULT_CHAINS if args.kv == "bf16" else DEFAULT_CHAINS_FP8)[args.config]
     if args.impl == "reference":
         return run_reference(args)
     if args.config == "trace":

@@ -195,8 +195,12 @@ int pkv_append_rope(const pkv_pool *pool, const uint16_t *k_new, const uint16_t 
 
 /* ---------------------------------------------------------------- decode */
 
-/* Bytes of device workspace pkv_decode_attention needs for B sequences, a
- * table width of max_blocks and pages_per_chunk pages per work unit. */
+/* Bytes of device workspace pkv_decode_attention (and pkv_decode_step) needs for
+ * B sequences, a table width of max_blocks and pages_per_chunk pages per work
+ * unit: per-(sequence, KV head) merge counters [B][8] int32, then the chunk
+ * partials (m, l) [B][32][chunks] and o [B][32][chunks][64] FP32, chunks =
+ * ceil(max_blocks / pages_per_chunk), each region 256-byte aligned.  0 for
+ * arguments below 1. */
 size_t pkv_decode_workspace_bytes(int B, int max_blocks, int pages_per_chunk);
 
 /* Paged decode attention for one layer (samir-vllm README summary, "目前已完成
@@ -211,12 +215,27 @@ size_t pkv_decode_workspace_bytes(int B, int max_blocks, int pages_per_chunk);
  * Work split: a sequence's pages are cut into chunks of pages_per_chunk pages
  * (1..128); one CTA handles one (sequence, KV head, chunk) and serves all 4
  * query heads of the group from a single read of each page; chunk partials
- * (running max, sum, unnormalised output in FP32) are merged by log-sum-exp.
+ * (running max, sum, unnormalised output in FP32) are merged by log-sum-exp in
+ * chunk order, inside the same launch: the CTA that finishes a (sequence, KV
+ * head) last merges it.
  * The chunking depends only on each sequence's own length and pages_per_chunk,
  * never on B, so a sequence's result is bit-identical alone or in any batch.
  *   workspace  device buffer of at least pkv_decode_workspace_bytes(...) bytes,
- *              16-byte aligned; contents need no initialisation
+ *              16-byte aligned (may be NULL when every sequence fits one chunk,
+ *              i.e. max_blocks <= pages_per_chunk).  Its counter region (the
+ *              first B*8 int32) must be zero before the FIRST call -- e.g. one
+ *              cudaMemset after allocating; every call leaves it zero again.
+ *              Calls sharing a workspace must not overlap on the GPU.
  *   scale      1/sqrt(64) = 0.125 for the engine
+ * Launch: programmatic dependent launch.  Before its dependency wait a CTA reads
+ * only seq_lens, bt_dev and the cached pages holding no position at or beyond
+ * seq_len - 2; q, the two last positions' pages and every output come after it.
+ * So the kernel immediately before this call on the stream may write q (e.g. a
+ * projection) and positions seq_len - 1 and seq_len - 2 (the append of this step,
+ * pkv_append_rope at pos = seq_len - 1, or of the previous step), but must not
+ * write seq_lens, bt_dev or any earlier position of these sequences' pages.  A
+ * pkv_prefill_append on the same pool makes the next decode launch on the pool go
+ * without programmatic dependent launch.
  * Device checks: seq_len outside [1, 16*max_blocks] or a page id outside the
  * pool sets the flag; the affected (sequence, head) outputs are zeros. */
 int pkv_decode_attention(const pkv_pool *pool, const uint16_t *q, const int32_t *bt_dev, int max_blocks,
@@ -224,8 +243,20 @@ int pkv_decode_attention(const pkv_pool *pool, const uint16_t *q, const int32_t 
                          void *workspace, size_t workspace_bytes, uint16_t *out, int32_t *dev_err_flag,
                          void *cuda_stream);
 
-/* As pkv_decode_attention, with the split kernel chosen explicitly
- * (PKV_DECODE_DEFAULT, PKV_DECODE_SIMT or PKV_DECODE_MMA). */
+/* The two-kernel form of pkv_decode_attention (option bit of
+ * pkv_decode_attention_variant): the split kernel writes every chunk's partial to
+ * the workspace and a second small kernel merges them by log-sum-exp.  Launched
+ * without programmatic dependent launch; the workspace needs no initialisation
+ * (its counter region is not used).  Results are bit-identical to the default
+ * form's: the merge does the same arithmetic in the same chunk order. */
+#define PKV_DECODE_SPLIT_MERGE 0x80000
+
+/* As pkv_decode_attention, with the page policy chosen explicitly in the low byte
+ * of `variant` (PKV_DECODE_DEFAULT, PKV_DECODE_SIMT or PKV_DECODE_MMA), OR-ed with
+ * launch options: PKV_STEP_NO_PDL, PKV_STEP_RING(n), PKV_STEP_SORTED and
+ * PKV_STEP_TEST_EXPIRE_WAIT as for pkv_decode_step, or PKV_DECODE_SPLIT_MERGE alone
+ * (the two-kernel form; no other option with it).  None of the options changes a
+ * result bit.  Unknown bits: PKV_ERR_INVALID_ARG. */
 int pkv_decode_attention_variant(const pkv_pool *pool, const uint16_t *q, const int32_t *bt_dev,
                                  int max_blocks, const int32_t *seq_lens_dev, int B, float scale,
                                  int pages_per_chunk, void *workspace, size_t workspace_bytes, uint16_t *out,
@@ -296,37 +327,39 @@ int pkv_sched_get_stats(const pkv_sched *sched, pkv_sched_stats *out);
  * 的功能": prefill fills the prompt's pages; decode appends at the absolute RoPE
  * position).  k, v: [layers][T][8][64] BF16; bt_rows: device [layers][max_blocks]
  * (this sequence's table in every layer).  Device checks: a position beyond the
- * table or max_pos, or a page id outside the pool, sets the flag and skips it. */
+ * table or max_pos, or a page id outside the pool, sets the flag and skips it.
+ * The next pkv_decode_step / pkv_decode_attention launch on this pool goes without
+ * programmatic dependent launch, because it may read these pages. */
 int pkv_prefill_append(const pkv_pool *pool, const uint16_t *k, const uint16_t *v, const int32_t *bt_rows,
                        int max_blocks, int layers, int start_pos, int T, const float *rope_table, int max_pos,
                        int32_t *dev_err_flag, void *cuda_stream);
 
 /* ------------------------------------------------------ fused decode step */
 
-/* option bits for pkv_decode_step */
-#define PKV_STEP_NO_PDL 0x100     /* launch without programmatic dependent launch */
-#define PKV_STEP_GRID 0x200       /* one CTA per (sequence, KV head, chunk) */
-#define PKV_STEP_PERSISTENT 0x400 /* a few CTAs per SM walk the units (B <= 512) */
-#define PKV_STEP_WS 0x800         /* warp-specialised: a producer warp streams, 4 consumer warps compute (B <= 512) */
-/* grid schedule: TMA ring depth per warp, 2..4 stages of 4 KiB (0 = library default).
+/* option bits for pkv_decode_step (and pkv_decode_attention_variant) */
+#define PKV_STEP_NO_PDL 0x100 /* launch without programmatic dependent launch */
+#define PKV_STEP_GRID 0x200   /* one CTA per (sequence, KV head, chunk): the only schedule, accepted for clarity */
+/* TMA ring depth per warp, 2..4 stages (0 = library default: 3 for pages_per_chunk
+ * >= 64, else 2).  A stage is 4 KiB for BF16 pages, one 2176-byte unit for FP8 pages.
  * Fewer stages mean less shared memory per CTA and more CTAs resident per SM. */
 #define PKV_STEP_RING(n) ((n) << 12)
 #define PKV_STEP_RING_MASK 0xf000
-/* grid schedule: let the next launch begin as soon as a CTA has issued its page
- * copies, instead of after it has consumed them (helps layers that fit in one
- * wave of CTAs; can slow launches of several waves) */
-#define PKV_STEP_EARLY_TRIGGER 0x10000
-/* Grid schedule: dispatch the work units largest first (page count, then sequence,
- * chunk, KV head) instead of in (KV head, sequence, chunk) order.  The block scheduler
- * places CTAs in index order wherever there is room, so the largest units start first
- * and small ones fill the gaps, which balances the SMs when a ragged batch fits in one
- * wave.  Which CTA computes which unit is all that changes: results are identical.
- * B <= 1024; not with PKV_STEP_PERSISTENT / PKV_STEP_WS (PKV_ERR_INVALID_ARG). */
+/* Dispatch the work units largest first (page count, then sequence, chunk, KV head)
+ * instead of in (KV head, sequence, chunk) order.  The block scheduler places CTAs in
+ * index order wherever there is room, so the largest units start first and small ones
+ * fill the gaps, which balances the SMs when a ragged batch fits in one wave.  Which
+ * CTA computes which unit is all that changes: results are identical.  B <= 1024
+ * (PKV_ERR_INVALID_ARG beyond). */
 #define PKV_STEP_SORTED 0x20000
+/* Testing aid for the bounded waits: the first wait for a page copy in every work unit
+ * of sequence 0 gives up without polling, as a wait that ran out of its iteration
+ * limit does.  The unit then waits (bounded) for its copies in flight -- they are
+ * copies of valid pages, so they land -- sets PKV_DEVERR_TIMEOUT in the error flag and
+ * finishes: sequence 0's outputs are undefined, every other sequence's are computed as
+ * usual, and the merge counters are left at zero.  No copy stalls and nothing faults. */
+#define PKV_STEP_TEST_EXPIRE_WAIT 0x40000
 
-/* Bytes of device workspace pkv_decode_step needs (a per-(sequence, KV head)
- * counter array and two work-distribution counters, followed by the chunk
- * partials). */
+/* Bytes of device workspace pkv_decode_step needs: pkv_decode_workspace_bytes. */
 size_t pkv_decode_step_workspace_bytes(int B, int max_blocks, int pages_per_chunk);
 
 /* One layer of the decode step in ONE kernel launch: pkv_append_rope with
@@ -342,23 +375,22 @@ size_t pkv_decode_step_workspace_bytes(int B, int max_blocks, int pages_per_chun
  *              Its counter region must be zero before the FIRST call (e.g. one
  *              cudaMemset after allocating); every call leaves it zero again.
  *              Calls sharing a workspace must not overlap on the GPU.
- *   options    PKV_DECODE_DEFAULT / _SIMT / _MMA, optionally | PKV_STEP_NO_PDL, and
- *              a schedule: PKV_STEP_GRID (one CTA per unit) or PKV_STEP_PERSISTENT
- *              (SMs x CTAs-per-SM CTAs walk a device-built list of the non-empty
- *              units, prefetching across unit boundaries; B <= 512).  Neither:
- *              grid.  Results are identical.
- * Launch: programmatic dependent launch (unless PKV_STEP_NO_PDL).  Before its
- * dependency wait a CTA reads only seq_lens and bt_dev and starts copying this
- * layer's cached pages; the caller must therefore not have an immediately
- * preceding kernel on the stream write those three (block tables of different
- * layers must not share pages -- pkv_block_tables_build never does).
+ *   options    PKV_DECODE_DEFAULT / _SIMT / _MMA, optionally | PKV_STEP_NO_PDL,
+ *              PKV_STEP_RING(n), PKV_STEP_SORTED, PKV_STEP_TEST_EXPIRE_WAIT.
+ *              None of them changes a result bit.
+ * Launch: programmatic dependent launch (unless PKV_STEP_NO_PDL), with the
+ * contract of pkv_decode_attention: before its dependency wait a CTA reads only
+ * seq_lens, bt_dev and the cached pages holding no position at or beyond
+ * seq_len - 2, and it lets the next launch begin only after its own wait.  So the
+ * previous step of the same layer may be the immediately preceding kernel (a
+ * one-layer model: it wrote position seq_len - 2), but that kernel must not write
+ * seq_lens, bt_dev or earlier positions.  The first decode launch on a pool after
+ * a pkv_prefill_append on it goes without programmatic dependent launch.
  * Device checks as pkv_decode_attention, plus seq_len > max_pos.
- * FP8 pools: the same single launch on the grid schedule (options PKV_STEP_RING,
- * PKV_STEP_EARLY_TRIGGER, PKV_STEP_SORTED and PKV_STEP_NO_PDL apply; a ring stage is
- * one 2176-byte unit): the new token's rotated key row and value row are quantized
- * as pkv_append_rope quantizes them, and results are bit-identical to the separate
- * calls.  PKV_STEP_PERSISTENT / PKV_STEP_WS and the SIMT variant return
- * PKV_ERR_UNSUPPORTED. */
+ * FP8 pools: the same single launch (a ring stage is one 2176-byte unit): the new
+ * token's rotated key row and value row are quantized as pkv_append_rope quantizes
+ * them, and results are bit-identical to the separate calls.  The SIMT variant
+ * returns PKV_ERR_UNSUPPORTED. */
 int pkv_decode_step(const pkv_pool *pool, const uint16_t *k_new, const uint16_t *v_new, uint16_t *q,
                     const int32_t *bt_dev, int max_blocks, const int32_t *seq_lens_dev, int B,
                     const float *rope_table, int max_pos, float scale, int pages_per_chunk, void *workspace,
@@ -397,8 +429,9 @@ int pkv_decode_step_layers(const pkv_pool *pool, int layers, const uint16_t *k_n
  * with no device allocator of its own.  The chunk partials go to a static
  * device array of PKV_NOALLOC_SCRATCH_BYTES inside the library, which every GPU
  * that loads the library holds until the process exits.
- *   Arguments, layouts and results are those of pkv_decode_attention (the same
- *   kernels run); the caller still passes every input and the output.
+ *   Arguments, layouts and results are those of pkv_decode_attention; it runs the
+ *   two-kernel form (PKV_DECODE_SPLIT_MERGE), whose results are bit-identical to
+ *   the default form's.  The caller still passes every input and the output.
  *   Limit: a problem whose pkv_decode_workspace_bytes(B, max_blocks,
  *   pages_per_chunk) exceeds PKV_NOALLOC_SCRATCH_BYTES is rejected with
  *   PKV_ERR_WORKSPACE_TOO_SMALL before anything is launched (for example batch

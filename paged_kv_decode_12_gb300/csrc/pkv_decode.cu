@@ -197,12 +197,9 @@ int launch_split(const CUtensorMap *tmap, const SplitArgs &a, int B, cudaStream_
 {
     auto kernel = decode_split_kernel<Warp, kStages>;
     constexpr int smem = split_smem_bytes<kStages>();
-    static bool attr_set = false;  // set once per process (before any graph capture)
-    if (!attr_set) {
-        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-            return PKV_ERR_CUDA;
-        attr_set = true;
-    }
+    static PerDeviceOnce attr;  // set on the first launch per device (before any graph capture)
+    if (const int st = ensure_smem_attr(attr, kernel, smem); st != PKV_OK)
+        return st;
     dim3 grid(a.max_chunks, kHkv, B);
     kernel<<<grid, kThreads, smem, s>>>(*tmap, a);
     return status_from_cuda(cudaGetLastError());
@@ -226,9 +223,9 @@ extern "C" size_t pkv_decode_workspace_bytes(int B, int max_blocks, int pages_pe
     if (B < 1 || max_blocks < 1 || pages_per_chunk < 1)
         return 0;
     const size_t chunks = (size_t)(max_blocks + pages_per_chunk - 1) / pages_per_chunk;
-    const size_t ml = (size_t)B * kHq * chunks * sizeof(float2);
-    const size_t o = (size_t)B * kHq * chunks * kD * sizeof(float);
-    return ((ml + 255) & ~size_t(255)) + o;
+    if (chunks > (size_t)INT32_MAX)
+        return 0;
+    return workspace_layout(B, (int)chunks).total();
 }
 
 extern "C" int pkv_decode_attention_variant(const pkv_pool *pool, const uint16_t *q, const int32_t *bt_dev,
@@ -243,9 +240,10 @@ extern "C" int pkv_decode_attention_variant(const pkv_pool *pool, const uint16_t
         return PKV_ERR_INVALID_ARG;
     if (pages_per_chunk < 1 || pages_per_chunk > kMaxPagesPerChunk || !(scale > 0.f) || !std::isfinite(scale))
         return PKV_ERR_INVALID_ARG;
-    if (variant < PKV_DECODE_DEFAULT || variant > PKV_DECODE_MMA)
+    const int policy = variant & 0xff;
+    if (policy < PKV_DECODE_DEFAULT || policy > PKV_DECODE_MMA)
         return PKV_ERR_INVALID_ARG;
-    if (pool->kv_format == PKV_KV_FP8 && variant == PKV_DECODE_SIMT)
+    if (pool->kv_format == PKV_KV_FP8 && policy == PKV_DECODE_SIMT)
         return PKV_ERR_UNSUPPORTED;  // FP8 pages have the MMA policy only
     if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out)) & 15u)
         return PKV_ERR_INVALID_ARG;
@@ -257,9 +255,19 @@ extern "C" int pkv_decode_attention_variant(const pkv_pool *pool, const uint16_t
         if (workspace_bytes < need)
             return PKV_ERR_WORKSPACE_TOO_SMALL;
     }
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    if (!(variant & PKV_DECODE_SPLIT_MERGE))
+        return launch_attention_fused(pool, q, bt_dev, max_blocks, seq_lens_dev, B, scale, pages_per_chunk,
+                                      workspace, out, dev_err_flag, s, variant);
+    // the two-kernel form: split kernel, then the separate LSE merge kernel
+    if (variant & ~(0xff | PKV_DECODE_SPLIT_MERGE))
+        return PKV_ERR_INVALID_ARG;
     const CUtensorMap *tmap = pool_tensor_map(pool);
     if (!tmap)
         return PKV_ERR_CUDA;
+    (void)take_pdl_permission(pool, false);  // this form launches without programmatic dependent launch
+    const WorkspaceLayout ws = workspace_layout(B, max_chunks);
+    char *wsp = static_cast<char *>(workspace);
     SplitArgs a;
     a.num_pages = pool->num_pages;
     a.q = q;
@@ -268,14 +276,12 @@ extern "C" int pkv_decode_attention_variant(const pkv_pool *pool, const uint16_t
     a.seq_lens = seq_lens_dev;
     a.scale_log2 = scale * kLog2e;
     a.pages_per_chunk = pages_per_chunk;
-    const size_t ml_bytes = ((size_t)B * kHq * max_chunks * sizeof(float2) + 255) & ~size_t(255);
-    a.part_ml = static_cast<float2 *>(workspace);
-    a.part_o = workspace ? reinterpret_cast<float *>(static_cast<char *>(workspace) + ml_bytes) : nullptr;
+    a.part_ml = wsp ? reinterpret_cast<float2 *>(wsp + ws.ml_offset()) : nullptr;
+    a.part_o = wsp ? reinterpret_cast<float *>(wsp + ws.o_offset()) : nullptr;
     a.max_chunks = max_chunks;
     a.out = out;
     a.err = dev_err_flag;
-    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
-    const int v = variant == PKV_DECODE_DEFAULT ? PKV_DECODE_MMA : variant;
+    const int v = policy == PKV_DECODE_DEFAULT ? PKV_DECODE_MMA : policy;
     int st;
     if (pool->kv_format == PKV_KV_FP8) {
         st = fp8_decode_split(pool, q, bt_dev, max_blocks, seq_lens_dev, B, a.scale_log2, pages_per_chunk,
@@ -320,29 +326,29 @@ static __device__ __align__(256) unsigned char pkv_noalloc_scratch[PKV_NOALLOC_S
 
 namespace {
 
-constexpr int kNoAllocMaxDevices = 64;
+// Device address of the static scratch on the current device, looked up on the first
+// call per device.  A failed lookup is not remembered: a later call (for example one
+// made outside a stream capture) tries again.
+void *g_noalloc_address[pkv::kMaxDevices];
+pkv::PerDeviceOnce g_noalloc_lookup;
 
-struct NoAllocScratchSlot {
-    std::once_flag once;
-    void *ptr = nullptr;
-    cudaError_t err = cudaSuccess;
-};
-
-NoAllocScratchSlot g_noalloc_slots[kNoAllocMaxDevices];
-
-// Device address of the static scratch on the current device (looked up once).
 int noalloc_scratch_address(void **out)
 {
     int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices)
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= pkv::kMaxDevices)
         return PKV_ERR_CUDA;
-    NoAllocScratchSlot &slot = g_noalloc_slots[dev];
-    std::call_once(slot.once, [&slot] {
-        slot.err = cudaGetSymbolAddress(&slot.ptr, pkv_noalloc_scratch);
+    const int st = g_noalloc_lookup.run([](int d) {
+        void *p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, pkv_noalloc_scratch);
+        if (e == cudaSuccess && p == nullptr)
+            return cudaErrorInvalidSymbol;
+        if (e == cudaSuccess)
+            g_noalloc_address[d] = p;
+        return e;
     });
-    if (slot.err != cudaSuccess || slot.ptr == nullptr)
-        return PKV_ERR_CUDA;
-    *out = slot.ptr;
+    if (st != PKV_OK)
+        return st;
+    *out = g_noalloc_address[dev];
     return PKV_OK;
 }
 
@@ -364,9 +370,10 @@ extern "C" int pkv_decode_attention_noalloc(const pkv_pool *pool, const uint16_t
     const int st = noalloc_scratch_address(&scratch);
     if (st != PKV_OK)
         return st;
-    // The partials of every chunk are written by the split kernel before the merge
-    // reads them, so nothing left in the array by an earlier call is ever read and
-    // nothing needs clearing.
-    return pkv_decode_attention(pool, q, bt_dev, max_blocks, seq_lens_dev, B, scale, pages_per_chunk, scratch,
-                                PKV_NOALLOC_SCRATCH_BYTES, out, dev_err_flag, cuda_stream);
+    // The two-kernel form: the partials of every chunk are written by the split kernel
+    // before the merge kernel reads them, so nothing left in the array by an earlier
+    // call is ever read and nothing needs to start at zero.
+    return pkv_decode_attention_variant(pool, q, bt_dev, max_blocks, seq_lens_dev, B, scale, pages_per_chunk,
+                                        scratch, PKV_NOALLOC_SCRATCH_BYTES, out, dev_err_flag, cuda_stream,
+                                        PKV_DECODE_DEFAULT | PKV_DECODE_SPLIT_MERGE);
 }

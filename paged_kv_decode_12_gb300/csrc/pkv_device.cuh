@@ -65,10 +65,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
-// Warp-uniform bounded wait: true once every lane has observed the phase.
-__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity)
+// Warp-uniform bounded wait: true once every lane has observed the phase; false
+// after `limit` polls.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, uint32_t limit = kWaitLimit)
 {
-    for (uint32_t i = 0; i < kWaitLimit; ++i)
+    for (uint32_t i = 0; i < limit; ++i)
         if (__all_sync(kFull, mbar_try_wait(bar, parity)))
             return true;
     return false;
@@ -470,20 +471,40 @@ __device__ __forceinline__ void init_warp_barriers(uint64_t *my_bars, int lane)
     __syncwarp();
 }
 
-// Issue the first min(STAGES, nmine) (page, KV head) copies of this warp.  Lane k
-// of the warp holds the physical id of the warp's k-th page in `my_page`.
+// Issue the (page, KV head) copies k0 .. k1-1 of this warp into ring stages k0 ..
+// k1-1 (k1 <= STAGES).  Lane k of the warp holds the physical id of the warp's k-th
+// page in `my_page`; k0 and k1 are warp-uniform.
 template <int STAGES>
-__device__ __forceinline__ void issue_prologue(const CUtensorMap *tmap, uint8_t *my_stages, uint64_t *my_bars,
-                                               int my_page, int nmine, int g, int lane, uint64_t policy)
+__device__ __forceinline__ void issue_copies(const CUtensorMap *tmap, uint8_t *my_stages, uint64_t *my_bars,
+                                             int my_page, int k0, int k1, int g, int lane, uint64_t policy)
 {
-    const int prologue = min(STAGES, nmine);
-    for (int k = 0; k < prologue; ++k) {
+    for (int k = k0; k < k1; ++k) {
         const int pk = __shfl_sync(kFull, my_page, k);
         if (lane == 0) {
             mbar_arrive_expect_tx(&my_bars[k], kStageBytes);
             tma_load_page_head(my_stages + k * kStageBytes, tmap, &my_bars[k], g, pk, policy);
         }
     }
+}
+
+// Issue the first min(STAGES, nmine) copies of this warp.
+template <int STAGES>
+__device__ __forceinline__ void issue_prologue(const CUtensorMap *tmap, uint8_t *my_stages, uint64_t *my_bars,
+                                               int my_page, int nmine, int g, int lane, uint64_t policy)
+{
+    issue_copies<STAGES>(tmap, my_stages, my_bars, my_page, 0, min(STAGES, nmine), g, lane, policy);
+}
+
+// How many of a warp's first min(stages, nmine) pages (pages j0 + warp + 4k of the
+// sequence) hold only positions below L - 2.  A decode launch may copy those before
+// its dependency wait: the previous decode step of the same layer wrote position
+// L - 2 and the append of this step (fused or a separate kernel just before) writes
+// L - 1, so the pages holding either are copied only after the wait.
+__device__ __forceinline__ int copies_before_wait(int L, int j0, int warp, int nmine, int stages)
+{
+    const int jsafe = max(L - 2, 0) / kPage;  // first page holding position L - 2 or later
+    const int n = jsafe > j0 + warp ? (jsafe - j0 - warp + kWarps - 1) / kWarps : 0;
+    return min(n, min(stages, nmine));
 }
 
 struct NoPatch {
@@ -493,16 +514,18 @@ struct NoPatch {
 // Consume this warp's pages j0 + warp + k*kWarps (k < nmine): wait for the stage,
 // let `patch(stage, j)` edit it, run the policy's page update, refill the stage
 // with page k + STAGES.  Returns false if a bounded wait gave up (after giving
-// the copies still in flight a bounded chance to land).
+// the copies still in flight a bounded chance to land).  The first wait polls at
+// most `first_limit` times (a testing aid can make it give up at once); the others,
+// and the drain of copies in flight, kWaitLimit times.
 template <int STAGES, class Warp, class Patch>
 __device__ __forceinline__ bool consume_pages(const CUtensorMap *tmap, uint8_t *my_stages, uint64_t *my_bars, Warp &w,
                                               int my_page, int nmine, int j0, int warp, int lane, int L, int g,
-                                              uint64_t policy, const Patch &patch)
+                                              uint64_t policy, const Patch &patch, uint32_t first_limit = kWaitLimit)
 {
     int k = 0;
     for (; k < nmine; ++k) {
         const int s = k % STAGES;
-        if (!mbar_wait_warp(&my_bars[s], (uint32_t)((k / STAGES) & 1)))
+        if (!mbar_wait_warp(&my_bars[s], (uint32_t)((k / STAGES) & 1), k == 0 ? first_limit : kWaitLimit))
             break;
         const int j = j0 + warp + k * kWarps;
         uint8_t *stage = my_stages + s * kStageBytes;

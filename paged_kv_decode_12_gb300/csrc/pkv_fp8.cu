@@ -342,12 +342,9 @@ int fp8_decode_split(const pkv_pool *pool, const uint16_t *q, const int32_t *bt,
         return PKV_ERR_CUDA;
     auto kernel = decode_split_fp8_kernel<kFp8Stages>;
     constexpr int smem = Fp8Smem<kFp8Stages>::kBytes;
-    static bool attr_set = false;  // set once per process (before any graph capture)
-    if (!attr_set) {
-        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-            return PKV_ERR_CUDA;
-        attr_set = true;
-    }
+    static PerDeviceOnce attr;  // set on the first launch per device (before any graph capture)
+    if (const int st = ensure_smem_attr(attr, kernel, smem); st != PKV_OK)
+        return st;
     Fp8SplitArgs a;
     a.num_pages = pool->num_pages;
     a.q = q;

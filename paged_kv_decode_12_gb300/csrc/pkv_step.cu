@@ -1,17 +1,19 @@
-// pkv_step.cu -- one fused launch per layer: RoPE + page-slot append of the new
-// token, paged GQA decode attention over the sequence's pages, and the
-// log-sum-exp merge of the chunk partials.
+// pkv_step.cu -- the fused grid kernel of the decode path, one launch per layer.
 //
-// It computes exactly what pkv_append_rope (positions = seq_lens - 1, q rotated
-// in place) followed by pkv_decode_attention computes -- the samir-vllm README
-// summary ("从零用 C++ 和 CUDA 实现 Llama 3.2 1B 推理引擎", section "目前已完成的功能")
-// describes both steps: decode appends one token at its absolute RoPE position,
-// then each query head streams its sequence's pages with an FP32 online softmax
-// -- with the same arithmetic, so the results are bit-identical to the two
-// separate calls.  What changes is the schedule.
+// pkv_decode_step: RoPE + page-slot append of the new token, paged GQA decode
+// attention over the sequence's pages, and the log-sum-exp merge of the chunk
+// partials, in one launch.  It computes exactly what pkv_append_rope (positions =
+// seq_lens - 1, q rotated in place) followed by pkv_decode_attention computes -- the
+// samir-vllm README summary ("从零用 C++ 和 CUDA 实现 Llama 3.2 1B 推理引擎", section
+// "目前已完成的功能") describes both steps: decode appends one token at its absolute
+// RoPE position, then each query head streams its sequence's pages with an FP32
+// online softmax -- with the same arithmetic, so the results are bit-identical to
+// the two separate calls.  pkv_decode_attention runs the same kernel without the
+// append (APPEND = false): the query rows are read as given and no page is written.
 //
-// Work unit = (sequence b, KV head g, chunk c of pages_per_chunk pages), as in the
-// split kernel.  Per unit:
+// Work unit = (sequence b, KV head g, chunk c of pages_per_chunk pages); one CTA per
+// unit (grid = KV heads x B x chunks), optionally dispatched largest unit first.
+// Per unit:
 //  * the 4 query rows of group g are rotated to position L-1 by the unit itself;
 //    the rotated rows are written back once, by the unit that finishes (b, g) last;
 //  * the sequence's last chunk computes the new token's rotated key and its value,
@@ -21,19 +23,17 @@
 //    takes a ticket from a per-(b, g) counter (one release-acquire atomicAdd, no
 //    waiting); the unit drawing the last ticket merges all chunks in chunk order
 //    (deterministic) and resets the counter to zero for the next launch.
-// Two schedules:
-//  * grid: one CTA per unit (grid = chunks x 8 x B); best for long sequences
-//    with large chunks;
-//  * persistent: a few CTAs per SM walk a compact, device-built list of the
-//    non-empty units; each warp's TMA ring keeps prefetching pages ACROSS unit
-//    boundaries, so a unit's set-up and epilogue (combine, ticket, merge) hide
-//    behind copies already in flight.  Best for ragged and small batches.
-// Both use programmatic dependent launch: before griddepcontrol.wait a CTA only
-// reads this step's lengths and block tables and starts the TMA copies of this
-// layer's cached pages (which no earlier kernel of the step writes: every layer
-// has its own pages); q, k_new, v_new are read and every output is written after
-// the wait.
+// Programmatic dependent launch: before griddepcontrol.wait a CTA reads only this
+// step's lengths and block tables and starts the TMA copies of those of its pages
+// that hold only positions below L - 2 (no kernel of this step or the previous one
+// writes them: the previous step's append of this layer wrote position L - 2, this
+// step's writes L - 1, and layers never share pages); the pages holding L - 2 or
+// L - 1 are copied after the wait, q, k_new, v_new are read after it, and every
+// output is written after it.  A CTA lets the next launch begin only after its own
+// wait, so at most one earlier kernel can still be running while it copies early.
 #include <cuda_bf16.h>
+
+#include <climits>
 
 #include "pkv_device.cuh"
 #include "pkv_fp8.cuh"
@@ -46,14 +46,14 @@ using namespace dev;
 struct StepArgs {
     int num_pages;
     uint16_t *slab;
-    const uint16_t *k_new;   // [B][8][64]
-    const uint16_t *v_new;   // [B][8][64]
-    uint16_t *q;             // [B][32][64], rotated in place
+    const uint16_t *k_new;   // [B][8][64] (APPEND)
+    const uint16_t *v_new;   // [B][8][64] (APPEND)
+    uint16_t *q;             // [B][32][64], rotated in place (APPEND) or read as given
     const int32_t *bt;       // [B][max_blocks]
     int max_blocks;
     const int32_t *seq_lens; // [B]
-    const float2 *rope;      // [max_pos][32] (cos, sin)
-    int max_pos;
+    const float2 *rope;      // [max_pos][32] (cos, sin) (APPEND)
+    int max_pos;             // APPEND: rope rows; otherwise INT_MAX
     float scale_log2;
     int pages_per_chunk;
     int *counters;           // [B][8], zero between launches
@@ -62,23 +62,15 @@ struct StepArgs {
     int max_chunks;
     uint16_t *out;           // [B][32][64]
     int32_t *err;
-    int early_trigger;       // grid schedule: allow the next launch as soon as the copies are issued
-    int sorted;              // grid schedule: units dispatched largest first (PKV_STEP_SORTED)
+    int sorted;              // units dispatched largest first (PKV_STEP_SORTED)
+    int expire_seq;          // testing aid: this sequence's first page waits give up at once (-1: none)
 };
 
-constexpr int kStepStages = 4;       // persistent schedule ring depth
-constexpr int kDefaultGridRing = 4;  // grid schedule ring depth unless the options choose one
-constexpr int kMaxPersistentBatch = 512;
 constexpr int kMaxSortedBatch = 1024;
 static_assert(kMaxPagesPerChunk + 1 + kWarps + 5 <= kWarps * kScratchFloats, "sorted-order scratch");
 
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void allow_dependent_launch() { asm volatile("griddepcontrol.launch_dependents;" ::); }
-
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
-{
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
 
 // Take a ticket: atomic increment with release and acquire semantics at GPU scope.
 __device__ __forceinline__ int ticket_acq_rel(int *counter)
@@ -275,15 +267,21 @@ __device__ __forceinline__ int chunks_of(const StepArgs &a, int L)
     return ((L + kPage - 1) / kPage + a.pages_per_chunk - 1) / a.pages_per_chunk;
 }
 
-// All kThreads threads: the 4 query rows of group g rotated to position pos into
-// q_rot[4][64] (one pair per thread) and, for the sequence's last chunk, the new
-// token's rotated key row and its value row into new_kv[2][64].
+// All kThreads threads: the 4 query rows of group g into q_rot[4][64] (one pair per
+// thread) -- rotated to position pos (APPEND), else as given -- and, for the
+// sequence's last chunk (APPEND), the new token's rotated key row and its value row
+// into new_kv[2][64].
+template <bool APPEND>
 __device__ __forceinline__ void unit_rows(const StepArgs &a, int b, int g, int pos, bool last_chunk, uint16_t *q_rot,
                                           uint16_t *new_kv)
 {
     const int hl = threadIdx.x >> 5, i = threadIdx.x & 31;
-    const float2 cs = a.rope[(size_t)pos * (kD / 2) + i];
     const uint16_t *qrow = a.q + ((size_t)b * kHq + g * kGroup + hl) * kD;
+    if (!APPEND) {
+        reinterpret_cast<uint32_t *>(q_rot + hl * kD)[i] = reinterpret_cast<const uint32_t *>(qrow)[i];
+        return;
+    }
+    const float2 cs = a.rope[(size_t)pos * (kD / 2) + i];
     float y1, y2;
     rope_rotate_pair(bf16_value(qrow[i]), bf16_value(qrow[i + kD / 2]), cs.x, cs.y, y1, y2);
     q_rot[hl * kD + i] = bf16_bits(y1);
@@ -328,31 +326,21 @@ __device__ __forceinline__ void write_zero_unit(const StepArgs &a, int b, int g)
         atomicOr(a.err, PKV_DEVERR_LENGTH);
 }
 
-// Unit epilogue, all threads: combine the warps' states through `state`, then
-// write the output (single chunk) or publish the chunk partial and take a ticket;
-// the unit drawing the last ticket merges every chunk of (b, g) in chunk order,
-// writes the output and the rotated query rows, and resets the counter.
-struct CtaSync {
-    __device__ __forceinline__ void operator()() const { __syncthreads(); }
-};
-
-// The 4 consumer warps only (named barrier 1), for kernels with a producer warp.
-struct ConsumerSync {
-    __device__ __forceinline__ void operator()() const { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-};
-
 // Chunk counts up to which the merging unit holds every partial in registers.
 constexpr int kMergeRegs = 8;
 
-template <class Warp, class Sync = CtaSync>
+// Unit epilogue, all threads: combine the warps' states through `state`, then
+// write the output (single chunk) or publish the chunk partial and take a ticket;
+// the unit drawing the last ticket merges every chunk of (b, g) in chunk order,
+// writes the output (and, WRITE_Q, the rotated query rows), and resets the counter.
+template <bool WRITE_Q, class Warp>
 __device__ __forceinline__ void finish_unit(const StepArgs &a, Warp &w, float *state, int *ticket,
-                                            const uint16_t *q_rot, int b, int g, int c, int nchunks,
-                                            Sync sync = Sync())
+                                            const uint16_t *q_rot, int b, int g, int c, int nchunks)
 {
     const int tid = threadIdx.x, warp = tid >> 5;
-    sync();
+    __syncthreads();
     w.store_state(state + warp * kStateFloats);
-    sync();
+    __syncthreads();
     const int hl = tid >> 5, dp = tid & 31, h = g * kGroup + hl;
     float M, lsum, o0, o1;
     combine_warps(state, hl, dp, M, lsum, o0, o1);
@@ -361,7 +349,8 @@ __device__ __forceinline__ void finish_unit(const StepArgs &a, Warp &w, float *s
     const uint32_t q_word = reinterpret_cast<const uint32_t *>(q_rot + hl * kD)[dp];
     if (nchunks == 1) {
         out_row[dp] = finish_pair(o0, o1, lsum);
-        q_row[dp] = q_word;
+        if (WRITE_Q)
+            q_row[dp] = q_word;
         return;
     }
     const size_t base = ((size_t)b * kHq + h) * a.max_chunks;
@@ -371,10 +360,10 @@ __device__ __forceinline__ void finish_unit(const StepArgs &a, Warp &w, float *s
     // publish: the CTA barrier orders every thread's partial stores before thread 0's
     // release-acquire ticket; the acquire side plus the barrier orders the merging
     // unit's loads after every other unit's partial stores
-    sync();
+    __syncthreads();
     if (tid == 0)
         *ticket = ticket_acq_rel(&a.counters[b * kHkv + g]);
-    sync();
+    __syncthreads();
     if (*ticket != nchunks - 1)
         return;
     float ls = 0.f, r0 = 0.f, r1 = 0.f;
@@ -421,7 +410,8 @@ __device__ __forceinline__ void finish_unit(const StepArgs &a, Warp &w, float *s
         }
     }
     out_row[dp] = finish_pair(r0, r1, ls);
-    q_row[dp] = q_word;
+    if (WRITE_Q)
+        q_row[dp] = q_word;
     if (tid == 0)
         a.counters[b * kHkv + g] = 0;
 }
@@ -489,19 +479,17 @@ struct Timeline {  // compiled out
 
 constexpr int kGridExtraBytes = kGroup * kD * 2 + 2 * kD * 2 + 16;  // rotated q rows, new K/V rows, ticket
 
-template <class Warp, int STAGES>
+template <class Warp, int STAGES, bool APPEND>
 __global__ void __launch_bounds__(kThreads) decode_step_kernel(const __grid_constant__ CUtensorMap tmap, StepArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
     SmemLayout<STAGES> sm(smem_raw);
-    uint16_t *q_rot = reinterpret_cast<uint16_t *>(sm.extra);  // [4][64] rotated query rows
+    uint16_t *q_rot = reinterpret_cast<uint16_t *>(sm.extra);  // [4][64] query rows (rotated when APPEND)
     uint16_t *new_kv = q_rot + kGroup * kD;                     // [2][64] rotated key row, value row
     int *ticket = reinterpret_cast<int *>(new_kv + 2 * kD);
     Timeline tl;
     tl.begin();
 
-    // chunk index slowest: every first chunk is dispatched before any later one, so the
-    // CTAs left empty by short sequences come last; or the sorted order
     int g = blockIdx.x, b = blockIdx.y, c = blockIdx.z;
     if (a.sorted) {
         const int lin = blockIdx.x + kHkv * (blockIdx.y + gridDim.y * blockIdx.z);
@@ -544,20 +532,22 @@ __global__ void __launch_bounds__(kThreads) decode_step_kernel(const __grid_cons
     uint64_t *my_bars = sm.bars + warp * STAGES;
     uint8_t *my_stages = sm.stages + warp * STAGES * kStageBytes;
     const uint64_t policy = l2_evict_first_policy();
+    const int nfirst = min(STAGES, nmine);
+    const int nearly = any_bad ? 0 : copies_before_wait(L, j0, warp, nmine, STAGES);
     if (!any_bad) {
         init_warp_barriers<STAGES>(my_bars, lane);
-        issue_prologue<STAGES>(&tmap, my_stages, my_bars, my_page, nmine, g, lane, policy);
+        issue_copies<STAGES>(&tmap, my_stages, my_bars, my_page, 0, nearly, g, lane, policy);
     }
-    if (a.early_trigger)
-        allow_dependent_launch();
 
-    grid_dependency_wait();  // q, k_new, v_new and every output belong to the dependency chain
+    grid_dependency_wait();  // q, k_new, v_new, recently written pages and every output follow it
     tl.stamp(2);
+    if (!any_bad)  // the pages holding positions L - 2 and L - 1
+        issue_copies<STAGES>(&tmap, my_stages, my_bars, my_page, nearly, nfirst, g, lane, policy);
 
     const int pos = L - 1, slot = pos % kPage;
-    unit_rows(a, b, g, pos, last_chunk, q_rot, new_kv);
+    unit_rows<APPEND>(a, b, g, pos, last_chunk, q_rot, new_kv);
     __syncthreads();
-    if (last_chunk && !any_bad && tid < 16)
+    if (APPEND && last_chunk && !any_bad && tid < 16)
         store_new_token(a, a.bt[(size_t)b * a.max_blocks + npages - 1], g, slot, new_kv);
     if (any_bad && tid == 0 && a.err)
         atomicOr(a.err, PKV_DEVERR_PAGE_RANGE);
@@ -566,23 +556,21 @@ __global__ void __launch_bounds__(kThreads) decode_step_kernel(const __grid_cons
     w.init(q_rot, a.scale_log2, lane, sm.scratch + warp * kScratchFloats);
     if (!any_bad) {
         const auto patch = [&](uint8_t *stage, int j) {
-            if (last_chunk && j == npages - 1)
+            if (APPEND && last_chunk && j == npages - 1)
                 patch_stage(stage, slot, new_kv, lane);
         };
-        if (!consume_pages<STAGES>(&tmap, my_stages, my_bars, w, my_page, nmine, j0, warp, lane, L, g, policy,
-                                   patch) &&
+        const uint32_t first_limit = b == a.expire_seq ? 0u : kWaitLimit;
+        if (!consume_pages<STAGES>(&tmap, my_stages, my_bars, w, my_page, nmine, j0, warp, lane, L, g, policy, patch,
+                                   first_limit) &&
             lane == 0 && a.err)
             atomicOr(a.err, PKV_DEVERR_TIMEOUT);
     }
     tl.stamp(3);
-    if (!a.early_trigger)
-        allow_dependent_launch();
+    allow_dependent_launch();
     // the stages are free now: they hold the combine area
-    finish_unit(a, w, reinterpret_cast<float *>(sm.stages), ticket, q_rot, b, g, c, nchunks);
+    finish_unit<APPEND>(a, w, reinterpret_cast<float *>(sm.stages), ticket, q_rot, b, g, c, nchunks);
     tl.end(b, c, jn);
 }
-
-
 
 // ------------------------------------------------------------------ FP8 pages, grid schedule
 
@@ -644,7 +632,7 @@ __device__ __forceinline__ void put_new_token_fp8(uint8_t *unit, int slot, const
 // units of 2176 B in flight per SM; the other rings keep six (80 registers, none spilled).
 constexpr int fp8_ctas_per_sm(int stages) { return stages == 3 ? 7 : 6; }
 
-template <int STAGES>
+template <int STAGES, bool APPEND>
 __global__ void __launch_bounds__(kThreads, fp8_ctas_per_sm(STAGES))
     decode_step_fp8_kernel(const __grid_constant__ CUtensorMap tmap, StepArgs a)
 {
@@ -685,23 +673,28 @@ __global__ void __launch_bounds__(kThreads, fp8_ctas_per_sm(STAGES))
     uint64_t *my_bars = sm.bars + warp * STAGES;
     uint8_t *my_stages = sm.stages + warp * STAGES * kFp8Unit;
     const uint64_t policy = l2_evict_first_policy();
-    if (!any_bad) {
-        init_warp_barriers<STAGES>(my_bars, lane);
-        for (int k = 0; k < min(STAGES, nmine); ++k) {
+    const int nfirst = min(STAGES, nmine);
+    const int nearly = any_bad ? 0 : copies_before_wait(L, j0, warp, nmine, STAGES);
+    const auto issue = [&](int k0, int k1) {
+        for (int k = k0; k < k1; ++k) {
             const int pk = __shfl_sync(kFull, my_page, k);
             if (lane == 0)
                 fp8::fp8_issue(&tmap, my_stages + k * kFp8Unit, &my_bars[k], g, pk, policy);
         }
+    };
+    if (!any_bad) {
+        init_warp_barriers<STAGES>(my_bars, lane);
+        issue(0, nearly);
     }
-    if (a.early_trigger)
-        allow_dependent_launch();
 
-    grid_dependency_wait();  // q, k_new, v_new and every output belong to the dependency chain
+    grid_dependency_wait();  // q, k_new, v_new, recently written pages and every output follow it
+    if (!any_bad)  // the pages holding positions L - 2 and L - 1
+        issue(nearly, nfirst);
 
     const int pos = L - 1, slot = pos % kPage;
-    unit_rows(a, b, g, pos, last_chunk, sm.q_rot, sm.new_kv);
+    unit_rows<APPEND>(a, b, g, pos, last_chunk, sm.q_rot, sm.new_kv);
     __syncthreads();
-    if (last_chunk) {
+    if (APPEND && last_chunk) {
         if (warp == 0) {  // key row: lane holds dims lane, lane + 32 (rotated, BF16)
             uint32_t c1, c2;
             float sc;
@@ -732,14 +725,15 @@ __global__ void __launch_bounds__(kThreads, fp8_ctas_per_sm(STAGES))
     fp8::Fp8MmaWarp w;
     w.init(sm.q_rot, a.scale_log2, lane);
     if (!any_bad) {
+        const uint32_t first_limit = b == a.expire_seq ? 0u : kWaitLimit;
         int k = 0;
         for (; k < nmine; ++k) {
             const int s = k % STAGES;
-            if (!mbar_wait_warp(&my_bars[s], (uint32_t)((k / STAGES) & 1)))
+            if (!mbar_wait_warp(&my_bars[s], (uint32_t)((k / STAGES) & 1), k == 0 ? first_limit : kWaitLimit))
                 break;
             const int j = j0 + warp + k * kWarps;
             uint8_t *stage = my_stages + s * kFp8Unit;
-            if (last_chunk && j == npages - 1) {  // the copy may predate the new token's store
+            if (APPEND && last_chunk && j == npages - 1) {  // the copy may predate the new token's store
                 put_new_token_fp8(stage, slot, sm.new_codes, sm.new_scales, lane);
                 __syncwarp();
             }
@@ -760,705 +754,149 @@ __global__ void __launch_bounds__(kThreads, fp8_ctas_per_sm(STAGES))
                 atomicOr(a.err, PKV_DEVERR_TIMEOUT);
         }
     }
-    if (!a.early_trigger)
-        allow_dependent_launch();
+    allow_dependent_launch();
     // the stages are free now: they hold the combine area
-    finish_unit(a, w, reinterpret_cast<float *>(sm.stages), sm.ticket, sm.q_rot, b, g, c, nchunks);
-}
-
-// ------------------------------------------------------------------ persistent schedule
-
-struct UnitInfo {
-    int b, g, c, L, nchunks, npages, j0, jn;
-    bool valid;
-};
-
-// Unit r of the compact list.  prefix[b] is the first unit of sequence b, which owns
-// 8 * nchunks(b) units ordered (KV head, chunk); an invalid length owns 8 empty units.
-__device__ __forceinline__ UnitInfo decode_unit(const StepArgs &a, const int *prefix, int B, int r)
-{
-    int lo = 0, hi = B - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (prefix[mid] <= r)
-            lo = mid;
-        else
-            hi = mid - 1;
-    }
-    UnitInfo u;
-    u.b = lo;
-    u.nchunks = (prefix[lo + 1] - prefix[lo]) / kHkv;
-    const int rem = r - prefix[lo];
-    u.g = rem / u.nchunks;
-    u.c = rem - u.g * u.nchunks;
-    u.L = a.seq_lens[lo];
-    u.valid = length_ok(a, u.L);
-    u.npages = u.valid ? (u.L + kPage - 1) / kPage : 0;
-    u.j0 = u.c * a.pages_per_chunk;
-    u.jn = u.valid ? min(u.npages - u.j0, a.pages_per_chunk) : 0;
-    return u;
-}
-
-__device__ __forceinline__ int warp_pages(const UnitInfo &u, int warp)
-{
-    return warp < u.jn ? (u.jn - warp + kWarps - 1) / kWarps : 0;
-}
-
-template <int STAGES>
-constexpr int persistent_smem_bytes(int B)
-{
-    return SmemLayout<STAGES>::kBaseBytes + kWarps * kStateFloats * 4 + kGroup * kD * 2 + 2 * kD * 2 + 16 +
-           kWarps * STAGES * 4 + kWarps * 4 + (B + 1) * 4;
-}
-
-template <class Warp, int STAGES>
-__global__ void __launch_bounds__(kThreads)
-decode_step_persistent_kernel(const __grid_constant__ CUtensorMap tmap, StepArgs a, int B)
-{
-    extern __shared__ uint8_t smem_raw[];
-    SmemLayout<STAGES> sm(smem_raw);
-    float *state = reinterpret_cast<float *>(sm.extra);                  // [4 warps][kStateFloats]
-    uint16_t *q_rot = reinterpret_cast<uint16_t *>(state + kWarps * kStateFloats);  // [4][64]
-    uint16_t *new_kv = q_rot + kGroup * kD;                               // [2][64]
-    int *ticket = reinterpret_cast<int *>(new_kv + 2 * kD);              // [4]
-    int *stage_bad = ticket + 4;                                          // [4 warps][STAGES]
-    int *warp_sums = stage_bad + kWarps * STAGES;                         // [4 warps]
-    int *prefix = warp_sums + kWarps;                                     // [B + 1]
-
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-
-    // ---- compact unit list: exclusive prefix sum over sequences (4 per thread)
-    int v[4], local = 0;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int b = 4 * tid + i;
-        int n = 0;
-        if (b < B) {
-            const int L = a.seq_lens[b];
-            n = kHkv * (length_ok(a, L) ? chunks_of(a, L) : 1);
-        }
-        v[i] = n;
-        local += n;
-    }
-    int incl = local;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const int t = __shfl_up_sync(kFull, incl, off);
-        if (lane >= off)
-            incl += t;
-    }
-    if (lane == 31)
-        warp_sums[warp] = incl;
-    __syncthreads();
-    int run = incl - local;
-    for (int ww = 0; ww < warp; ++ww)
-        run += warp_sums[ww];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        if (4 * tid + i < B)
-            prefix[4 * tid + i] = run;
-        run += v[i];
-    }
-    if (tid == kThreads - 1)
-        prefix[B] = run;
-    __syncthreads();
-    const int R = prefix[B];
-    const int P = gridDim.x;
-    const int my_units = (int)blockIdx.x < R ? (R - 1 - (int)blockIdx.x) / P + 1 : 0;
-    if (my_units == 0)
-        return;
-
-    uint64_t *my_bars = sm.bars + warp * STAGES;
-    uint8_t *my_stages = sm.stages + warp * STAGES * kStageBytes;
-    int *my_bad = stage_bad + warp * STAGES;
-    init_warp_barriers<STAGES>(my_bars, lane);
-    const uint64_t policy = l2_evict_first_policy();
-
-    // ---- producer: walks this CTA's units ahead of the consumer, at most STAGES
-    //      pages ahead, across unit boundaries.  Lane k holds the page id of the
-    //      warp's k-th page of the unit being issued.
-    int p_i = 0;
-    UnitInfo pu = decode_unit(a, prefix, B, blockIdx.x);
-    int p_n = warp_pages(pu, warp), p_k = 0;
-    int p_id = lane < p_n ? a.bt[(size_t)pu.b * a.max_blocks + pu.j0 + warp + lane * kWarps] : 0;
-    uint32_t issued = 0, consumed = 0;
-    bool dead = false;  // a bounded wait gave up: stop streaming, keep the bookkeeping going
-    const auto produce = [&]() {
-        while (!dead && (int)(issued - consumed) < STAGES && p_i < my_units) {
-            if (p_k >= p_n) {
-                if (++p_i >= my_units)
-                    break;
-                pu = decode_unit(a, prefix, B, blockIdx.x + p_i * P);
-                p_n = warp_pages(pu, warp);
-                p_k = 0;
-                p_id = lane < p_n ? a.bt[(size_t)pu.b * a.max_blocks + pu.j0 + warp + lane * kWarps] : 0;
-                continue;
-            }
-            const int id = __shfl_sync(kFull, p_id, p_k);
-            const int s = issued % STAGES;
-            if (lane == 0) {
-                const bool ok = id >= 0 && id < a.num_pages;
-                my_bad[s] = ok ? 0 : 1;
-                if (ok) {
-                    fence_proxy_async_smem();
-                    mbar_arrive_expect_tx(&my_bars[s], kStageBytes);
-                    tma_load_page_head(my_stages + s * kStageBytes, &tmap, &my_bars[s], pu.g, id, policy);
-                } else {
-                    mbar_arrive(&my_bars[s]);  // completes the phase without a copy
-                }
-            }
-            __syncwarp();
-            ++issued;
-            ++p_k;
-        }
-    };
-    produce();
-
-    grid_dependency_wait();  // q, k_new, v_new and every output belong to the dependency chain
-
-    for (int i = 0; i < my_units; ++i) {
-        const UnitInfo u = decode_unit(a, prefix, B, blockIdx.x + i * P);
-        __syncthreads();  // the previous unit's epilogue no longer reads q_rot, new_kv, state
-        if (i == my_units - 1)
-            allow_dependent_launch();
-        if (!u.valid) {
-            write_zero_unit(a, u.b, u.g);
-            continue;
-        }
-        const int pos = u.L - 1, slot = pos % kPage;
-        const bool last_chunk = u.c == u.nchunks - 1;
-        unit_rows(a, u.b, u.g, pos, last_chunk, q_rot, new_kv);
-        __syncthreads();
-        if (last_chunk && tid < 16) {
-            const int page = a.bt[(size_t)u.b * a.max_blocks + u.npages - 1];
-            if (page >= 0 && page < a.num_pages)
-                store_new_token(a, page, u.g, slot, new_kv);
-        }
-        Warp w;
-        w.init(q_rot, a.scale_log2, lane, sm.scratch + warp * kScratchFloats);
-        const int n = warp_pages(u, warp);
-        for (int k = 0; k < n; ++k) {
-            const int s = consumed % STAGES;
-            const int j = u.j0 + warp + k * kWarps;
-            if (!dead && !mbar_wait_warp(&my_bars[s], (consumed / STAGES) & 1)) {
-                // give the other copies in flight a bounded chance to land, then stop
-                for (uint32_t kk = consumed + 1; kk < issued; ++kk)
-                    (void)mbar_wait_warp(&my_bars[kk % STAGES], (kk / STAGES) & 1);
-                dead = true;
-                if (lane == 0 && a.err)
-                    atomicOr(a.err, PKV_DEVERR_TIMEOUT);
-            }
-            if (!dead) {
-                uint8_t *stage = my_stages + s * kStageBytes;
-                if (my_bad[s]) {
-                    if (lane == 0 && a.err)
-                        atomicOr(a.err, PKV_DEVERR_PAGE_RANGE);
-                } else {
-                    if (last_chunk && j == u.npages - 1)
-                        patch_stage(stage, slot, new_kv, lane);
-                    w.page(stage, min(kPage, u.L - j * kPage));
-                }
-            }
-            __syncwarp();
-            ++consumed;
-            produce();
-        }
-        finish_unit(a, w, state, ticket, q_rot, u.b, u.g, u.c, u.nchunks);
-    }
-}
-
-// ------------------------------------------------------------------ warp-specialised schedule
-//
-// Per CTA, 4 consumer warps (threads 0..127) and one producer warp (128..159); 2 CTAs
-// per SM.  The producer walks the compact unit list -- the CTA's first unit is
-// blockIdx.x, every further one is drawn from a work counter after the dependency
-// wait -- and for each unit posts a descriptor (the unit's raw query rows, new key
-// and value rows and RoPE row, fetched by 1-D bulk copies) and streams the unit's
-// pages into a CTA-wide ring of kWsRing stages with full/empty mbarriers.  Consumers
-// read a unit's inputs from shared memory only; their epilogue (combine, ticket,
-// merge) overlaps the producer's copies of the next units.  The last CTA to finish
-// resets the work counter, so the workspace counters are zero between launches.
-// A unit's descriptor is posted before any of its pages beyond the first ring-full,
-// so the consumers can always drain the ring (no circular wait).
-
-constexpr int kWsRing = 24;
-constexpr int kWsUnitSlots = 4;
-constexpr int kWsThreads = kThreads + 32;
-
-struct WsDesc {
-    int b, g, c, L, nchunks, j0, jn, first, new_page, valid, end, pad[5];  // 64 B
-    uint16_t q[kGroup * kD];  // raw query rows of the group (512 B)
-    uint16_t k[kD];           // new key row, not yet rotated (128 B)
-    uint16_t v[kD];           // new value row (128 B)
-    float2 rope[kD / 2];      // (cos, sin) at position L-1 (256 B)
-};
-constexpr uint32_t kWsDescCopyBytes = kGroup * kD * 2 + kD * 2 + kD * 2 + (kD / 2) * 8;
-static_assert(sizeof(WsDesc) == 64 + kWsDescCopyBytes && sizeof(WsDesc) % 16 == 0, "descriptor layout");
-
-constexpr int ws_smem_bytes(int B)
-{
-    return 1024 + kWsRing * kStageBytes + (2 * kWsRing + 2 * kWsUnitSlots) * 8 + kWsRing * 4 +
-           kWsUnitSlots * (int)sizeof(WsDesc) + kWarps * kStateFloats * 4 + kWarps * kScratchFloats * 4 +
-           kGroup * kD * 2 + 2 * kD * 2 + 16 + (kWarps + 1) * 4 + (B + 1) * 4;
-}
-
-__device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
-{
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     smem_addr(dst)),
-                 "l"(src), "r"(bytes), "r"(smem_addr(bar))
-                 : "memory");
-}
-
-// OR of a predicate over the 128 consumer threads (named barrier 1).
-__device__ __forceinline__ bool consumer_any(bool p)
-{
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred pi, po;\n\t"
-        "setp.ne.u32 pi, %1, 0;\n\t"
-        "bar.red.or.pred po, 1, 128, pi;\n\t"
-        "selp.u32 %0, 1, 0, po;\n\t}"
-        : "=r"(r)
-        : "r"((uint32_t)p)
-        : "memory");
-    return r != 0;
-}
-
-template <class Warp>
-__global__ void __launch_bounds__(kWsThreads)
-decode_step_ws_kernel(const __grid_constant__ CUtensorMap tmap, StepArgs a, int B, int *work_counter, int *exit_counter)
-{
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *full = reinterpret_cast<uint64_t *>(ring + kWsRing * kStageBytes);
-    uint64_t *empty = full + kWsRing;
-    uint64_t *ufull = empty + kWsRing;
-    uint64_t *uempty = ufull + kWsUnitSlots;
-    int *bad = reinterpret_cast<int *>(uempty + kWsUnitSlots);
-    WsDesc *desc = reinterpret_cast<WsDesc *>(bad + kWsRing);
-    float *state = reinterpret_cast<float *>(desc + kWsUnitSlots);
-    float *scratch = state + kWarps * kStateFloats;
-    uint16_t *q_rot = reinterpret_cast<uint16_t *>(scratch + kWarps * kScratchFloats);
-    uint16_t *new_kv = q_rot + kGroup * kD;
-    int *ticket = reinterpret_cast<int *>(new_kv + 2 * kD);
-    int *warp_sums = ticket + 4;
-    int *prefix = warp_sums + kWarps + 1;
-
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-
-    // ---- compact unit list (as the persistent schedule), 4 sequences per thread
-    {
-        int v[4], local = 0;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int b = 4 * tid + i;
-            int n = 0;
-            if (b < B) {
-                const int L = a.seq_lens[b];
-                n = kHkv * (length_ok(a, L) ? chunks_of(a, L) : 1);
-            }
-            v[i] = n;
-            local += n;
-        }
-        int incl = local;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int t = __shfl_up_sync(kFull, incl, off);
-            if (lane >= off)
-                incl += t;
-        }
-        if (lane == 31)
-            warp_sums[warp] = incl;
-        if (tid == 0) {
-            for (int s = 0; s < kWsRing; ++s) {
-                mbar_init(&full[s], 1);
-                mbar_init(&empty[s], 1);
-            }
-            for (int s = 0; s < kWsUnitSlots; ++s) {
-                mbar_init(&ufull[s], 1);
-                mbar_init(&uempty[s], 1);
-            }
-            fence_barrier_init();
-        }
-        __syncthreads();
-        int run = incl - local;
-        for (int ww = 0; ww < warp; ++ww)
-            run += warp_sums[ww];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            if (4 * tid + i < B)
-                prefix[4 * tid + i] = run;
-            run += v[i];
-        }
-        if (tid == kWsThreads - 1)
-            prefix[B] = run;
-        __syncthreads();
-    }
-    const int R = prefix[B];
-
-    if (warp == kWarps) {
-        // ================================================================ producer
-        const uint64_t policy = l2_evict_first_policy();
-        int r = blockIdx.x;
-        uint32_t G = 0, ui = 0;
-        bool waited = false, dead = false;
-        for (;;) {
-            const int us = ui % kWsUnitSlots;
-            if (ui >= kWsUnitSlots && !dead &&
-                !mbar_wait_warp(&uempty[us], ((ui / kWsUnitSlots) - 1) & 1))
-                dead = true;
-            WsDesc *d = desc + us;
-            if (r >= R || dead) {
-                if (!waited)
-                    grid_dependency_wait();
-                if (lane == 0) {
-                    d->end = 1;
-                    mbar_arrive(&ufull[us]);
-                }
-                break;
-            }
-            const UnitInfo u = decode_unit(a, prefix, B, r);
-            int id[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int k = lane + 32 * i;
-                id[i] = k < u.jn ? a.bt[(size_t)u.b * a.max_blocks + u.j0 + k] : 0;
-            }
-            const auto page_id = [&](int k) {
-                const int i = k >> 5;
-                const int mine = i == 0 ? id[0] : i == 1 ? id[1] : i == 2 ? id[2] : id[3];
-                return __shfl_sync(kFull, mine, k & 31);
-            };
-            // Issue pages k .. k+n-1 (n <= 4) from lanes 0..n-1.  A stage is reused only
-            // after its consumer released it (empty barrier, acquire after release); the
-            // consumers' reads need no proxy fence before the copy overwrites them.
-            const auto issue_pages = [&](int k, int n) {
-                for (int i = 0; i < n; ++i) {
-                    const uint32_t gi = G + i;
-                    if (gi >= kWsRing && !dead &&
-                        !mbar_wait_warp(&empty[gi % kWsRing], ((gi / kWsRing) - 1) & 1))
-                        dead = true;
-                }
-                // k is a multiple of 4, so pages k..k+3 share one 32-entry register block
-                const int reg = k >> 5;
-                const int mine = reg == 0 ? id[0] : reg == 1 ? id[1] : reg == 2 ? id[2] : id[3];
-                const int pid = __shfl_sync(kFull, mine, (k & 31) + (lane & 3));
-                if (lane < n) {
-                    const int s = (G + lane) % kWsRing;
-                    const bool ok = pid >= 0 && pid < a.num_pages && !dead;
-                    bad[s] = ok ? 0 : 1;
-                    if (ok) {
-                        mbar_arrive_expect_tx(&full[s], kStageBytes);
-                        tma_load_page_head(ring + s * kStageBytes, &tmap, &full[s], u.g, pid, policy);
-                    } else {
-                        mbar_arrive(&full[s]);
-                    }
-                }
-                __syncwarp();
-                G += n;
-            };
-            const uint32_t first = G;
-            int k = 0;
-            if (!waited) {
-                // before the dependency wait: only this layer's cached pages, at most one ring-full
-                const int pre = min(u.jn, kWsRing);
-                for (; k < pre; k += 4)
-                    issue_pages(k, min(4, pre - k));
-                grid_dependency_wait();
-                waited = true;
-            }
-            // the unit's descriptor, then its remaining pages
-            const int new_page = (u.valid && u.c == u.nchunks - 1 && u.jn > 0) ? page_id(u.jn - 1) : -1;
-            if (lane == 0) {
-                d->b = u.b;
-                d->g = u.g;
-                d->c = u.c;
-                d->L = u.L;
-                d->nchunks = u.nchunks;
-                d->j0 = u.j0;
-                d->jn = u.jn;
-                d->first = (int)first;
-                d->new_page = new_page;
-                d->valid = u.valid ? 1 : 0;
-                d->end = 0;
-                if (u.valid) {
-                    fence_proxy_async_smem();
-                    mbar_arrive_expect_tx(&ufull[us], kWsDescCopyBytes);
-                    bulk_copy_g2s(d->q, a.q + ((size_t)u.b * kHq + u.g * kGroup) * kD, kGroup * kD * 2, &ufull[us]);
-                    bulk_copy_g2s(d->k, a.k_new + ((size_t)u.b * kHkv + u.g) * kD, kD * 2, &ufull[us]);
-                    bulk_copy_g2s(d->v, a.v_new + ((size_t)u.b * kHkv + u.g) * kD, kD * 2, &ufull[us]);
-                    bulk_copy_g2s(d->rope, a.rope + (size_t)(u.L - 1) * (kD / 2), (kD / 2) * 8, &ufull[us]);
-                } else {
-                    mbar_arrive(&ufull[us]);
-                }
-            }
-            int nxt = 0;
-            if (lane == 0)
-                nxt = (int)gridDim.x + atomicAdd(work_counter, 1);
-            for (; k < u.jn; k += 4)
-                issue_pages(k, min(4, u.jn - k));
-            r = __shfl_sync(kFull, nxt, 0);
-            ++ui;
-        }
-        allow_dependent_launch();
-    } else {
-        // ================================================================ consumers
-        const ConsumerSync csync;
-        uint32_t ui = 0;
-        bool dead = false, waited = false;
-        for (;;) {
-            const int us = ui % kWsUnitSlots;
-            csync();  // the previous unit's epilogue no longer reads q_rot, new_kv, state
-            const bool timed_out = !mbar_wait_warp(&ufull[us], (ui / kWsUnitSlots) & 1);
-            if (consumer_any(timed_out)) {
-                if (tid == 0 && a.err)
-                    atomicOr(a.err, PKV_DEVERR_TIMEOUT);
-                break;
-            }
-            const WsDesc *d = desc + us;
-            if (d->end)
-                break;
-            if (!waited) {
-                grid_dependency_wait();
-                waited = true;
-            }
-            const int b = d->b, g = d->g, c = d->c, L = d->L, nchunks = d->nchunks, j0 = d->j0, jn = d->jn;
-            const int first = d->first, new_page = d->new_page;
-            if (!d->valid) {
-                csync();
-                if (tid == 0)
-                    mbar_arrive(&uempty[us]);
-                write_zero_unit(a, b, g);
-                ++ui;
-                continue;
-            }
-            const int pos = L - 1, slot = pos % kPage, npages = (L + kPage - 1) / kPage;
-            const bool last_chunk = c == nchunks - 1;
-            {
-                const int hl = tid >> 5, i = tid & 31;
-                const float2 cs = d->rope[i];
-                float y1, y2;
-                rope_rotate_pair(bf16_value(d->q[hl * kD + i]), bf16_value(d->q[hl * kD + i + kD / 2]), cs.x, cs.y,
-                                 y1, y2);
-                q_rot[hl * kD + i] = bf16_bits(y1);
-                q_rot[hl * kD + i + kD / 2] = bf16_bits(y2);
-                if (last_chunk && hl == 0) {
-                    rope_rotate_pair(bf16_value(d->k[i]), bf16_value(d->k[i + kD / 2]), cs.x, cs.y, y1, y2);
-                    new_kv[i] = bf16_bits(y1);
-                    new_kv[i + kD / 2] = bf16_bits(y2);
-                } else if (last_chunk && hl == 1) {
-                    reinterpret_cast<uint32_t *>(new_kv + kD)[i] = reinterpret_cast<const uint32_t *>(d->v)[i];
-                }
-            }
-            csync();
-            if (tid == 0)
-                mbar_arrive(&uempty[us]);  // the descriptor is consumed
-            if (last_chunk && tid < 16 && new_page >= 0 && new_page < a.num_pages)
-                store_new_token(a, new_page, g, slot, new_kv);
-            Warp w;
-            w.init(q_rot, a.scale_log2, lane, scratch + warp * kScratchFloats);
-            for (int k = warp; k < jn; k += kWarps) {
-                const uint32_t gi = (uint32_t)first + k;
-                const int s = gi % kWsRing;
-                if (!dead && !mbar_wait_warp(&full[s], (gi / kWsRing) & 1)) {
-                    dead = true;
-                    if (lane == 0 && a.err)
-                        atomicOr(a.err, PKV_DEVERR_TIMEOUT);
-                }
-                if (!dead) {
-                    uint8_t *stage = ring + s * kStageBytes;
-                    if (bad[s]) {
-                        if (lane == 0 && a.err)
-                            atomicOr(a.err, PKV_DEVERR_PAGE_RANGE);
-                    } else {
-                        const int j = j0 + k;
-                        const bool patched = last_chunk && j == npages - 1;
-                        if (patched)
-                            patch_stage(stage, slot, new_kv, lane);
-                        w.page(stage, min(kPage, L - j * kPage));
-                        if (patched)  // generic stores into the stage precede the next copy into it
-                            fence_proxy_async_smem();
-                    }
-                }
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(&empty[s]);
-            }
-            finish_unit(a, w, state, ticket, q_rot, b, g, c, nchunks, csync);
-            ++ui;
-        }
-    }
-
-    // ---- the last CTA to finish resets the work counter for the next launch
-    __syncthreads();
-    if (tid == 0) {
-        grid_dependency_wait();
-        __threadfence();
-        if (atomicAdd(exit_counter, 1) == (int)gridDim.x - 1) {
-            atomicExch(work_counter, 0);
-            atomicExch(exit_counter, 0);
-        }
-    }
+    finish_unit<APPEND>(a, w, reinterpret_cast<float *>(sm.stages), sm.ticket, sm.q_rot, b, g, c, nchunks);
 }
 
 // ------------------------------------------------------------------ launch
 
-size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+// Ring depth per warp when the options leave it to the library: 3 stages for long
+// chunks (4 CTAs per SM for BF16, 7 for FP8), else 2 (6 per SM), the measured best
+// for 128-page chunks and for 16- to 32-page chunks of ragged batches respectively.
+int default_ring(int pages_per_chunk) { return pages_per_chunk >= 64 ? 3 : 2; }
 
-cudaLaunchAttribute pdl_attribute()
-{
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr.val.programmaticStreamSerializationAllowed = 1;
-    return attr;
-}
-
-template <class Warp, int STAGES>
+template <class Warp, int STAGES, bool APPEND>
 int launch_grid(const CUtensorMap *tmap, const StepArgs &a, int B, cudaStream_t s, bool pdl)
 {
-    auto kernel = decode_step_kernel<Warp, STAGES>;
+    auto kernel = decode_step_kernel<Warp, STAGES, APPEND>;
     constexpr int smem = SmemLayout<STAGES>::kBaseBytes + kGridExtraBytes;
-    static bool attr_set = false;  // set once per process (before any graph capture)
-    if (!attr_set) {
-        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-            return PKV_ERR_CUDA;
-        attr_set = true;
-    }
+    static PerDeviceOnce attr;
+    if (const int st = ensure_smem_attr(attr, kernel, smem); st != PKV_OK)
+        return st;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(kHkv, B, a.max_chunks);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1] = {pdl_attribute()};
-    cfg.attrs = attr;
+    cudaLaunchAttribute attrs[1] = {pdl_attribute()};
+    cfg.attrs = attrs;
     cfg.numAttrs = pdl ? 1 : 0;
     return status_from_cuda(cudaLaunchKernelEx(&cfg, kernel, *tmap, a));
 }
 
 // FP8 pages: ring depth per warp 2..4 units (2176 B each).
-template <int STAGES>
+template <int STAGES, bool APPEND>
 int launch_fp8_grid(const CUtensorMap *tmap, const StepArgs &a, int B, cudaStream_t s, bool pdl)
 {
-    auto kernel = decode_step_fp8_kernel<STAGES>;
+    auto kernel = decode_step_fp8_kernel<STAGES, APPEND>;
     constexpr int smem = Fp8StepSmem<STAGES>::kBytes;
-    static bool attr_set = false;  // set once per process (before any graph capture)
-    if (!attr_set) {
-        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-            return PKV_ERR_CUDA;
-        attr_set = true;
-    }
+    static PerDeviceOnce attr;
+    if (const int st = ensure_smem_attr(attr, kernel, smem); st != PKV_OK)
+        return st;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(kHkv, B, a.max_chunks);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1] = {pdl_attribute()};
-    cfg.attrs = attr;
+    cudaLaunchAttribute attrs[1] = {pdl_attribute()};
+    cfg.attrs = attrs;
     cfg.numAttrs = pdl ? 1 : 0;
     return status_from_cuda(cudaLaunchKernelEx(&cfg, kernel, *tmap, a));
 }
 
+template <bool APPEND>
 int launch_fp8_depth(const CUtensorMap *tmap, const StepArgs &a, int B, cudaStream_t s, bool pdl, int depth)
 {
     switch (depth) {
-    case 2: return launch_fp8_grid<2>(tmap, a, B, s, pdl);
-    case 3: return launch_fp8_grid<3>(tmap, a, B, s, pdl);
-    default: return launch_fp8_grid<4>(tmap, a, B, s, pdl);
+    case 2: return launch_fp8_grid<2, APPEND>(tmap, a, B, s, pdl);
+    case 3: return launch_fp8_grid<3, APPEND>(tmap, a, B, s, pdl);
+    default: return launch_fp8_grid<4, APPEND>(tmap, a, B, s, pdl);
     }
 }
 
 // Ring depth per warp: 2 stages (36 KB per CTA, 6 CTAs per SM), 3 (4 per SM) or 4 (3 per SM).
-template <class Warp>
+template <class Warp, bool APPEND>
 int launch_grid_depth(const CUtensorMap *tmap, const StepArgs &a, int B, cudaStream_t s, bool pdl, int depth)
 {
     switch (depth) {
-    case 2: return launch_grid<Warp, 2>(tmap, a, B, s, pdl);
-    case 3: return launch_grid<Warp, 3>(tmap, a, B, s, pdl);
-    default: return launch_grid<Warp, 4>(tmap, a, B, s, pdl);
+    case 2: return launch_grid<Warp, 2, APPEND>(tmap, a, B, s, pdl);
+    case 3: return launch_grid<Warp, 3, APPEND>(tmap, a, B, s, pdl);
+    default: return launch_grid<Warp, 4, APPEND>(tmap, a, B, s, pdl);
     }
 }
 
-// CTAs per SM the persistent kernel is sized for, and the SM count, per device.
-struct PersistentShape {
-    int sms = 0;
-    int ctas_per_sm = 0;
-};
+// Option bits both entry points accept for the fused grid kernel.
+constexpr int kGridOptions = 0xff | PKV_STEP_NO_PDL | PKV_STEP_GRID | PKV_STEP_RING_MASK | PKV_STEP_SORTED |
+                             PKV_STEP_TEST_EXPIRE_WAIT;
 
-template <class Warp>
-int launch_persistent(const CUtensorMap *tmap, const StepArgs &a, int B, cudaStream_t s, bool pdl)
+// Validates the options, fills the launch-dependent fields of `a` and launches the
+// kernel for the pool's format.
+template <bool APPEND>
+int launch_fused(const pkv_pool *pool, StepArgs &a, int B, int max_blocks, int pages_per_chunk, void *workspace,
+                 cudaStream_t s, int options)
 {
-    auto kernel = decode_step_persistent_kernel<Warp, kStepStages>;
-    constexpr int max_smem = persistent_smem_bytes<kStepStages>(kMaxPersistentBatch);
-    constexpr int kMaxDevices = 64;
-    static PersistentShape shape[kMaxDevices];  // filled on the first call per device (before any capture)
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    const int variant = options & 0xff;
+    if (variant < PKV_DECODE_DEFAULT || variant > PKV_DECODE_MMA || (options & ~kGridOptions))
+        return PKV_ERR_INVALID_ARG;
+    if ((options & PKV_STEP_SORTED) && B > kMaxSortedBatch)
+        return PKV_ERR_INVALID_ARG;  // the sorted order handles up to 1024 sequences
+    const int ring = (options & PKV_STEP_RING_MASK) >> 12;
+    if (ring != 0 && (ring < 2 || ring > 4))
+        return PKV_ERR_INVALID_ARG;
+    if (pool->kv_format == PKV_KV_FP8 && variant == PKV_DECODE_SIMT)
+        return PKV_ERR_UNSUPPORTED;  // FP8 pages: the MMA policy only
+    const int max_chunks = (max_blocks + pages_per_chunk - 1) / pages_per_chunk;
+    if (max_chunks > 65535)  // the chunk index is gridDim.z
+        return PKV_ERR_INVALID_ARG;
+    const CUtensorMap *tmap = pool_tensor_map(pool);
+    if (!tmap)
         return PKV_ERR_CUDA;
-    PersistentShape &ps = shape[dev];
-    if (ps.sms == 0) {
-        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem) != cudaSuccess ||
-            cudaDeviceGetAttribute(&ps.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ps.ctas_per_sm, kernel, kThreads, max_smem) !=
-                cudaSuccess ||
-            ps.ctas_per_sm < 1) {
-            ps.sms = 0;
-            return PKV_ERR_CUDA;
-        }
-    }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(ps.sms * ps.ctas_per_sm);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = persistent_smem_bytes<kStepStages>(B);
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1] = {pdl_attribute()};
-    cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 1 : 0;
-    return status_from_cuda(cudaLaunchKernelEx(&cfg, kernel, *tmap, a, B));
-}
-
-template <class Warp>
-int launch_ws(const CUtensorMap *tmap, const StepArgs &a, int B, cudaStream_t s, bool pdl)
-{
-    auto kernel = decode_step_ws_kernel<Warp>;
-    constexpr int max_smem = ws_smem_bytes(kMaxPersistentBatch);
-    constexpr int kMaxDevices = 64;
-    static PersistentShape shape[kMaxDevices];  // filled on the first call per device (before any capture)
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
-        return PKV_ERR_CUDA;
-    PersistentShape &ps = shape[dev];
-    if (ps.sms == 0) {
-        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem) != cudaSuccess ||
-            cudaDeviceGetAttribute(&ps.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ps.ctas_per_sm, kernel, kWsThreads, max_smem) !=
-                cudaSuccess ||
-            ps.ctas_per_sm < 1) {
-            ps.sms = 0;
-            return PKV_ERR_CUDA;
-        }
-    }
-    int *work_counter = a.counters + (size_t)B * kHkv;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(ps.sms * ps.ctas_per_sm);
-    cfg.blockDim = dim3(kWsThreads);
-    cfg.dynamicSmemBytes = ws_smem_bytes(B);
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1] = {pdl_attribute()};
-    cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 1 : 0;
-    return status_from_cuda(cudaLaunchKernelEx(&cfg, kernel, *tmap, a, B, work_counter, work_counter + 1));
+    const WorkspaceLayout ws = workspace_layout(B, max_chunks);
+    char *wsp = static_cast<char *>(workspace);
+    a.num_pages = pool->num_pages;
+    a.slab = reinterpret_cast<uint16_t *>(pool->slab);
+    a.max_blocks = max_blocks;
+    a.pages_per_chunk = pages_per_chunk;
+    a.counters = wsp ? reinterpret_cast<int *>(wsp) : nullptr;
+    a.part_ml = wsp ? reinterpret_cast<float2 *>(wsp + ws.ml_offset()) : nullptr;
+    a.part_o = wsp ? reinterpret_cast<float *>(wsp + ws.o_offset()) : nullptr;
+    a.max_chunks = max_chunks;
+    a.sorted = (options & PKV_STEP_SORTED) ? 1 : 0;
+    a.expire_seq = (options & PKV_STEP_TEST_EXPIRE_WAIT) ? 0 : -1;
+    const bool pdl = take_pdl_permission(pool, !(options & PKV_STEP_NO_PDL));
+    const int depth = ring ? ring : default_ring(pages_per_chunk);
+    if (pool->kv_format == PKV_KV_FP8)
+        return launch_fp8_depth<APPEND>(tmap, a, B, s, pdl, depth);
+    return variant == PKV_DECODE_SIMT ? launch_grid_depth<SimtWarp, APPEND>(tmap, a, B, s, pdl, depth)
+                                      : launch_grid_depth<MmaWarp, APPEND>(tmap, a, B, s, pdl, depth);
 }
 
 }  // namespace
+
+int launch_attention_fused(const pkv_pool *pool, const uint16_t *q, const int32_t *bt, int max_blocks,
+                           const int32_t *seq_lens, int B, float scale, int pages_per_chunk, void *workspace,
+                           uint16_t *out, int32_t *err, cudaStream_t s, int options)
+{
+    StepArgs a = {};
+    a.k_new = nullptr;
+    a.v_new = nullptr;
+    a.q = const_cast<uint16_t *>(q);  // read only: no append writes the rows back
+    a.bt = bt;
+    a.seq_lens = seq_lens;
+    a.rope = nullptr;
+    a.max_pos = INT_MAX;
+    a.scale_log2 = scale * kLog2e;
+    a.out = out;
+    a.err = err;
+    return launch_fused<false>(pool, a, B, max_blocks, pages_per_chunk, workspace, s, options);
+}
+
 }  // namespace pkv
 
 extern "C" size_t pkv_decode_step_workspace_bytes(int B, int max_blocks, int pages_per_chunk)
 {
-    using namespace pkv;
-    if (B < 1 || max_blocks < 1 || pages_per_chunk < 1)
-        return 0;
-    return align256(((size_t)B * kHkv + 2) * sizeof(int)) + pkv_decode_workspace_bytes(B, max_blocks, pages_per_chunk);
+    return pkv_decode_workspace_bytes(B, max_blocks, pages_per_chunk);
 }
 
 extern "C" int pkv_decode_step(const pkv_pool *pool, const uint16_t *k_new, const uint16_t *v_new, uint16_t *q,
@@ -1474,16 +912,6 @@ extern "C" int pkv_decode_step(const pkv_pool *pool, const uint16_t *k_new, cons
         return PKV_ERR_INVALID_ARG;
     if (pages_per_chunk < 1 || pages_per_chunk > kMaxPagesPerChunk || !(scale > 0.f) || !(scale < INFINITY))
         return PKV_ERR_INVALID_ARG;
-    const int variant = options & 0xff;
-    if (variant < PKV_DECODE_DEFAULT || variant > PKV_DECODE_MMA ||
-        (options & ~(0xff | PKV_STEP_NO_PDL | PKV_STEP_GRID | PKV_STEP_PERSISTENT | PKV_STEP_WS |
-                     PKV_STEP_RING_MASK | PKV_STEP_EARLY_TRIGGER | PKV_STEP_SORTED)) ||
-        (!!(options & PKV_STEP_GRID) + !!(options & PKV_STEP_PERSISTENT) + !!(options & PKV_STEP_WS) > 1))
-        return PKV_ERR_INVALID_ARG;
-    if ((options & (PKV_STEP_PERSISTENT | PKV_STEP_WS)) && B > kMaxPersistentBatch)
-        return PKV_ERR_INVALID_ARG;
-    if ((options & PKV_STEP_SORTED) && ((options & (PKV_STEP_PERSISTENT | PKV_STEP_WS)) || B > kMaxSortedBatch))
-        return PKV_ERR_INVALID_ARG;  // the sorted order is a grid-schedule option, up to 1024 sequences
     const uintptr_t align = reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new) |
                             reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out) |
                             reinterpret_cast<uintptr_t>(rope_table) | reinterpret_cast<uintptr_t>(workspace);
@@ -1491,57 +919,19 @@ extern "C" int pkv_decode_step(const pkv_pool *pool, const uint16_t *k_new, cons
         return PKV_ERR_INVALID_ARG;
     if (workspace_bytes < pkv_decode_step_workspace_bytes(B, max_blocks, pages_per_chunk))
         return PKV_ERR_WORKSPACE_TOO_SMALL;
-    if (pool->kv_format == PKV_KV_FP8 &&
-        (variant == PKV_DECODE_SIMT || (options & (PKV_STEP_PERSISTENT | PKV_STEP_WS))))
-        return PKV_ERR_UNSUPPORTED;  // FP8 pages: the grid schedule and the MMA policy only
-    const CUtensorMap *tmap = pool_tensor_map(pool);
-    if (!tmap)
-        return PKV_ERR_CUDA;
-    const int max_chunks = (max_blocks + pages_per_chunk - 1) / pages_per_chunk;
-    if (max_chunks > 65535)  // the grid schedule puts the chunk index in gridDim.z
-        return PKV_ERR_INVALID_ARG;
-    char *ws = static_cast<char *>(workspace);
-    const size_t counters_bytes = align256(((size_t)B * kHkv + 2) * sizeof(int));
-    const size_t ml_bytes = align256((size_t)B * kHq * max_chunks * sizeof(float2));
-    StepArgs a;
-    a.num_pages = pool->num_pages;
-    a.slab = reinterpret_cast<uint16_t *>(pool->slab);
+    StepArgs a = {};
     a.k_new = k_new;
     a.v_new = v_new;
     a.q = q;
     a.bt = bt_dev;
-    a.max_blocks = max_blocks;
     a.seq_lens = seq_lens_dev;
     a.rope = reinterpret_cast<const float2 *>(rope_table);
     a.max_pos = max_pos;
-    a.scale_log2 = scale * 1.4426950408889634f;
-    a.pages_per_chunk = pages_per_chunk;
-    a.counters = reinterpret_cast<int *>(ws);
-    a.part_ml = reinterpret_cast<float2 *>(ws + counters_bytes);
-    a.part_o = reinterpret_cast<float *>(ws + counters_bytes + ml_bytes);
-    a.max_chunks = max_chunks;
+    a.scale_log2 = scale * kLog2e;
     a.out = out;
     a.err = dev_err_flag;
-    a.early_trigger = (options & PKV_STEP_EARLY_TRIGGER) ? 1 : 0;
-    a.sorted = (options & PKV_STEP_SORTED) ? 1 : 0;
-    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
-    const bool pdl = !(options & PKV_STEP_NO_PDL);
-    // the grid schedule is the measured default; the persistent one is chosen explicitly
-    if (options & PKV_STEP_WS)
-        return variant == PKV_DECODE_SIMT ? launch_ws<SimtWarp>(tmap, a, B, s, pdl)
-                                          : launch_ws<MmaWarp>(tmap, a, B, s, pdl);
-    const bool persistent = (options & PKV_STEP_PERSISTENT) != 0;
-    if (persistent)
-        return variant == PKV_DECODE_SIMT ? launch_persistent<SimtWarp>(tmap, a, B, s, pdl)
-                                          : launch_persistent<MmaWarp>(tmap, a, B, s, pdl);
-    const int ring = (options & PKV_STEP_RING_MASK) >> 12;
-    if (ring != 0 && (ring < 2 || ring > 4))
-        return PKV_ERR_INVALID_ARG;
-    const int depth = ring ? ring : kDefaultGridRing;
-    if (pool->kv_format == PKV_KV_FP8)
-        return launch_fp8_depth(tmap, a, B, s, pdl, depth);
-    return variant == PKV_DECODE_SIMT ? launch_grid_depth<SimtWarp>(tmap, a, B, s, pdl, depth)
-                                      : launch_grid_depth<MmaWarp>(tmap, a, B, s, pdl, depth);
+    return launch_fused<true>(pool, a, B, max_blocks, pages_per_chunk, workspace,
+                              static_cast<cudaStream_t>(cuda_stream), options);
 }
 
 #ifdef PKV_TIMELINE

@@ -11,12 +11,14 @@ every step of the computation runs in libpkv's kernels.
 ``run_host`` is the end-to-end form: inputs come from pinned host memory and
 the result goes back to it, with the copies on the same stream as the kernels.
 
-Micro-batch chains (``chains=K``, fused path): the batch rows are cut into K
-contiguous groups, each group runs its own chain of per-layer fused launches on
-its own stream (forked from and joined back to the caller's stream), so one
-group's layer tail overlaps another group's streaming.  Layer order is kept
-inside every group; sequences never interact, so every output byte is the same
-as with one chain.
+By default each layer runs as one fused launch (``pkv_decode_step``: append and
+attention in one kernel); ``fused=False`` runs the two named calls instead.
+
+Micro-batch chains (``chains=K``): the batch rows are cut into K contiguous
+groups, each group runs its own chain of per-layer launches on its own stream
+(forked from and joined back to the caller's stream), so one group's layer tail
+overlaps another group's streaming.  Layer order is kept inside every group;
+sequences never interact, so every output byte is the same as with one chain.
 """
 from __future__ import annotations
 
@@ -29,21 +31,18 @@ from . import pkv
 from . import workloads as wl
 
 
-SCHEDULES = {"auto": 0, "grid": pkv.PKV_STEP_GRID, "persistent": pkv.PKV_STEP_PERSISTENT, "ws": pkv.PKV_STEP_WS}
-
-
 class DecodeEngine:
     def __init__(self, num_pages: int, layers: int, batch: int, max_blocks: int = wl.MAX_BLOCKS,
                  pages_per_chunk: int = 16, variant: int = pkv.PKV_DECODE_DEFAULT, max_pos: int = wl.MAX_CONTEXT,
                  theta: float = wl.ROPE_THETA, pool_seed: int = 0, device: str = "cuda", fused: bool = True,
-                 pdl: bool = True, schedule: str = "auto", ring: int = 0, early_trigger: bool = False,
-                 kv: str = "bf16", sorted_units: bool = False, chains: int = 1):
+                 pdl: bool = True, ring: int = 0, kv: str = "bf16", sorted_units: bool = False, chains: int = 1,
+                 split_merge: bool = False):
         if kv not in ("bf16", "fp8"):
             raise ValueError(f"kv must be 'bf16' or 'fp8', not {kv!r}")
         if not 1 <= chains <= batch:
             raise ValueError(f"chains must be in [1, batch], not {chains}")
-        if chains > 1 and not fused:
-            raise ValueError("micro-batch chains run the fused step only")
+        if split_merge and fused:
+            raise ValueError("split_merge selects the two-kernel attention of the separate path (fused=False)")
         self.kv = kv
         self.device = torch.device(device)
         self.layers, self.batch, self.max_blocks = layers, batch, max_blocks
@@ -59,24 +58,22 @@ class DecodeEngine:
         self.rope = torch.empty(max_pos * (wl.HEAD_DIM // 2) * 2, dtype=torch.float32, device=self.device)
         pkv.pkv_rope_table_init(theta, max_pos, wl.HEAD_DIM // 2, self.rope)
         self.err = torch.zeros(1, dtype=torch.int32, device=self.device)
+        # the attention workspace (the fused step's too) starts with per-(sequence, KV head)
+        # merge counters that must be zero before the first call (every call leaves them zero)
         self.ws_bytes = pkv.pkv_decode_workspace_bytes(batch, max_blocks, pages_per_chunk)
-        self.workspace = torch.empty(max(self.ws_bytes, 16), dtype=torch.uint8, device=self.device)
-        # the fused step's workspace starts with per-(sequence, KV head) counters that
-        # must be zero before the first call (every call leaves them zero)
+        self.workspace = torch.zeros(max(self.ws_bytes, 16), dtype=torch.uint8, device=self.device)
         self.step_ws_bytes = pkv.pkv_decode_step_workspace_bytes(batch, max_blocks, pages_per_chunk)
-        self.step_ws = torch.zeros(self.step_ws_bytes, dtype=torch.uint8, device=self.device)
+        self.step_ws = self.workspace
         self.fused = fused
-        self.step_options = (variant | (0 if pdl else pkv.PKV_STEP_NO_PDL) | SCHEDULES[schedule]
-                             | pkv.PKV_STEP_RING(ring) | (pkv.PKV_STEP_EARLY_TRIGGER if early_trigger else 0)
+        # launch options of the fused step and of the separate path's attention call
+        self.step_options = (variant | (0 if pdl else pkv.PKV_STEP_NO_PDL) | pkv.PKV_STEP_RING(ring)
                              | (pkv.PKV_STEP_SORTED if sorted_units else 0))
-        if kv == "fp8" and schedule in ("persistent", "ws"):
-            raise ValueError("FP8 pools run the fused step on the grid schedule only: no persistent or ws "
-                             "options")
+        self.attn_options = pkv.PKV_DECODE_SPLIT_MERGE | variant if split_merge else self.step_options
         self.bt = None
         self.bt_host = None
         self.chains = chains
         self.chain_bounds = chain_bounds(batch, chains)
-        # each chain has its own stream and its own step workspace (counters start at zero)
+        # each chain has its own stream and its own workspace (counters start at zero)
         self.chain_streams = [torch.cuda.Stream(device=self.device) for _ in range(chains)] if chains > 1 else []
         self.chain_ws = [torch.zeros(self.step_ws_bytes, dtype=torch.uint8, device=self.device)
                          for _ in range(chains)] if chains > 1 else []
@@ -126,14 +123,22 @@ class DecodeEngine:
             pass
 
     # ------------------------------------------------------------------ step
-    def append(self, layer: int, k_new, v_new, q, pos_dev, stream=None) -> None:
-        pkv.pkv_append_rope(self.pool, k_new, v_new, q, self.bt[layer], self.max_blocks, pos_dev, self.batch,
-                            self.rope, self.max_pos, self.err, stream)
+    def append(self, layer: int, k_new, v_new, q, pos_dev, stream=None, rows=None) -> None:
+        """pkv_append_rope of one layer (rows r0..r1-1 with ``rows=(r0, r1)``)."""
+        r0, r1 = rows if rows is not None else (0, self.batch)
+        pkv.pkv_append_rope(self.pool, k_new[r0:r1], v_new[r0:r1], q[r0:r1], self.bt[layer, r0:r1], self.max_blocks,
+                            pos_dev[r0:r1], r1 - r0, self.rope, self.max_pos, self.err, stream)
 
-    def attention(self, layer: int, q, seq_lens_dev, out, stream=None, variant=None) -> None:
-        pkv.pkv_decode_attention_variant(self.pool, q, self.bt[layer], self.max_blocks, seq_lens_dev, self.batch,
-                                         self.scale, self.pages_per_chunk, self.workspace, self.ws_bytes, out,
-                                         self.err, stream, self.variant if variant is None else variant)
+    def attention(self, layer: int, q, seq_lens_dev, out, stream=None, variant=None, rows=None,
+                  workspace=None) -> None:
+        """pkv_decode_attention(_variant) of one layer with the engine's attention options
+        (or ``variant``); rows and workspace as for ``fused_layer``."""
+        r0, r1 = rows if rows is not None else (0, self.batch)
+        pkv.pkv_decode_attention_variant(self.pool, q[r0:r1], self.bt[layer, r0:r1], self.max_blocks,
+                                         seq_lens_dev[r0:r1], r1 - r0, self.scale, self.pages_per_chunk,
+                                         self.workspace if workspace is None else workspace, self.ws_bytes,
+                                         out[r0:r1], self.err, stream,
+                                         self.attn_options if variant is None else variant)
 
     def fused_layer(self, layer: int, q, k_new, v_new, seq_lens_dev, out, stream=None, rows=None,
                     workspace=None) -> None:
@@ -162,19 +167,36 @@ class DecodeEngine:
                                    out[0, r0:r1], self.err, stream, self.step_options, k_new.stride(0),
                                    q.stride(0), self.bt.stride(0))
 
-    def _step_chains(self, q, k_new, v_new, seq_lens_dev, out, stream=None, layer_hook=None) -> None:
-        """The fused step as micro-batch chains.  Each chain waits for the caller's stream,
-        runs its layers on its own stream, and the caller's stream waits for every chain.
-        With a ``layer_hook`` the chains run one after another on the caller's stream
-        instead, so that the hook's events bracket one launch each."""
+    def _rows_layers(self, q, k_new, v_new, pos_dev, seq_lens_dev, out, stream, rows, ws, layer_hook=None) -> None:
+        """Every layer for batch rows ``rows`` on ``stream``: one fused launch per layer, or
+        (separate path) pkv_append_rope then pkv_decode_attention.  ``layer_hook(layer, phase)``
+        is called around each attention launch."""
+        if self.fused and layer_hook is None:
+            self.fused_layers(q, k_new, v_new, seq_lens_dev, out, stream, rows, ws)
+            return
+        for layer in range(self.layers):
+            if not self.fused:
+                self.append(layer, k_new[layer], v_new[layer], q[layer], pos_dev, stream, rows)
+            if layer_hook:
+                layer_hook(layer, "before")
+            if self.fused:
+                self.fused_layer(layer, q[layer], k_new[layer], v_new[layer], seq_lens_dev, out[layer], stream,
+                                 rows, ws)
+            else:
+                self.attention(layer, q[layer], seq_lens_dev, out[layer], stream, rows=rows, workspace=ws)
+            if layer_hook:
+                layer_hook(layer, "after")
+
+    def _step_chains(self, q, k_new, v_new, pos_dev, seq_lens_dev, out, stream=None, layer_hook=None) -> None:
+        """The step as micro-batch chains.  Each chain waits for the caller's stream, runs
+        its layers on its own stream, and the caller's stream waits for every chain.  With
+        a ``layer_hook`` the chains run one after another on the caller's stream instead, so
+        that the hook's events bracket one launch each."""
         groups = list(zip(self.chain_bounds[:-1], self.chain_bounds[1:]))
         if layer_hook is not None:
             for k, rows in enumerate(groups):
-                for layer in range(self.layers):
-                    layer_hook(layer, "before")
-                    self.fused_layer(layer, q[layer], k_new[layer], v_new[layer], seq_lens_dev, out[layer], stream,
-                                     rows, self.chain_ws[k])
-                    layer_hook(layer, "after")
+                self._rows_layers(q, k_new, v_new, pos_dev, seq_lens_dev, out, stream, rows, self.chain_ws[k],
+                                  layer_hook)
             return
         cur = torch.cuda.current_stream(self.device) if stream is None else stream
         fork = torch.cuda.Event()
@@ -183,7 +205,7 @@ class DecodeEngine:
         for k, rows in enumerate(groups):
             s = self.chain_streams[k]
             s.wait_event(fork)
-            self.fused_layers(q, k_new, v_new, seq_lens_dev, out, s, rows, self.chain_ws[k])
+            self._rows_layers(q, k_new, v_new, pos_dev, seq_lens_dev, out, s, rows, self.chain_ws[k])
             done = torch.cuda.Event()
             done.record(s)
             joins.append(done)
@@ -200,26 +222,10 @@ class DecodeEngine:
         torch.cuda.Stream or None (the current stream).
         ``layer_hook(layer, phase)`` (optional) is called around each attention launch.
         """
-        if self.fused and self.chains > 1:
-            self._step_chains(q, k_new, v_new, seq_lens_dev, out, stream, layer_hook)
+        if self.chains > 1:
+            self._step_chains(q, k_new, v_new, pos_dev, seq_lens_dev, out, stream, layer_hook)
             return
-        if self.fused and layer_hook is None:
-            self.fused_layers(q, k_new, v_new, seq_lens_dev, out, stream)
-            return
-        for layer in range(self.layers):
-            if self.fused:
-                if layer_hook:
-                    layer_hook(layer, "before")
-                self.fused_layer(layer, q[layer], k_new[layer], v_new[layer], seq_lens_dev, out[layer], stream)
-                if layer_hook:
-                    layer_hook(layer, "after")
-                continue
-            self.append(layer, k_new[layer], v_new[layer], q[layer], pos_dev, stream)
-            if layer_hook:
-                layer_hook(layer, "before")
-            self.attention(layer, q[layer], seq_lens_dev, out[layer], stream)
-            if layer_hook:
-                layer_hook(layer, "after")
+        self._rows_layers(q, k_new, v_new, pos_dev, seq_lens_dev, out, stream, None, self.step_ws, layer_hook)
 
     def run_host(self, io: "PackedIO", out_dev, out_host, stream=None) -> None:
         """End-to-end step: one copy of the step's inputs (q, k_new, v_new, pos, seq_lens, packed

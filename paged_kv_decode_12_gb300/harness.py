@@ -37,20 +37,21 @@ class DeviceWorkload:
 
 def setup(name: str, seed: int = wl.DEFAULT_SEED, pages_per_chunk: int = 16,
           variant: int = pkv.PKV_DECODE_DEFAULT, layers: int | None = None, device: str = "cuda",
-          fused: bool = True, pdl: bool = True, schedule: str = "auto", ring: int = 0,
-          early_trigger: bool = False, kv: str = "bf16", sorted_units: bool = False,
-          chains: int = 1) -> DeviceWorkload:
+          fused: bool = True, pdl: bool = True, ring: int = 0, kv: str = "bf16", sorted_units: bool = False,
+          chains: int = 1, split_merge: bool = False) -> DeviceWorkload:
     """Build the named workload on the GPU: pool filled with N(0,1) BF16 (plus the
     key outliers of ``b64``) or, with ``kv="fp8"``, with FP8 pages drawn by
     ``workloads.fill_fp8_pages_``; block tables from the library's seeded
     allocator, per-layer q / k_new / v_new draws, positions = lengths - 1.
-    ``chains`` > 1 runs the fused step as that many micro-batch chains (see engine)."""
+    ``chains`` > 1 runs the step as that many micro-batch chains (see engine); ``fused=False``
+    runs pkv_append_rope + pkv_decode_attention per layer (``split_merge``: the two-kernel
+    attention form)."""
     w = wl.make_workload(name, seed)
     if layers is not None and layers != w.layers:
         w = dataclasses.replace(w, layers=layers, pool_pages=w.pool_pages * layers // w.layers)
     eng = DecodeEngine(w.pool_pages, w.layers, w.batch, w.max_blocks, pages_per_chunk, variant, pool_seed=seed,
-                       device=device, fused=fused, pdl=pdl, schedule=schedule, ring=ring,
-                       early_trigger=early_trigger, kv=kv, sorted_units=sorted_units, chains=chains)
+                       device=device, fused=fused, pdl=pdl, ring=ring, kv=kv, sorted_units=sorted_units,
+                       chains=chains, split_merge=split_merge)
     if kv == "fp8":
         codes, scales = eng.fp8_views()
         wl.fill_fp8_pages_(codes, scales, seed, w.key_outlier_frac)
@@ -77,13 +78,21 @@ def setup(name: str, seed: int = wl.DEFAULT_SEED, pages_per_chunk: int = 16,
 
 
 def kernels_per_step(dw: DeviceWorkload) -> int:
-    """Library kernel launches in one step: per layer one fused kernel (BF16 or FP8
-    pages) per micro-batch chain, or (separate path) the append, the split kernel and,
-    when a sequence can span several chunks, the merge."""
-    if dw.eng.fused:
-        return dw.w.layers * dw.eng.chains
-    merge = 1 if (dw.w.max_blocks + dw.eng.pages_per_chunk - 1) // dw.eng.pages_per_chunk > 1 else 0
-    return dw.w.layers * (2 + merge)
+    """Library kernel launches in one step, per layer and micro-batch chain: one fused
+    kernel (BF16 or FP8 pages), or (separate path) the append and the attention kernel
+    (two-kernel form: the split kernel and, when a sequence can span several chunks,
+    the merge kernel)."""
+    per_layer = 1
+    if not dw.eng.fused:
+        two_kernel = bool(dw.eng.attn_options & pkv.PKV_DECODE_SPLIT_MERGE)
+        multi = (dw.w.max_blocks + dw.eng.pages_per_chunk - 1) // dw.eng.pages_per_chunk > 1
+        per_layer = 2 + (1 if two_kernel and multi else 0)
+    return dw.w.layers * dw.eng.chains * per_layer
+
+
+def attention_launches_per_step(dw: DeviceWorkload) -> int:
+    """Attention launches (the dominant kernel) in one step: one per layer and chain."""
+    return dw.w.layers * dw.eng.chains
 
 
 def external_events_supported() -> bool:

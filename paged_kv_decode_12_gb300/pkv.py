@@ -43,11 +43,10 @@ PKV_DECODE_SIMT = 1
 PKV_DECODE_MMA = 2
 PKV_STEP_NO_PDL = 0x100
 PKV_STEP_GRID = 0x200
-PKV_STEP_PERSISTENT = 0x400
-PKV_STEP_WS = 0x800
 PKV_STEP_RING_MASK = 0xF000
-PKV_STEP_EARLY_TRIGGER = 0x10000
 PKV_STEP_SORTED = 0x20000
+PKV_STEP_TEST_EXPIRE_WAIT = 0x40000
+PKV_DECODE_SPLIT_MERGE = 0x80000
 
 
 def PKV_STEP_RING(n: int) -> int:

@@ -146,11 +146,16 @@ def test_block_tables_seeded_and_all_or_nothing():
 
 
 def test_workspace_bytes():
-    # B x 32 heads x chunks x (m, l) floats, 256-aligned, then x 64 floats of o
-    ws = pkv.pkv_decode_workspace_bytes(256, 128, 16)
-    chunks = 8
-    ml = 256 * 32 * chunks * 8
-    assert ws == ((ml + 255) // 256) * 256 + 256 * 32 * chunks * 64 * 4
+    # B x 8 merge counters, then B x 32 heads x chunks x (m, l) floats, each 256-aligned,
+    # then x 64 floats of o; the fused step uses the same layout
+    def align(x):
+        return (x + 255) // 256 * 256
+
+    for B, max_blocks, ppc in ((256, 128, 16), (3, 100, 7), (1, 1, 1)):
+        chunks = -(-max_blocks // ppc)
+        want = align(B * 8 * 4) + align(B * 32 * chunks * 8) + B * 32 * chunks * 64 * 4
+        assert pkv.pkv_decode_workspace_bytes(B, max_blocks, ppc) == want
+        assert pkv.pkv_decode_step_workspace_bytes(B, max_blocks, ppc) == want
     assert pkv.pkv_decode_workspace_bytes(0, 128, 16) == 0
 
 
@@ -166,10 +171,13 @@ def test_launch_entry_points_validate_before_any_cuda_call():
     with pytest.raises(pkv.PkvError) as e:     # workspace too small
         pkv.pkv_decode_attention(p, dummy, dummy, 128, dummy, 4, 0.125, 16, dummy, 64, dummy, None, 0)
     assert e.value.status == pkv.PKV_ERR_WORKSPACE_TOO_SMALL
-    with pytest.raises(pkv.PkvError) as e:     # unknown variant
-        pkv.pkv_decode_attention_variant(p, dummy, dummy, 128, dummy, 4, 0.125, 16, dummy, 1 << 20, dummy, None,
-                                         0, variant=9)
-    assert e.value.status == pkv.PKV_ERR_INVALID_ARG
+    for variant in (9, 0x400, 0x800, 0x10000, pkv.PKV_DECODE_SPLIT_MERGE | pkv.PKV_STEP_SORTED,
+                    pkv.PKV_DECODE_SPLIT_MERGE | pkv.PKV_STEP_TEST_EXPIRE_WAIT, pkv.PKV_STEP_RING(1),
+                    pkv.PKV_STEP_RING(5)):
+        with pytest.raises(pkv.PkvError) as e:     # unknown variant or option
+            pkv.pkv_decode_attention_variant(p, dummy, dummy, 128, dummy, 4, 0.125, 16, dummy, 1 << 20, dummy,
+                                             None, 0, variant=variant)
+        assert e.value.status == pkv.PKV_ERR_INVALID_ARG, hex(variant)
     with pytest.raises(pkv.PkvError) as e:     # misaligned k_new
         pkv.pkv_append_rope(p, dummy + 2, dummy, None, dummy, 128, dummy, 4, dummy, 2048, None, 0)
     assert e.value.status == pkv.PKV_ERR_INVALID_ARG
@@ -210,20 +218,22 @@ def test_fp8_pool_rejects_unsupported_options_before_any_cuda_call():
                                          0, variant=pkv.PKV_DECODE_SIMT)
     assert e.value.status == pkv.PKV_ERR_UNSUPPORTED
     ws = pkv.pkv_decode_step_workspace_bytes(4, 128, 16)
-    for opt in (pkv.PKV_STEP_PERSISTENT, pkv.PKV_STEP_WS, pkv.PKV_DECODE_SIMT):
-        with pytest.raises(pkv.PkvError) as e:
-            pkv.pkv_decode_step(p, dummy, dummy, dummy, dummy, 128, dummy, 4, dummy, 2048, 0.125, 16, dummy, ws,
-                                dummy, None, 0, options=opt)
-        assert e.value.status == pkv.PKV_ERR_UNSUPPORTED, hex(opt)
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.pkv_decode_step(p, dummy, dummy, dummy, dummy, 128, dummy, 4, dummy, 2048, 0.125, 16, dummy, ws,
+                            dummy, None, 0, options=pkv.PKV_DECODE_SIMT)
+    assert e.value.status == pkv.PKV_ERR_UNSUPPORTED
     pkv.pkv_pool_destroy(p)
 
 
-def test_grid_schedule_options_validation_before_any_cuda_call():
+def test_step_options_validation_before_any_cuda_call():
     p = make_pool(8)
     dummy = FAKE_SLAB
     ws = pkv.pkv_decode_step_workspace_bytes(1025, 128, 16)
-    for B, opt in ((1025, pkv.PKV_STEP_SORTED), (4, pkv.PKV_STEP_SORTED | pkv.PKV_STEP_PERSISTENT),
-                   (4, pkv.PKV_STEP_SORTED | pkv.PKV_STEP_WS)):
+    # more sequences than the sorted order handles; bits of schedules that no longer
+    # exist (0x400, 0x800) or of the removed early trigger (0x10000); the two-kernel
+    # attention form is not a step option; ring depths outside 2..4
+    for B, opt in ((1025, pkv.PKV_STEP_SORTED), (4, 0x400), (4, 0x800), (4, 0x10000),
+                   (4, pkv.PKV_DECODE_SPLIT_MERGE), (4, pkv.PKV_STEP_RING(1)), (4, pkv.PKV_STEP_RING(7))):
         with pytest.raises(pkv.PkvError) as e:
             pkv.pkv_decode_step(p, dummy, dummy, dummy, dummy, 128, dummy, B, dummy, 2048, 0.125, 16, dummy, ws,
                                 dummy, None, 0, options=opt)

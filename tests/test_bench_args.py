@@ -41,11 +41,15 @@ def test_explicit_flags_win(captured):
     assert captured["args"].sorted is True
 
 
-def test_separate_path_runs_one_chain(captured):
-    bench.main(["--path", "separate"])
-    assert captured["args"].chains == 1
-    with pytest.raises(SystemExit):
-        bench.main(["--path", "separate", "--chains", "2"])
+def test_separate_path_options(captured):
+    # the separate path (pkv_append_rope + pkv_decode_attention) takes the workload's chains
+    bench.main(["--path", "separate", "--config", "b64"])
+    assert captured["args"].chains == launch.CHAINS["b64"] and not captured["args"].split_merge
+    bench.main(["--path", "separate", "--chains", "2", "--split-merge"])
+    a = captured["args"]
+    assert a.chains == 2 and a.split_merge and a.sorted is False
+    with pytest.raises(SystemExit):     # the two-kernel form belongs to the separate path
+        bench.main(["--split-merge"])
     with pytest.raises(SystemExit):
         bench.main(["--sorted", "--unsorted"])
 

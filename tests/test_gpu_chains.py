@@ -39,11 +39,11 @@ def run(name, kv, chains, graph, steps=2):
     st, flag = dw.eng.check_errors()
     res = dict(status=st, flag=flag, bounds=list(dw.eng.chain_bounds), out=dw.out.cpu().clone(),
                q=dw.q.cpu().clone(), slab=dw.eng.slab.cpu().clone())
-    # a call over B rows keeps B x 8 + 2 counters at the start of its workspace
+    # a call over B rows keeps B x 8 merge counters at the start of its workspace
     ws = dw.eng.chain_ws if chains > 1 else [dw.eng.step_ws]
     rows = np.diff(dw.eng.chain_bounds)
     res["counters_zero"] = all(
-        bool((w[: (int(n) * 8 + 2) * 4].view(torch.int32) == 0).all()) for w, n in zip(ws, rows))
+        bool((w[: int(n) * 8 * 4].view(torch.int32) == 0).all()) for w, n in zip(ws, rows))
     dw.eng.close()
     return res
 

@@ -239,7 +239,7 @@ def fp8_step_run(c, chunk, fused, ring=0, sorted_units=False, pdl=True, repeats=
         out = torch.zeros((1, c["B"], HQ, D), dtype=torch.bfloat16, device="cuda")
         eng.step(q, dev_bf16(c["k_new"])[None], dev_bf16(c["v_new"])[None], lens_d - 1, lens_d, out)
     st, flag = eng.check_errors()
-    counters = eng.step_ws[: (c["B"] * 8 + 2) * 4].view(torch.int32).cpu().numpy()
+    counters = eng.step_ws[: c["B"] * 8 * 4].view(torch.int32).cpu().numpy()
     res = dict(out=u16(out)[0], q=u16(q)[0], pool=eng.slab.cpu().numpy(), status=st, flag=flag, counters=counters)
     eng.close()
     return res

@@ -26,15 +26,15 @@ def native():
     pkv.lib()
 
 
-# "sorted": the grid schedule with units dispatched largest first (PKV_STEP_SORTED)
-SCHEDULES = ["grid", "persistent", "ws", "sorted"]
+# "sorted": units dispatched largest first (PKV_STEP_SORTED); "grid": in grid order
+SCHEDULES = ["grid", "sorted"]
 
 
 def fused_run(c, chunk=16, variant=pkv.PKV_DECODE_DEFAULT, pdl=True, seq_lens_override=None, repeats=1,
               schedule="auto", ring=0):
     sorted_units = schedule == "sorted"
-    eng = DecodeEngine(c["num_pages"], 1, c["B"], c["max_blocks"], chunk, variant, pdl=pdl,
-                       schedule="grid" if sorted_units else schedule, ring=ring, sorted_units=sorted_units)
+    eng = DecodeEngine(c["num_pages"], 1, c["B"], c["max_blocks"], chunk, variant, pdl=pdl, ring=ring,
+                       sorted_units=sorted_units)
     eng.slab.copy_(torch.from_numpy(c["pool"].view(np.uint8)).cuda())
     eng.set_tables(c["bt"][None])
     lens = c["seq_lens"] if seq_lens_override is None else np.asarray(seq_lens_override, np.int32)
@@ -47,7 +47,7 @@ def fused_run(c, chunk=16, variant=pkv.PKV_DECODE_DEFAULT, pdl=True, seq_lens_ov
         eng.fused_layer(0, q, k_new, v_new, lens_d, out)
         outs.append(u16(out))
     status, flag = eng.check_errors()
-    counters = eng.step_ws[: (c["B"] * 8 + 2) * 4].view(torch.int32).cpu().numpy()
+    counters = eng.step_ws[: c["B"] * 8 * 4].view(torch.int32).cpu().numpy()
     res = dict(pool=u16(eng.slab.view(torch.bfloat16)), q=u16(q), out=outs[-1], outs=outs, status=status,
                flag=flag, counters=counters)
     eng.close()
@@ -117,18 +117,17 @@ def test_ring_depth_changes_no_bit(ring):
     assert np.array_equal(a["q"], b["q"]) and np.all(b["counters"] == 0)
 
 
-def test_persistent_many_units_per_cta():
-    # more units than CTAs (batch 300 > 152 SMs x 3 CTAs / 8 heads): every CTA walks
-    # several units, crossing unit boundaries with copies in flight
+def test_sorted_many_units_per_launch():
+    # far more units than resident CTAs (batch 300, 2-page chunks): several waves, the
+    # sorted order covering every unit exactly once
     rng = np.random.default_rng(35)
     lens = rng.integers(1, 300, size=300)
     c = make_case(35, lens, max_blocks=64)
     g = fused_run(c, chunk=2, schedule="grid")
-    for schedule in ("persistent", "ws", "sorted"):
-        p = fused_run(c, chunk=2, schedule=schedule, repeats=2)
-        assert p["status"] == pkv.PKV_OK and np.all(p["counters"] == 0)
-        assert np.array_equal(p["out"], g["out"]) and np.array_equal(p["pool"], g["pool"])
-        assert np.array_equal(p["q"], g["q"])
+    p = fused_run(c, chunk=2, schedule="sorted", repeats=2)
+    assert p["status"] == pkv.PKV_OK and np.all(p["counters"] == 0)
+    assert np.array_equal(p["out"], g["out"]) and np.array_equal(p["pool"], g["pool"])
+    assert np.array_equal(p["q"], g["q"])
 
 
 @pytest.mark.parametrize("chunk", [1, 5, 32])

@@ -69,24 +69,31 @@ def test_prefill_fill_matches_oracle(start, T):
     pkv.pkv_pool_destroy(p)
 
 
-@pytest.mark.parametrize("kv,chains", [("bf16", 1), ("fp8", 1), ("bf16", 3)])
-def test_trace_steps_match_oracle(kv, chains):
+@pytest.mark.parametrize("kv,chains,static", [("bf16", 1, False), ("fp8", 1, False), ("bf16", 3, False),
+                                               ("bf16", 1, True), ("fp8", 1, True)])
+def test_trace_steps_match_oracle(kv, chains, static):
     # The oracle rebuilds each sampled sequence's pages from the raw seeded inputs that
     # went into them -- the prompt K/V draw of its admission and the new K/V row of every
     # step since -- and decodes with the step's unrotated query; nothing the CUDA path
-    # wrote is read back as an oracle input.
+    # wrote is read back as an oracle input.  Static batching (samir-vllm README summary,
+    # "构建": --static; "当前范围": the next group is admitted only after the current one
+    # has finished) runs the same kernels on group-wise batches.
     layers, max_batch = 2, 24
     runner = TraceRunner(pool_pages=3000, layers=layers, max_batch=max_batch, pages_per_chunk=4, seed=5, kv=kv,
-                         chains=chains)
+                         chains=chains, static=static)
     fp8 = kv == "fp8"
-    reqs = wl.trace_schedule(seed=5, steps=60, arrival_rate=0.8, prompt_lo=8, prompt_hi=200, out_lo=4, out_hi=60)
+    # static groups live as long as their longest member: shorter budgets let several groups run
+    reqs = wl.trace_schedule(seed=5, steps=60, arrival_rate=0.8, prompt_lo=8, prompt_hi=200, out_lo=4,
+                             out_hi=25 if static else 60)
     rng = np.random.default_rng(9)
     check_steps = {3, 17, 31, 45, 59}
     k_new, v_new, q0 = u16(runner.k_new), u16(runner.v_new), u16(runner.q0)
     history = {}   # request id -> [(position, batch slot)] of its decode tokens so far
     pending = {}
+    batches = []   # the ids of every non-empty decode batch, in step order
 
     def before(step, ids, lens, bt):
+        batches.append(set(ids.tolist()))
         for b, rid in enumerate(ids.tolist()):
             history.setdefault(rid, []).append((int(lens[b]) - 1, b))
         if step in check_steps:
@@ -129,4 +136,13 @@ def test_trace_steps_match_oracle(kv, chains):
     assert s["max_decode_batch"] == max(res.batch_sizes) and s["peak_active"] >= s["max_decode_batch"]
     assert s["allocated_pages"] + s["final_free_pages"] == s["pool_pages"]
     assert res.decode_steps > 0 and res.tokens == sum(res.batch_sizes)
+    # admission: under static batching a batch either continues the previous group (its
+    # ids a subset: members only finish) or is a whole new group (no id in common);
+    # continuous batching admits into a running batch, so some batch mixes the two
+    mixed = [bool(a & b) and not b <= a for a, b in zip(batches, batches[1:])]
+    if static:
+        assert not any(mixed)
+        assert sum(1 for a, b in zip(batches, batches[1:]) if not (a & b)) >= 1   # a second group ran
+    else:
+        assert any(mixed)
     runner.close()
