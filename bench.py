@@ -4,8 +4,9 @@
 A *step* is one decode step of the 16-layer engine's attention hot path: for
 every layer, the RoPE + page-slot append of each sequence's new token, then
 paged GQA decode attention over the sequence's pages with the log-sum-exp merge
-of its chunks -- by default one fused kernel per layer (``--path separate``:
-append, split and merge launches).  Default workload ``b256``: batch 256, every sequence at 2,048 tokens
+of its chunks -- by default one fused kernel per layer (``--path separate``: the
+two named calls, pkv_append_rope then pkv_decode_attention; ``--split-merge``:
+the attention's two-kernel form).  Default workload ``b256``: batch 256, every sequence at 2,048 tokens
 (128 pages per sequence and layer), 32 query / 8 KV heads, head_dim 64, BF16 KV
 pool of 524,288 pages (16 GiB).  Other workloads: ``--config b64`` (log-normal
 lengths, median 300) and ``--config b8`` (uniform lengths).
@@ -17,6 +18,13 @@ bracketed by external timing events; these give the dominant kernel's average
 duration for the roofline (the step time itself comes from uninstrumented
 graphs, since an event between two launches would serialise their programmatic
 dependent launch).
+
+The default run also measures further configurations (``--extra``: the ragged
+batch 64, batch 8, the separate calls on batch 64, FP8 pages on batch 64 and
+256) and reports them under ``configs``; a read-only HBM probe gives the
+streaming ceiling the fractions are also reported against.  The CPU baseline is
+the FP64 oracle on the GPU batch's own inputs, single-threaded and on every
+host core.
 
 ``--impl reference`` times the FP64 CPU oracle on a bounded sample of the same
 workload on the host cores (the reference arm; it runs none of the CUDA path).
@@ -178,7 +186,7 @@ def kernel_source_digest() -> str:
 
 
 def measured_traffic(config: str, path: str, variant_name: str, pages_per_chunk: int, ring: int,
-                     kv: str = "bf16", chains: int = 1, sorted_units: bool = False):
+                     kv: str = "bf16", chains: int = 1, sorted_units: bool = False, split_merge: bool = False):
     """DRAM bytes per attention launch from the committed ncu summary
     (profiles/decode_traffic.json), if it was taken on the current kernel source;
     else None."""
@@ -192,18 +200,26 @@ def measured_traffic(config: str, path: str, variant_name: str, pages_per_chunk:
         if (e.get("config") == config and e.get("path") == path and e.get("variant") == variant_name and
                 e.get("pages_per_chunk") == pages_per_chunk and e.get("ring", 4) == ring and
                 e.get("kv", "bf16") == kv and e.get("chains", 1) == chains and
-                e.get("sorted_units", False) == sorted_units and
+                e.get("sorted_units", False) == sorted_units and e.get("split_merge", False) == split_merge and
                 e.get("kernel_source_sha") == digest):
             return e.get("dram_bytes_per_launch")
     return None
 
 
-# --------------------------------------------------------------------------- CPU oracle sample
+# --------------------------------------------------------------------------- CPU oracle baseline
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
 
 def oracle_samples(w, n_seqs: int, seed: int, kv: str = "bf16"):
     """Host-side synthetic inputs for ``n_seqs`` sequences of one layer of workload ``w``
     (same length mix), each in its own small paged pool (FP8 pools: codes drawn as for the
-    GPU workloads, N(0, 128^2) converted to E4M3, row scales uniform in [0.005, 0.009])."""
+    GPU workloads, N(0, 128^2) converted to E4M3, row scales uniform in [0.005, 0.009]).
+    The reference arm uses these: it runs on the host cores only."""
     import oracle
     from paged_kv_decode_12_gb300 import workloads as wl
 
@@ -231,58 +247,162 @@ def oracle_samples(w, n_seqs: int, seed: int, kv: str = "bf16"):
     return out
 
 
-def oracle_run_sample(sample, kv: str = "bf16") -> int:
-    """One oracle pass (append + attention, all 32 heads) over each sampled sequence;
+# (layers, sequences) of the GPU batch the CPU baseline runs, per workload: whole steps
+# where the oracle finishes them in seconds, else a stated fraction of one step
+CPU_SAMPLE = {"tiny": (None, None), "b8": (None, None), "b64": (1, None), "b256": (1, 32)}
+
+
+def gpu_batch_sample(dw, kv: str):
+    """Oracle inputs copied from the GPU batch itself (so the CPU baseline runs the very
+    inputs the GPU step runs): per (layer, sequence) of ``CPU_SAMPLE``, the sequence's
+    pages from the device pool, its block-table row renumbered into that small pool, and
+    its unrotated q, k_new, v_new rows.  Returns (samples, fraction of one step)."""
+    import torch
+
+    from paged_kv_decode_12_gb300 import workloads as wl
+
+    w = dw.w
+    n_layers, n_seqs = CPU_SAMPLE.get(w.name, (1, 8))
+    layers = range(w.layers if n_layers is None else min(n_layers, w.layers))
+    seqs = range(w.batch if n_seqs is None else min(n_seqs, w.batch))
+    page_bytes = dw.eng.page_bytes
+    pages_view = dw.eng.slab.view(dw.eng.num_pages, page_bytes)
+    q0, k_new, v_new = (t.view(torch.int16).cpu().numpy().view(np.uint16) for t in (dw.q0, dw.k_new, dw.v_new))
+    out = []
+    for l in layers:
+        for b in seqs:
+            L = int(w.seq_lens[b])
+            npg = -(-L // wl.PAGE_SIZE)
+            ids = torch.from_numpy(dw.eng.bt_host[l, b, :npg].astype(np.int64)).to(pages_view.device)
+            mini = pages_view[ids].cpu().numpy().reshape(-1)
+            pool = mini.copy() if kv == "fp8" else mini.view(np.uint16).copy()
+            bt = np.full((1, w.max_blocks), -1, dtype=np.int32)
+            bt[0, :npg] = np.arange(npg)
+            out.append(dict(L=L, npg=npg, pool=pool, bt=bt, q=q0[l, b][None].copy(), k_new=k_new[l, b][None].copy(),
+                            v_new=v_new[l, b][None].copy()))
+    frac = len(out) / (w.layers * w.batch)
+    return out, frac
+
+
+def oracle_run_one(s, kv: str = "bf16") -> int:
+    """One oracle pass (append + attention, all 32 heads) over one sampled sequence;
     returns the KV tokens attended."""
     import oracle
     from paged_kv_decode_12_gb300 import workloads as wl
 
     append, decode = (oracle.append_fp8, oracle.decode_fp8) if kv == "fp8" else (oracle.append, oracle.decode)
-    tokens = 0
-    for s in sample:
-        g = oracle.geom(s["npg"])
-        q = s["q"].copy()
-        append(s["pool"], g, s["bt"], [s["L"] - 1], s["k_new"], s["v_new"], q)
-        decode(s["pool"], g, s["bt"], [s["L"]], q, 1.0 / math.sqrt(wl.HEAD_DIM))
-        tokens += s["L"]
-    return tokens
+    g = oracle.geom(s["npg"])
+    q = s["q"].copy()
+    append(s["pool"], g, s["bt"], [s["L"] - 1], s["k_new"], s["v_new"], q)
+    decode(s["pool"], g, s["bt"], [s["L"]], q, 1.0 / math.sqrt(wl.HEAD_DIM))
+    return s["L"]
 
 
-def cpu_baseline(w, seconds: float, seed: int, kv: str = "bf16") -> dict:
+def oracle_run_sample(sample, kv: str = "bf16", threads: int = 1) -> int:
+    """Every sampled sequence once, on ``threads`` host threads (the C oracle releases the
+    interpreter lock, and each sequence has its own pages); returns the KV tokens attended."""
+    if threads <= 1:
+        return sum(oracle_run_one(s, kv) for s in sample)
+    import concurrent.futures
+
+    with concurrent.futures.ThreadPoolExecutor(max_workers=threads) as ex:
+        return sum(ex.map(lambda s: oracle_run_one(s, kv), sample))
+
+
+def time_oracle(sample, kv: str, threads: int, min_seconds: float):
+    """Whole passes over the sample until ``min_seconds`` have elapsed: (KV GB/s, passes, s)."""
     from paged_kv_decode_12_gb300 import workloads as wl
 
     per_token = wl.kv_bytes_per_token(1, kv=kv)
-    pool = oracle_samples(w, 64, seed, kv)
-    tokens, seqs = 0, 0
+    tokens, passes = 0, 0
     t0 = time.perf_counter()
-    while time.perf_counter() - t0 < seconds:       # cycle over the prepared sample
-        tokens += oracle_run_sample([pool[seqs % len(pool)]], kv)
-        seqs += 1
-    dt = time.perf_counter() - t0
-    return {"value": tokens * per_token / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{seqs} sequences of one layer ({tokens} KV tokens): append + attention for all 32 "
-                      f"query heads, FP64, single thread, {dt:.1f} s"}
+    while True:
+        tokens += oracle_run_sample(sample, kv, threads)
+        passes += 1
+        dt = time.perf_counter() - t0
+        if dt >= min_seconds:
+            return tokens * per_token / dt / 1e9, passes, dt
 
 
-# --------------------------------------------------------------------------- arms
+def cpu_baseline(dw, seconds: float, kv: str = "bf16") -> dict:
+    """The FP64 oracle on the host cores, on the GPU batch's own inputs: single-threaded and
+    with one thread per host core; ``value`` is the all-cores figure."""
+    sample, frac = gpu_batch_sample(dw, kv)
+    cores = host_cores()
+    one, n1, t1 = time_oracle(sample, kv, 1, seconds * 0.5)
+    many, nn, tn = time_oracle(sample, kv, cores, seconds * 0.5)
+    w = dw.w
+    what = (f"{len(sample)} (layer, sequence) pairs of the GPU batch ({frac:.4g} of one {w.layers}-layer step of "
+            f"{w.name}; {sum(s['L'] for s in sample)} KV tokens): append + attention for all 32 query heads, "
+            f"FP64 C oracle on the inputs the GPU step runs")
+    return {"value": many, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{what}; {nn} passes on {cores} threads in {tn:.1f} s",
+            "fraction_of_step": frac, "host_cores": cores,
+            "single_thread": {"value": one, "unit": "GB/s", "cores": 1,
+                              "sample": f"{n1} passes on one thread in {t1:.1f} s"}}
 
-def config_block(w, args, variant_name: str, graph: bool) -> dict:
-    kv = w.kv_bytes_per_step(getattr(args, "kv", "bf16"))
-    return {"workload": f"{args.config}: {CONFIG_TEXT[args.config]}", "batch": w.batch, "layers": w.layers,
+
+# --------------------------------------------------------------------------- read-only HBM ceiling
+
+def read_ceiling(device, gib: int = 4, reps: int = 5) -> dict:
+    """Best read-only streaming rate of the device's HBM: libpkv's two read probes (16-byte
+    loads; TMA bulk copies into shared memory) over a buffer far larger than L2, each at a
+    few CTA counts, CUDA events on the launching stream, best of ``reps``."""
+    import torch
+
+    from paged_kv_decode_12_gb300 import pkv
+
+    nbytes = gib << 30
+    buf = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    buf.random_(0, 256)
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    sink = torch.zeros(sms * 4 + 1, dtype=torch.int32, device=device)
+    results = {}
+    for name, fn, ctas in (("ldg", pkv.pkv_probe_read_ldg, (1, 2, 4)), ("bulk", pkv.pkv_probe_read_bulk, (1, 2))):
+        for c in ctas:
+            fn(buf, nbytes, sink, c)   # warm
+            best = 0.0
+            for _ in range(reps):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                fn(buf, nbytes, sink, c)
+                b.record()
+                torch.cuda.synchronize()
+                best = max(best, nbytes / (a.elapsed_time(b) / 1e3) / 1e9)
+            results[f"{name}_{c}"] = best
+    if int(sink[-1].item()) != 0:
+        raise SystemExit("read probe: a bounded wait gave up")
+    del buf
+    torch.cuda.empty_cache()
+    top = max(results, key=results.get)
+    return {"gbs": results[top], "best_probe": top, "probes": results,
+            "how": f"libpkv read probes over {gib} GiB (16-byte loads; TMA bulk copies of 32 KiB), best of {reps} "
+                   "per probe and CTA count, CUDA events"}
+
+
+NOMINAL_HBM_GBS = 7900.0   # GB300 HBM3e, nominal
+
+
+def config_block(w, a, variant_name: str, graph: bool) -> dict:
+    """The ``config`` object of a JSON line; ``a`` holds one run's launch settings."""
+    kv = w.kv_bytes_per_step(getattr(a, "kv", "bf16"))
+    return {"workload": f"{a.config}: {CONFIG_TEXT[a.config]}", "batch": w.batch, "layers": w.layers,
             "seq_len_max": int(w.seq_lens.max()), "seq_len_mean": float(w.seq_lens.mean()),
-            "pages_per_chunk": args.pages_per_chunk, "kernel_variant": variant_name, "cuda_graph": graph,
-            "path": getattr(args, "path", "fused"), "pdl": not getattr(args, "no_pdl", False),
-            "ring": getattr(args, "ring", 0), "sorted_units": getattr(args, "sorted", False),
-            "split_merge": getattr(args, "split_merge", False),
-            "chains": getattr(args, "chains", 1),
-            "steps_per_graph": getattr(args, "steps_per_graph", None) if graph else None,
-            "kv_pages": getattr(args, "kv", "bf16"),
+            "pages_per_chunk": a.pages_per_chunk, "kernel_variant": variant_name, "cuda_graph": graph,
+            "path": getattr(a, "path", "fused"), "pdl": not getattr(a, "no_pdl", False),
+            "ring": getattr(a, "ring", 0), "sorted_units": getattr(a, "sorted", False),
+            "split_merge": getattr(a, "split_merge", False),
+            "chains": getattr(a, "chains", 1),
+            "steps_per_graph": getattr(a, "steps_per_graph", None) if graph else None,
+            "kv_pages": getattr(a, "kv", "bf16"),
             "kv_bytes_per_step": kv,
             "l2": f"inputs larger than L2 ({kv / 1e9:.2f} GB of KV per step vs {L2_BYTES / 1e6:.0f} MB L2), "
-                  "no flush", "seed": args.seed}
+                  "no flush", "seed": a.seed}
 
 
 def run_reference(args):
+    """The reference arm: the FP64 oracle, as it stands, on the host cores (one thread per
+    core), over a bounded sample of the workload per step (the pages ship no code)."""
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
@@ -292,24 +412,25 @@ def run_reference(args):
     if args.layers:
         w.layers = args.layers
     per_token = wl.kv_bytes_per_token(1, kv=args.kv)
+    cores = host_cores()
     sample = oracle_samples(w, args.ref_seqs, args.seed, args.kv)
     for _ in range(args.warmup):
-        oracle_run_sample(sample, args.kv)
+        oracle_run_sample(sample, args.kv, cores)
     times = []
     tokens = 0
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        tokens = oracle_run_sample(sample, args.kv)
+        tokens = oracle_run_sample(sample, args.kv, cores)
         times.append(time.perf_counter() - t0)
     dt = sum(times)
     value = tokens * per_token * args.steps / dt / 1e9
-    desc = (f"{len(sample)} sequences of one layer per step ({tokens} KV tokens): append + attention for all "
-            f"32 query heads, FP64 C oracle, single thread")
+    desc = (f"{len(sample)} sequences of one layer per step ({tokens} KV tokens) drawn like the {w.name} workload: "
+            f"append + attention for all 32 query heads, FP64 C oracle, {cores} host threads")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": config_block(w, args, "oracle", False),
-            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": desc},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -382,38 +503,58 @@ def run_trace(args):
     return 0
 
 
-def run_pkv(args):
+def run_settings(args, config: str, kv: str = "bf16", path: str = "fused", split_merge: bool = False,
+                 steps: int | None = None):
+    """Launch settings of one measured configuration: the workload's measured defaults
+    (launch table), or the command line's for the headline configuration."""
+    a = argparse.Namespace(**vars(args))
+    if config != args.config or kv != args.kv or path != args.path or split_merge != args.split_merge:
+        a.config, a.kv, a.path, a.split_merge = config, kv, path, split_merge
+        a.pages_per_chunk = DEFAULT_CHUNK[config]
+        a.ring = (DEFAULT_RING if kv == "bf16" else DEFAULT_RING_FP8)[config]
+        a.sorted = DEFAULT_SORTED[config] and not split_merge
+        a.chains = (DEFAULT_CHAINS if kv == "bf16" else DEFAULT_CHAINS_FP8)[config]
+        a.no_pdl = False
+    if steps is not None:
+        a.steps = steps
+    return a
+
+
+def kernel_label(a, variant_name: str) -> str:
+    if a.path == "fused":
+        return ("fused decode step kernel over FP8 pages (append + quantize + attention + merge)" if a.kv == "fp8"
+                else f"fused decode step kernel (append + attention + merge), variant {variant_name}")
+    if a.split_merge:
+        return f"pkv_decode_attention two-kernel form (split kernel + LSE merge kernel), variant {variant_name}"
+    return f"pkv_decode_attention kernel (attention + in-kernel LSE merge), variant {variant_name}"
+
+
+def measure(a, rank, world, device, peak, peak_src, read_peak, with_cpu: bool):
+    """Set up one configuration, time ``a.steps`` steps (CUDA graphs, events on the caller's
+    stream), the dominant kernel per launch, the end-to-end form and (optionally) the CPU
+    oracle on the same inputs.  Returns (line fields, DeviceWorkload closed)."""
     import torch
 
     from paged_kv_decode_12_gb300 import harness, pkv
 
-    rank, world, local = dist_env()
-    if not torch.cuda.is_available():
-        raise SystemExit("bench.py needs a CUDA GPU (the CUDA path has no CPU fallback)")
-    torch.cuda.set_device(local)
-    device = torch.device("cuda", local)
-    if world > 1:
-        import torch.distributed as dist
-
-        dist.init_process_group("nccl", device_id=device)
-
-    variant_name = args.variant
-    dw = harness.setup(args.config, replica_seed(args.seed, rank), args.pages_per_chunk, VARIANTS[variant_name],
-                       layers=args.layers, fused=args.path == "fused", pdl=not args.no_pdl, ring=args.ring,
-                       kv=args.kv, sorted_units=args.sorted, chains=args.chains, split_merge=args.split_merge)
+    variant_name = a.variant
+    dw = harness.setup(a.config, replica_seed(a.seed, rank), a.pages_per_chunk, VARIANTS[variant_name],
+                       layers=a.layers, fused=a.path == "fused", pdl=not a.no_pdl, ring=a.ring, kv=a.kv,
+                       sorted_units=a.sorted, chains=a.chains, split_merge=a.split_merge)
     w = dw.w
+    cpu = cpu_baseline(dw, a.cpu_seconds, a.kv) if with_cpu else None
     harness.warm(dw, 2)
     dw.reset_q()
     ext = harness.external_events_supported()
-    per_graph = max(1, min(args.steps, args.steps_per_graph))
-    warm_cap = harness.capture_steps(dw, max(1, min(args.warmup, per_graph)))
+    per_graph = max(1, min(a.steps, a.steps_per_graph))
+    warm_cap = harness.capture_steps(dw, max(1, min(a.warmup, per_graph)))
 
     # The timed steps replay one captured graph of per_graph steps (plus one graph for the
     # remainder): a serving loop replays the same graph every step, and many distinct graph
     # instances of thousands of nodes each (micro-batch chains) cost the device time to
     # switch between.  The step time comes from these plain graphs: a timing event between
     # two launches would turn their programmatic (overlapping) dependency into a full one.
-    n_full, rem = divmod(args.steps, per_graph)
+    n_full, rem = divmod(a.steps, per_graph)
     timed = [harness.capture_steps(dw, per_graph)] * n_full
     if rem:
         timed.append(harness.capture_steps(dw, rem))
@@ -426,9 +567,8 @@ def run_pkv(args):
     for cap in {id(c): c for c in timed}.values():
         cap.graph.replay()
     torch.cuda.synchronize()
-    # warm-up: W steps
     done = 0
-    while done < args.warmup:
+    while done < a.warmup:
         warm_cap.graph.replay()
         done += warm_cap.steps
     torch.cuda.synchronize()
@@ -436,7 +576,7 @@ def run_pkv(args):
         torch.distributed.barrier()
 
     uuid = str(getattr(torch.cuda.get_device_properties(device), "uuid", "") or "")
-    sampler = ClockSampler(uuid if uuid.startswith("GPU-") else (f"GPU-{uuid}" if uuid else str(local)))
+    sampler = ClockSampler(uuid if uuid.startswith("GPU-") else (f"GPU-{uuid}" if uuid else str(device.index)))
     sampler.start()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
@@ -462,64 +602,120 @@ def run_pkv(args):
     if st != pkv.PKV_OK:
         raise SystemExit(f"device error flag set during the timed region: {flag:#x}")
 
-    # dominant kernel: the attention launches (split + merge), timed inside the graphs
-    split_ms = [s.elapsed_time(e) for cap in timed_ev for (s, e) in cap.split_events]
-    kv_step = w.kv_bytes_per_step(args.kv)
+    att_ms = [s_.elapsed_time(e_) for cap in timed_ev for (s_, e_) in cap.split_events]
+    kv_step = w.kv_bytes_per_step(a.kv)
     launches = harness.attention_launches_per_step(dw)
     kv_launch = kv_step // launches  # average over the layers (and the micro-batch chains)
-    peak, peak_src = hbm_peak()
-    steps_per_s = args.steps / (elapsed_ms / 1e3)
+    steps_per_s = a.steps / (elapsed_ms / 1e3)
     value = kv_step * steps_per_s * world / 1e9
     roofline = None
-    if split_ms:
-        avg = sum(split_ms) / len(split_ms)
+    if att_ms:
+        avg = sum(att_ms) / len(att_ms)
         alone = kv_launch / (avg / 1e3) / 1e9
-        timing = f"external events around every launch in a second pass of {per_graph} steps"
+        timing = f"external events around every attention launch in a second pass of {per_graph} steps"
         eff_ms, achieved = avg, alone
-        if args.chains > 1:
-            # the chains' launches overlap on the GPU, and an event between two launches of
-            # one chain would serialise them: a launch's duration comes from the timed region
-            # (every launch in it is this kernel), the serialised per-launch figure is kept
-            eff_ms = (elapsed_ms / args.steps) / launches
+        if a.chains > 1 or a.path != "fused":
+            # launches overlap on the GPU (micro-batch chains; the append kernels of the separate
+            # path), and an event between two launches of one chain would serialise them: a launch's
+            # GPU time comes from the timed region (step time / attention launches per step), and
+            # the serialised per-launch figure is kept beside it
+            eff_ms = (elapsed_ms / a.steps) / launches
             achieved = kv_launch / (eff_ms / 1e3) / 1e9
-            timing = ("micro-batch chains overlap their launches: GPU time per launch = step time / launches per "
-                      "step, from the timed region (every launch in it is this kernel); launch_alone: "
-                      + timing + ", the chains one after another")
+            timing = ("GPU time per attention launch = step time / attention launches per step, from the timed "
+                      "region (CUDA events on the caller's stream around it)" +
+                      (", which also holds the separate path's append launches" if a.path != "fused" else "") +
+                      "; launch_alone: " + timing + ", the chains one after another")
         roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                    "traffic": measured_traffic(args.config, args.path, variant_name, args.pages_per_chunk,
-                                                args.ring, args.kv, args.chains, args.sorted),
-                    "kernel": ("fused decode step kernel over FP8 pages (append + quantize + attention + merge)"
-                               if args.kv == "fp8" else
-                               f"fused decode step kernel (append + attention + merge), variant {variant_name}"
-                               if args.path == "fused" else
-                               f"paged decode attention launch (split + merge), variant {variant_name}"),
-                    "timing": timing, "algorithmic_bytes_per_launch": kv_launch, "avg_launch_us": eff_ms * 1e3,
-                    "launches_timed": len(split_ms), "peak_source": f"{peak_src} hbm_gbs (burst copy)"}
-        if args.chains > 1:
-            roofline["launch_alone"] = {"achieved": alone, "frac": alone / peak, "avg_launch_us": avg * 1e3}
+                    "traffic": measured_traffic(a.config, a.path, variant_name, a.pages_per_chunk, a.ring, a.kv,
+                                                a.chains, a.sorted, a.split_merge),
+                    "kernel": kernel_label(a, variant_name), "timing": timing,
+                    "algorithmic_bytes_per_launch": kv_launch, "avg_launch_us": eff_ms * 1e3,
+                    "launches_timed": len(att_ms), "peak_source": f"{peak_src} hbm_gbs (burst copy, reads + writes)",
+                    "frac_of_nominal": achieved / NOMINAL_HBM_GBS}
+        if read_peak:
+            roofline["frac_of_read_ceiling"] = achieved / read_peak["gbs"]
+        roofline["launch_alone"] = {"achieved": alone, "frac": alone / peak, "avg_launch_us": avg * 1e3,
+                                    "frac_of_read_ceiling": alone / read_peak["gbs"] if read_peak else None}
 
-    # end to end through the public API with pinned host buffers
-    e2e = None
-    if not args.no_e2e:
-        e2e = measure_e2e(dw, args, world, device)
+    e2e = None if a.no_e2e else measure_e2e(dw, a, world, device)
+    fields = {"value": value, "unit": "GB/s", "ms_per_step": elapsed_ms / a.steps, "steps": a.steps,
+              "hbm_frac_of_peak": value / world / peak,
+              "hbm_frac_of_nominal": value / world / NOMINAL_HBM_GBS,
+              "hbm_frac_of_read_ceiling": value / world / read_peak["gbs"] if read_peak else None,
+              "steps_per_s": steps_per_s, "tokens_per_s": w.batch * steps_per_s * world,
+              "attended_kv_tokens_per_s": float(w.seq_lens.sum()) * w.layers * steps_per_s * world,
+              "dtype": "bf16" if a.kv == "bf16" else "fp8e4m3 KV, f16 MMA, f32 softmax",
+              "config": config_block(w, a, variant_name, True), "roofline": roofline, "e2e": e2e,
+              "cpu_baseline": cpu, "gpu_launches": harness.kernels_per_step(dw) * a.steps, "clocks": clocks}
+    dw.eng.close()
+    del dw
+    torch.cuda.empty_cache()
+    return fields
 
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(w, args.cpu_seconds, args.seed, args.kv)
 
-    line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16" if args.kv == "bf16" else "fp8e4m3 KV, f16 MMA, f32 softmax", "data": "synthetic",
-            "config": config_block(w, args, variant_name, True),
-            "hbm_frac_of_peak": value / world / peak, "steps_per_s": steps_per_s,
-            "tokens_per_s": w.batch * steps_per_s * world,
-            "attended_kv_tokens_per_s": float(w.seq_lens.sum()) * w.layers * steps_per_s * world,
-            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": harness.kernels_per_step(dw) * args.steps, "clocks": clocks}
+# further configurations measured beside the headline one in the default run: the other
+# 70 %-target batch (b64), the batch-8 shape, the two named calls per layer (b64), FP8 pages
+EXTRA_DEFAULT = ("b64", "b8", "b64:separate", "b64:fp8", "b256:fp8")
+
+
+def parse_extra(spec: str):
+    parts = spec.split(":")
+    config, kv, path, split = parts[0], "bf16", "fused", False
+    for p in parts[1:]:
+        if p == "fp8":
+            kv = "fp8"
+        elif p == "separate":
+            path = "separate"
+        elif p == "split-merge":
+            path, split = "separate", True
+        else:
+            raise SystemExit(f"unknown extra configuration part {p!r} in {spec!r}")
+    if config not in DEFAULT_CHUNK or config == "trace":
+        raise SystemExit(f"unknown extra configuration {spec!r}")
+    return config, kv, path, split
+
+
+def run_pkv(args):
+    import torch
+
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the CUDA path has no CPU fallback)")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=device)
+
+    peak, peak_src = hbm_peak()
+    read_peak = None if args.no_read_ceiling else read_ceiling(device)
+    head = measure(run_settings(args, args.config, args.kv, args.path, args.split_merge), rank, world, device, peak,
+                   peak_src, read_peak, with_cpu=rank == 0 and world == 1 and not args.no_cpu_baseline)
+    extras = {}
+    specs = EXTRA_DEFAULT if args.extra == "default" else tuple(x for x in args.extra.split(",") if x and x != "none")
+    for spec in specs:
+        config, kv, path, split = parse_extra(spec)
+        if (config, kv, path, split) == (args.config, args.kv, args.path, args.split_merge):
+            continue
+        a = run_settings(args, config, kv, path, split,
+                         steps=max(args.steps, args.extra_min_steps) if config != "b256" else args.steps)
+        extras[spec] = measure(a, rank, world, device, peak, peak_src, read_peak, with_cpu=False)
+
+    line = {"metric": METRIC, "value": head["value"], "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": head["dtype"], "data": "synthetic",
+            "config": head["config"],
+            "hbm_frac_of_peak": head["hbm_frac_of_peak"], "hbm_frac_of_nominal": head["hbm_frac_of_nominal"],
+            "hbm_frac_of_read_ceiling": head["hbm_frac_of_read_ceiling"],
+            "steps_per_s": head["steps_per_s"], "tokens_per_s": head["tokens_per_s"],
+            "attended_kv_tokens_per_s": head["attended_kv_tokens_per_s"],
+            "roofline": head["roofline"], "cpu_baseline": head["cpu_baseline"], "e2e": head["e2e"],
+            "gpu_launches": head["gpu_launches"], "clocks": head["clocks"],
+            "read_ceiling": read_peak, "nominal_hbm_gbs": NOMINAL_HBM_GBS,
+            "configs": extras}
     if rank == 0:
         print(json.dumps(line), flush=True)
-    dw.eng.close()
     if world > 1:
         torch.distributed.destroy_process_group()
     return 0
@@ -596,8 +792,16 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--ref-seqs", type=int, default=2, help="sequences per reference-arm step")
+    ap.add_argument("--cpu-seconds", type=float, default=8.0,
+                    help="CPU baseline: seconds of oracle work, half single-threaded, half on every host core")
+    ap.add_argument("--ref-seqs", type=int, default=16, help="sequences per reference-arm step")
+    ap.add_argument("--extra", default="default",
+                    help="further configurations measured in the same run and reported under 'configs': "
+                         "comma-separated workload[:fp8][:separate|:split-merge] items, 'none', or 'default' ("
+                         + ", ".join(EXTRA_DEFAULT) + ")")
+    ap.add_argument("--extra-min-steps", type=int, default=200, help="at least this many timed steps per extra "
+                    "configuration other than b256")
+    ap.add_argument("--no-read-ceiling", action="store_true", help="skip the read-only HBM probe")
     args = ap.parse_args(argv)
     if args.pages_per_chunk is None:
         args.pages_per_chunk = DEFAULT_CHUNK[args.config]

@@ -164,14 +164,22 @@ int pkv_block_tables_build(pkv_pool *pool, int layers, int B, const int32_t *seq
 
 /* ------------------------------------------------------------------- RoPE */
 
-/* Fill a device table of rotary-embedding factors: dev_cos_sin[p][i] =
- * {cos(p * theta^(-2i/(2*half_dim))), sin(...)} as FP32, computed on the host
- * in FP64 and rounded once ("从零构建大模型推理引擎" section 4.1: rotary embedding
- * injects the absolute position; the samir-vllm page's RoPE item).  The pairing
- * is rotate-half: dimension i turns with dimension i + half_dim.
+/* Bytes of the rotary-embedding table of pkv_rope_table_init: max_pos x half_dim
+ * entries of 4 floats (16 bytes); 0 for max_pos < 1 or half_dim other than 32. */
+size_t pkv_rope_table_bytes(int max_pos, int half_dim);
+
+/* Fill a device table of rotary-embedding factors ("从零构建大模型推理引擎" section 4.1:
+ * rotary embedding injects the absolute position; the samir-vllm page's RoPE item).
+ * Entry (p, i) holds c = cos(p * theta^(-2i/(2*half_dim))) and s = sin(...), computed
+ * on the host in FP64, each as two FP32 parts: {c_hi, s_hi, c_lo, s_lo} with c_hi the
+ * FP32 nearest c and c_lo the FP32 nearest c - c_hi (about 48 bits together).  The
+ * kernels rotate with both parts and error-free products, so a rotated value rounds to
+ * the BF16 nearest the exact rotation even where its two products nearly cancel.  The
+ * pairing is rotate-half: dimension i turns with dimension i + half_dim.
  *   theta      base (500000 for Llama 3.2); half_dim must be 32
  *   max_pos    rows; positions 0 .. max_pos-1 (2048 for the engine's context)
- *   dev_cos_sin device buffer of max_pos * half_dim * 2 floats
+ *   dev_cos_sin device buffer of pkv_rope_table_bytes(max_pos, half_dim) bytes
+ *              (max_pos * half_dim * 4 floats), 16-byte aligned
  * Copies synchronously with respect to the host (the stream is synchronised). */
 int pkv_rope_table_init(double theta, int max_pos, int half_dim, float *dev_cos_sin, void *cuda_stream);
 

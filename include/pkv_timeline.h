@@ -6,8 +6,9 @@
  * writes libpkv_timeline.so beside libpkv.so) records it and exports the function
  * below; the default libpkv.so has neither the records nor the symbol.
  *
- * Each launch of the grid schedule (pkv_decode_step without PKV_STEP_PERSISTENT /
- * PKV_STEP_WS) stores, for every CTA linear index i = x + 8 (y + B z) below 16384:
+ * Each launch of the BF16 grid kernel (pkv_decode_step, and pkv_decode_attention
+ * without PKV_DECODE_SPLIT_MERGE) stores, for every CTA linear index
+ * i = x + 8 (y + B z) below 16384:
  *   stamps[i][0..4]  %globaltimer (ns) at CTA entry, once its work unit is known,
  *                    after the wait for the previous launch, after its page loop,
  *                    and at its end (after the combine / merge);

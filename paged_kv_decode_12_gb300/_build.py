@@ -20,7 +20,7 @@ LIB = os.path.join(HERE, "libpkv.so")
 BUILD_DIR = os.path.join(ROOT, "_build")
 
 SOURCES = ["pkv_host.cpp", "pkv_sched.cpp", "pkv_layers.cpp", "pkv_append.cu", "pkv_decode.cu", "pkv_step.cu",
-           "pkv_fp8.cu"]
+           "pkv_fp8.cu", "pkv_probe.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -52,7 +52,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None, timeline
     build_dir = os.path.join(BUILD_DIR, "timeline") if timeline else BUILD_DIR
     os.makedirs(build_dir, exist_ok=True)
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh"))]
-    headers.append(os.path.join(INCLUDE, "pkv.h"))
+    headers += [os.path.join(INCLUDE, h) for h in os.listdir(INCLUDE) if h.endswith(".h")]
     srcs = [os.path.join(CSRC, s) for s in SOURCES]
     objs = [os.path.join(build_dir, os.path.basename(s) + ".o") for s in srcs]
     if not force and not _stale([lib_path], srcs + headers + [__file__]):

@@ -52,11 +52,11 @@ append_rope_kernel(uint16_t *__restrict__ slab, int num_pages, const uint16_t *_
     }
 
     // rotations: rows 0..7 are keys, rows 8..39 queries (if given); 16 threads per row
-    const float4 *rope_row = rope + (size_t)p * (kD / 4);  // [32 pairs] x (cos, sin) = 16 float4
+    const float4 *rope_row = rope + (size_t)p * (kD / 2);  // [32 pairs] x {cos, sin hi; cos, sin lo}
     const int rows = kHkv + (q ? kHq : 0);
     for (int item = threadIdx.x; item < rows * 16; item += kAppendThreads) {
         const int r = item / 16, j = item % 16;  // pairs 2j and 2j+1
-        const float4 cs = rope_row[j];           // cos(2j), sin(2j), cos(2j+1), sin(2j+1)
+        const float4 cs0 = rope_row[2 * j], cs1 = rope_row[2 * j + 1];
         const uint16_t *src;
         uint16_t *dst;
         if (r < kHkv) {
@@ -70,8 +70,8 @@ append_rope_kernel(uint16_t *__restrict__ slab, int num_pages, const uint16_t *_
         const float2 x1 = __bfloat1622float2(lo);   // dims 2j, 2j+1
         const float2 x2 = __bfloat1622float2(hi);   // dims 2j+32, 2j+33
         float2 y1, y2;
-        dev::rope_rotate_pair(x1.x, x2.x, cs.x, cs.y, y1.x, y2.x);
-        dev::rope_rotate_pair(x1.y, x2.y, cs.z, cs.w, y1.y, y2.y);
+        dev::rope_rotate_pair(x1.x, x2.x, cs0, y1.x, y2.x);
+        dev::rope_rotate_pair(x1.y, x2.y, cs1, y1.y, y2.y);
         *reinterpret_cast<__nv_bfloat162 *>(dst + 2 * j) = __float22bfloat162_rn(y1);
         *reinterpret_cast<__nv_bfloat162 *>(dst + kD / 2 + 2 * j) = __float22bfloat162_rn(y2);
     }
@@ -114,7 +114,7 @@ constexpr int kPrefillThreads = 128;
 __global__ void __launch_bounds__(kPrefillThreads)
 prefill_append_kernel(uint16_t *__restrict__ slab, int num_pages, const uint16_t *__restrict__ k,
                       const uint16_t *__restrict__ v, const int32_t *__restrict__ bt_rows, int max_blocks, int start_pos,
-                      int T, const float2 *__restrict__ rope, int max_pos, int32_t *__restrict__ err)
+                      int T, const float4 *__restrict__ rope, int max_pos, int32_t *__restrict__ err)
 {
     const int t = blockIdx.x, l = blockIdx.y;
     const int p = start_pos + t;
@@ -139,12 +139,12 @@ prefill_append_kernel(uint16_t *__restrict__ slab, int num_pages, const uint16_t
     }
     for (int item = threadIdx.x; item < kHkv * (kD / 2); item += kPrefillThreads) {
         const int h = item / (kD / 2), i = item % (kD / 2);
-        const float2 cs = rope[(size_t)p * (kD / 2) + i];
+        const float4 cs = rope[(size_t)p * (kD / 2) + i];
         const uint16_t *src = k + row0 + (size_t)h * kD;
         const float x1 = __uint_as_float((uint32_t)src[i] << 16);
         const float x2 = __uint_as_float((uint32_t)src[i + kD / 2] << 16);
         float y1, y2;
-        dev::rope_rotate_pair(x1, x2, cs.x, cs.y, y1, y2);
+        dev::rope_rotate_pair(x1, x2, cs, y1, y2);
         const __nv_bfloat16 b1 = __float2bfloat16_rn(y1), b2 = __float2bfloat16_rn(y2);
         uint16_t *dst = page_base + ((size_t)h * kPage + slot) * kD;
         dst[i] = *reinterpret_cast<const uint16_t *>(&b1);
@@ -173,6 +173,6 @@ extern "C" int pkv_prefill_append(const pkv_pool *pool, const uint16_t *k, const
                                   dev_err_flag, s);
     prefill_append_kernel<<<dim3(T, layers), kPrefillThreads, 0, s>>>(
         reinterpret_cast<uint16_t *>(pool->slab), pool->num_pages, k, v, bt_rows, max_blocks, start_pos, T,
-        reinterpret_cast<const float2 *>(rope_table), max_pos, dev_err_flag);
+        reinterpret_cast<const float4 *>(rope_table), max_pos, dev_err_flag);
     return status_from_cuda(cudaGetLastError());
 }

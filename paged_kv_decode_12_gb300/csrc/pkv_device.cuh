@@ -110,13 +110,32 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
-// Rotary embedding of one (i, i + 32) pair by the table's FP32 factors (c, s):
-// y1 = x1 c - x2 s, y2 = x2 c + x1 s.  Every kernel that rotates uses this one
-// expression, so the append kernel and the fused step kernel round identically.
-__device__ __forceinline__ void rope_rotate_pair(float x1, float x2, float c, float s, float &y1, float &y2)
+// a c + b s for BF16-valued a, b and factors held as FP32 pairs c = ch + cl, s = sh + sl
+// (about 48 bits each).  a ch and b sh have at most 8 + 24 significant bits, so each is
+// split exactly into an FP32 product and its FMA remainder; the two leading products
+// are added exactly (two-sum) and everything below them goes into one correction term.
+// The FP32 result is within one rounding of the exact value plus a few units of
+// 2^-48 max(|a|, |b|): even where a c and b s nearly cancel it rounds to the same BF16
+// as the exact rotation, except within that distance of a rounding boundary.  The
+// intrinsics keep the compiler from contracting the products into other FMAs.
+__device__ __forceinline__ float rope_comb(float a, float b, float ch, float cl, float sh, float sl)
 {
-    y1 = fmaf(x1, c, -(x2 * s));
-    y2 = fmaf(x2, c, x1 * s);
+    const float p = __fmul_rn(a, ch), pe = __fmaf_rn(a, ch, -p);
+    const float r = __fmul_rn(b, sh), re = __fmaf_rn(b, sh, -r);
+    const float t = __fadd_rn(p, r), bb = __fsub_rn(t, p);
+    const float e = __fadd_rn(__fsub_rn(p, __fsub_rn(t, bb)), __fsub_rn(r, bb));
+    const float lo = __fadd_rn(__fadd_rn(pe, re), __fmaf_rn(a, cl, __fmul_rn(b, sl)));
+    return __fadd_rn(t, __fadd_rn(e, lo));
+}
+
+// Rotary embedding of one (i, i + 32) pair by the table entry {cos_hi, sin_hi, cos_lo,
+// sin_lo} of its (position, i): y1 = x1 c - x2 s, y2 = x2 c + x1 s.  Every kernel that
+// rotates uses this one function, so the append kernels and the fused step kernel round
+// identically.
+__device__ __forceinline__ void rope_rotate_pair(float x1, float x2, float4 cs, float &y1, float &y2)
+{
+    y1 = rope_comb(x1, -x2, cs.x, cs.z, cs.y, cs.w);
+    y2 = rope_comb(x2, x1, cs.x, cs.z, cs.y, cs.w);
 }
 
 // ------------------------------------------------------------------ SIMT policy

@@ -46,13 +46,13 @@ using namespace fp8;
 
 // One warp stores the K row of head h: lane i rotates the pair (i, i + 32) with
 // the table's factors, rounds both to BF16 and quantizes them with the row scale.
-__device__ __forceinline__ void store_key_row_fp8(uint8_t *page, int h, int slot, const uint16_t *k, float2 cs,
+__device__ __forceinline__ void store_key_row_fp8(uint8_t *page, int h, int slot, const uint16_t *k, float4 cs,
                                                   int lane)
 {
     const float x1 = __uint_as_float((uint32_t)k[lane] << 16);
     const float x2 = __uint_as_float((uint32_t)k[lane + kD / 2] << 16);
     float y1, y2;
-    rope_rotate_pair(x1, x2, cs.x, cs.y, y1, y2);
+    rope_rotate_pair(x1, x2, cs, y1, y2);
     uint32_t c1, c2;
     float scale;
     quantize_pair(bf16_round(y1), bf16_round(y2), c1, c2, scale);
@@ -88,7 +88,7 @@ __global__ void __launch_bounds__(kAppendThreads)
 append_rope_fp8_kernel(uint8_t *__restrict__ slab, int num_pages, const uint16_t *__restrict__ k_new,
                        const uint16_t *__restrict__ v_new, uint16_t *__restrict__ q, const int32_t *__restrict__ bt,
                        int max_blocks, const int32_t *__restrict__ pos,
-                       const float2 *__restrict__ rope, int max_pos, int32_t *__restrict__ err)
+                       const float4 *__restrict__ rope, int max_pos, int32_t *__restrict__ err)
 {
     const int b = blockIdx.x;
     const int p = pos[b];
@@ -106,7 +106,7 @@ append_rope_fp8_kernel(uint8_t *__restrict__ slab, int num_pages, const uint16_t
     const int slot = p % kPage;
     const int h = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint8_t *page_base = slab + (size_t)page * kFp8PageBytes;
-    const float2 *rope_row = rope + (size_t)p * (kD / 2);
+    const float4 *rope_row = rope + (size_t)p * (kD / 2);
     store_key_row_fp8(page_base, h, slot, k_new + ((size_t)b * kHkv + h) * kD, rope_row[lane], lane);
     store_value_row_fp8(page_base, h, slot, v_new + ((size_t)b * kHkv + h) * kD, lane);
     if (!q)
@@ -115,11 +115,11 @@ append_rope_fp8_kernel(uint8_t *__restrict__ slab, int num_pages, const uint16_t
     for (int item = threadIdx.x; item < kHq * (kD / 2); item += kAppendThreads) {
         const int r = item / (kD / 2), i = item % (kD / 2);
         uint16_t *row = q + ((size_t)b * kHq + r) * kD;
-        const float2 cs = rope_row[i];
+        const float4 cs = rope_row[i];
         const float x1 = __uint_as_float((uint32_t)row[i] << 16);
         const float x2 = __uint_as_float((uint32_t)row[i + kD / 2] << 16);
         float y1, y2;
-        rope_rotate_pair(x1, x2, cs.x, cs.y, y1, y2);
+        rope_rotate_pair(x1, x2, cs, y1, y2);
         const __nv_bfloat16 b1 = __float2bfloat16_rn(y1), b2 = __float2bfloat16_rn(y2);
         row[i] = *reinterpret_cast<const uint16_t *>(&b1);
         row[i + kD / 2] = *reinterpret_cast<const uint16_t *>(&b2);
@@ -133,7 +133,7 @@ constexpr int kPrefillThreads = 128;
 __global__ void __launch_bounds__(kPrefillThreads)
 prefill_append_fp8_kernel(uint8_t *__restrict__ slab, int num_pages, const uint16_t *__restrict__ k,
                           const uint16_t *__restrict__ v, const int32_t *__restrict__ bt_rows, int max_blocks,
-                          int start_pos, int T, const float2 *__restrict__ rope, int max_pos,
+                          int start_pos, int T, const float4 *__restrict__ rope, int max_pos,
                           int32_t *__restrict__ err)
 {
     const int t = blockIdx.x, l = blockIdx.y;
@@ -153,7 +153,7 @@ prefill_append_fp8_kernel(uint8_t *__restrict__ slab, int num_pages, const uint1
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint8_t *page_base = slab + (size_t)page * kFp8PageBytes;
     const size_t row0 = ((size_t)l * T + t) * kHkv * kD;  // token t of layer l: [8][64]
-    const float2 cs = rope[(size_t)p * (kD / 2) + lane];
+    const float4 cs = rope[(size_t)p * (kD / 2) + lane];
 #pragma unroll
     for (int hh = 0; hh < kHkv / 4; ++hh) {
         const int h = w + 4 * hh;
@@ -319,7 +319,7 @@ int fp8_append_rope(const pkv_pool *pool, const uint16_t *k_new, const uint16_t 
 {
     append_rope_fp8_kernel<<<B, kAppendThreads, 0, s>>>(reinterpret_cast<uint8_t *>(pool->slab), pool->num_pages,
                                                         k_new, v_new, q, bt, max_blocks, pos,
-                                                        reinterpret_cast<const float2 *>(rope), max_pos, err);
+                                                        reinterpret_cast<const float4 *>(rope), max_pos, err);
     return status_from_cuda(cudaGetLastError());
 }
 
@@ -329,7 +329,7 @@ int fp8_prefill_append(const pkv_pool *pool, const uint16_t *k, const uint16_t *
 {
     prefill_append_fp8_kernel<<<dim3(T, layers), kPrefillThreads, 0, s>>>(
         reinterpret_cast<uint8_t *>(pool->slab), pool->num_pages, k, v, bt_rows, max_blocks, start_pos, T,
-        reinterpret_cast<const float2 *>(rope), max_pos, err);
+        reinterpret_cast<const float4 *>(rope), max_pos, err);
     return status_from_cuda(cudaGetLastError());
 }
 

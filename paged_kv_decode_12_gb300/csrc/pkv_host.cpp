@@ -219,22 +219,33 @@ int pkv_block_tables_build(pkv_pool *pool, int layers, int B, const int32_t *seq
     return PKV_OK;
 }
 
+size_t pkv_rope_table_bytes(int max_pos, int half_dim)
+{
+    if (max_pos < 1 || half_dim != PKV_HEAD_DIM / 2)
+        return 0;
+    return (size_t)max_pos * half_dim * 4 * sizeof(float);
+}
+
 int pkv_rope_table_init(double theta, int max_pos, int half_dim, float *dev_cos_sin, void *cuda_stream)
 {
     if (!dev_cos_sin || max_pos < 1 || half_dim != PKV_HEAD_DIM / 2 || !(theta > 1.0))
         return PKV_ERR_INVALID_ARG;
     std::vector<float> table;
     try {
-        table.resize((size_t)max_pos * half_dim * 2);
+        table.resize((size_t)max_pos * half_dim * 4);
     } catch (...) {
         return PKV_ERR_INVALID_ARG;
     }
     const double dim = 2.0 * half_dim;
     for (int p = 0; p < max_pos; ++p) {
         for (int i = 0; i < half_dim; ++i) {
-            double angle = (double)p * std::pow(theta, -2.0 * i / dim);
-            table[((size_t)p * half_dim + i) * 2 + 0] = (float)std::cos(angle);
-            table[((size_t)p * half_dim + i) * 2 + 1] = (float)std::sin(angle);
+            const double angle = (double)p * std::pow(theta, -2.0 * i / dim);
+            const double c = std::cos(angle), s = std::sin(angle);
+            float *e = &table[((size_t)p * half_dim + i) * 4];
+            e[0] = (float)c;                      // nearest FP32
+            e[1] = (float)s;
+            e[2] = (float)(c - (double)e[0]);     // the rest (exact in FP64), rounded to FP32
+            e[3] = (float)(s - (double)e[1]);
         }
     }
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);

@@ -52,7 +52,7 @@ struct StepArgs {
     const int32_t *bt;       // [B][max_blocks]
     int max_blocks;
     const int32_t *seq_lens; // [B]
-    const float2 *rope;      // [max_pos][32] (cos, sin) (APPEND)
+    const float4 *rope;      // [max_pos][32] {cos, sin} high then low FP32 parts (APPEND)
     int max_pos;             // APPEND: rope rows; otherwise INT_MAX
     float scale_log2;
     int pages_per_chunk;
@@ -281,14 +281,14 @@ __device__ __forceinline__ void unit_rows(const StepArgs &a, int b, int g, int p
         reinterpret_cast<uint32_t *>(q_rot + hl * kD)[i] = reinterpret_cast<const uint32_t *>(qrow)[i];
         return;
     }
-    const float2 cs = a.rope[(size_t)pos * (kD / 2) + i];
+    const float4 cs = a.rope[(size_t)pos * (kD / 2) + i];
     float y1, y2;
-    rope_rotate_pair(bf16_value(qrow[i]), bf16_value(qrow[i + kD / 2]), cs.x, cs.y, y1, y2);
+    rope_rotate_pair(bf16_value(qrow[i]), bf16_value(qrow[i + kD / 2]), cs, y1, y2);
     q_rot[hl * kD + i] = bf16_bits(y1);
     q_rot[hl * kD + i + kD / 2] = bf16_bits(y2);
     if (last_chunk && hl == 0) {
         const uint16_t *krow = a.k_new + ((size_t)b * kHkv + g) * kD;
-        rope_rotate_pair(bf16_value(krow[i]), bf16_value(krow[i + kD / 2]), cs.x, cs.y, y1, y2);
+        rope_rotate_pair(bf16_value(krow[i]), bf16_value(krow[i + kD / 2]), cs, y1, y2);
         new_kv[i] = bf16_bits(y1);
         new_kv[i + kD / 2] = bf16_bits(y2);
     } else if (last_chunk && hl == 1) {
@@ -925,7 +925,7 @@ extern "C" int pkv_decode_step(const pkv_pool *pool, const uint16_t *k_new, cons
     a.q = q;
     a.bt = bt_dev;
     a.seq_lens = seq_lens_dev;
-    a.rope = reinterpret_cast<const float2 *>(rope_table);
+    a.rope = reinterpret_cast<const float4 *>(rope_table);
     a.max_pos = max_pos;
     a.scale_log2 = scale * kLog2e;
     a.out = out;

@@ -55,8 +55,7 @@ class DecodeEngine:
         else:
             self.pool = pkv.pkv_pool_create(self.slab, self.slab.numel(), seed=pool_seed)
         self.num_pages = num_pages
-        self.rope = torch.empty(max_pos * (wl.HEAD_DIM // 2) * 2, dtype=torch.float32, device=self.device)
-        pkv.pkv_rope_table_init(theta, max_pos, wl.HEAD_DIM // 2, self.rope)
+        self.rope = pkv.rope_table(max_pos, self.device, theta)
         self.err = torch.zeros(1, dtype=torch.int32, device=self.device)
         # the attention workspace (the fused step's too) starts with per-(sequence, KV head)
         # merge counters that must be zero before the first call (every call leaves them zero)

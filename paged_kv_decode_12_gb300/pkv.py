@@ -55,7 +55,8 @@ def PKV_STEP_RING(n: int) -> int:
 # every symbol include/pkv.h declares
 EXPORTED = (
     "pkv_pool_create", "pkv_pool_destroy", "pkv_pool_alloc", "pkv_pool_free", "pkv_pool_info",
-    "pkv_block_tables_build", "pkv_rope_table_init", "pkv_append_rope", "pkv_decode_workspace_bytes",
+    "pkv_block_tables_build", "pkv_rope_table_bytes", "pkv_rope_table_init", "pkv_append_rope",
+    "pkv_decode_workspace_bytes",
     "pkv_decode_attention", "pkv_decode_attention_variant", "pkv_decode_attention_noalloc",
     "pkv_decode_step_workspace_bytes", "pkv_decode_step", "pkv_decode_step_layers", "pkv_check_device_error",
     "pkv_status_string", "pkv_version",
@@ -90,6 +91,8 @@ def lib():
     L.pkv_pool_info.argtypes = [_vp, ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(ctypes.c_int64),
                                 ctypes.POINTER(_i32), ctypes.POINTER(_i32)]
     L.pkv_block_tables_build.argtypes = [_vp, _i32, _i32, _i32p, _i32, _i32p]
+    L.pkv_rope_table_bytes.argtypes = [_i32, _i32]
+    L.pkv_rope_table_bytes.restype = ctypes.c_size_t
     L.pkv_rope_table_init.argtypes = [ctypes.c_double, _i32, _i32, _vp, _vp]
     L.pkv_append_rope.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _vp, _i32, _vp, _vp]
     L.pkv_decode_workspace_bytes.argtypes = [_i32, _i32, _i32]
@@ -112,8 +115,8 @@ def lib():
     L.pkv_version.argtypes = []
     L.pkv_version.restype = ctypes.c_char_p
     for name in EXPORTED:
-        if name not in ("pkv_decode_workspace_bytes", "pkv_decode_step_workspace_bytes", "pkv_status_string",
-                        "pkv_version"):
+        if name not in ("pkv_decode_workspace_bytes", "pkv_decode_step_workspace_bytes", "pkv_rope_table_bytes",
+                        "pkv_status_string", "pkv_version"):
             getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -211,6 +214,19 @@ def pkv_block_tables_build(pool, layers: int, seq_lens, max_blocks: int) -> np.n
 
 
 # ---------------------------------------------------------------------------- RoPE / append / decode
+
+def pkv_rope_table_bytes(max_pos: int, half_dim: int) -> int:
+    return int(lib().pkv_rope_table_bytes(max_pos, half_dim))
+
+
+def rope_table(max_pos: int, device, theta: float = 500000.0, half_dim: int = PKV_HEAD_DIM // 2):
+    """A device float32 tensor of pkv_rope_table_bytes(...) bytes, filled by pkv_rope_table_init."""
+    import torch
+
+    t = torch.empty(pkv_rope_table_bytes(max_pos, half_dim) // 4, dtype=torch.float32, device=device)
+    pkv_rope_table_init(theta, max_pos, half_dim, t)
+    return t
+
 
 def pkv_rope_table_init(theta: float, max_pos: int, half_dim: int, dev_cos_sin, stream=None) -> None:
     _check(lib().pkv_rope_table_init(float(theta), max_pos, half_dim, _ptr(dev_cos_sin), _stream(stream)),
@@ -427,3 +443,31 @@ def pkv_pool_kv_format(pool) -> int:
     if st < 0:
         raise PkvError(st, "pkv_pool_kv_format")
     return st
+
+
+# ---------------------------------------------------------------------------- read-bandwidth probes
+
+# every symbol include/pkv_probe.h declares (a measurement aid, not the decode path)
+EXPORTED_PROBE = ("pkv_probe_read_ldg", "pkv_probe_read_bulk")
+
+_lib_fp8 = lib
+
+
+def lib():  # noqa: F811 -- extends the loader with the probe signatures
+    L = _lib_fp8()
+    if not getattr(L, "_pkv_probe_bound", False):
+        for name in EXPORTED_PROBE:
+            getattr(L, name).argtypes = [_vp, ctypes.c_size_t, _vp, _i32, _vp]
+            getattr(L, name).restype = ctypes.c_int
+        L._pkv_probe_bound = True
+    return L
+
+
+def pkv_probe_read_ldg(buf, nbytes: int, sink, ctas_per_sm: int = 2, stream=None) -> None:
+    _check(lib().pkv_probe_read_ldg(_ptr(buf), int(nbytes), _ptr(sink), int(ctas_per_sm), _stream(stream)),
+           "pkv_probe_read_ldg")
+
+
+def pkv_probe_read_bulk(buf, nbytes: int, sink, ctas_per_sm: int = 2, stream=None) -> None:
+    _check(lib().pkv_probe_read_bulk(_ptr(buf), int(nbytes), _ptr(sink), int(ctas_per_sm), _stream(stream)),
+           "pkv_probe_read_bulk")

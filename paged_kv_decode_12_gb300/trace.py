@@ -58,8 +58,7 @@ class TraceRunner:
         self.num_pages = pool_pages
         self.sched = pkv.pkv_sched_create(self.pool, layers, max_blocks, max_context, max_batch,
                                           pkv.PKV_SCHED_STATIC if static else pkv.PKV_SCHED_CONTINUOUS)
-        self.rope = torch.empty(max_context * wl.HEAD_DIM, dtype=torch.float32, device=self.device)
-        pkv.pkv_rope_table_init(wl.ROPE_THETA, max_context, wl.HEAD_DIM // 2, self.rope)
+        self.rope = pkv.rope_table(max_context, self.device, wl.ROPE_THETA)
         self.err = torch.zeros(1, dtype=torch.int32, device=self.device)
         self.ws_bytes = pkv.pkv_decode_step_workspace_bytes(max_batch, max_blocks, pages_per_chunk)
         self.ws = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=self.device)

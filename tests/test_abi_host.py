@@ -25,8 +25,8 @@ def built():
     _build.build()
 
 
-def header_functions():
-    text = open(HEADER).read()
+def header_functions(path=HEADER):
+    text = open(path).read()
     return sorted(set(re.findall(r"^(?:int|size_t|const char \*)\s*(pkv_\w+)\(", text, flags=re.M)))
 
 
@@ -37,6 +37,20 @@ def test_every_declared_symbol_is_exported():
     for name in declared:
         assert hasattr(lib, name), name
     assert sorted(pkv.EXPORTED) == declared
+    # the measurement header's probes are in the same library and bound by the binding
+    probes = header_functions(os.path.join(ROOT, "include", "pkv_probe.h"))
+    assert probes == sorted(pkv.EXPORTED_PROBE)
+    for name in probes:
+        assert hasattr(lib, name), name
+
+
+def test_probe_validation_before_any_cuda_call():
+    for fn in (pkv.pkv_probe_read_ldg, pkv.pkv_probe_read_bulk):
+        for nbytes, sink, ctas in ((0, FAKE_SLAB, 1), (32768, None, 1), (32768 + 8, FAKE_SLAB, 1),
+                                   (32768, FAKE_SLAB, 0), (32768, FAKE_SLAB, 9)):
+            with pytest.raises(pkv.PkvError) as e:
+                fn(FAKE_SLAB, nbytes, sink, ctas, 0)
+            assert e.value.status == pkv.PKV_ERR_INVALID_ARG
 
 
 def test_version_and_status_strings():
@@ -157,6 +171,13 @@ def test_workspace_bytes():
         assert pkv.pkv_decode_workspace_bytes(B, max_blocks, ppc) == want
         assert pkv.pkv_decode_step_workspace_bytes(B, max_blocks, ppc) == want
     assert pkv.pkv_decode_workspace_bytes(0, 128, 16) == 0
+
+
+def test_rope_table_bytes():
+    # 16 bytes per (position, pair): cos and sin, each as a high and a low FP32 part
+    assert pkv.pkv_rope_table_bytes(2048, 32) == 2048 * 32 * 16
+    assert pkv.pkv_rope_table_bytes(1, 32) == 512
+    assert pkv.pkv_rope_table_bytes(0, 32) == 0 and pkv.pkv_rope_table_bytes(2048, 16) == 0
 
 
 def test_launch_entry_points_validate_before_any_cuda_call():

@@ -110,6 +110,19 @@ def assert_close(gpu_u16, ref_f64):
 
 # ---------------------------------------------------------------------------- append
 
+def test_rope_table_holds_cos_and_sin_to_48_bits():
+    # entry (p, i) = {cos_hi, sin_hi, cos_lo, sin_lo}: hi the nearest FP32, hi + lo the
+    # FP64 factor to about 2^-48 (the oracle's definition of the angle, R5/R6)
+    max_pos = 2048
+    t = pkv.rope_table(max_pos, "cuda", wl.ROPE_THETA).cpu().numpy().reshape(max_pos, D // 2, 4).astype(np.float64)
+    p = np.arange(max_pos)[:, None]
+    ang = p * np.array([oracle.rope_inv_freq(wl.ROPE_THETA, D, int(k)) for k in range(D // 2)])[None, :]
+    c, s_ = np.cos(ang), np.sin(ang)
+    assert np.array_equal(t[..., 0], c.astype(np.float32)) and np.array_equal(t[..., 1], s_.astype(np.float32))
+    assert np.abs(t[..., 0] + t[..., 2] - c).max() <= 2.0**-47
+    assert np.abs(t[..., 1] + t[..., 3] - s_).max() <= 2.0**-47
+
+
 @pytest.mark.parametrize("seq_lens", [[17, 40], [1, 16, 17, 32, 33, 2048]])
 def test_append_placement_bit_exact(seq_lens):
     c = make_case(1, seq_lens)

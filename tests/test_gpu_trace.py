@@ -49,8 +49,7 @@ def test_prefill_fill_matches_oracle(start, T):
     pool0 = ph.new_pool(num_pages)
     slab = torch.from_numpy(pool0.view(np.uint8).copy()).cuda()
     p = pkv.pkv_pool_create(slab, slab.numel())
-    rope = torch.empty(2048 * D, dtype=torch.float32, device="cuda")
-    pkv.pkv_rope_table_init(wl.ROPE_THETA, 2048, D // 2, rope)
+    rope = pkv.rope_table(2048, "cuda", wl.ROPE_THETA)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     pkv.pkv_prefill_append(p, dev_bf16(k), dev_bf16(v), torch.from_numpy(bt).cuda(), max_blocks, layers, start, T,
                            rope, 2048, err)
