@@ -724,7 +724,9 @@ def run_pkv(args):
 def measure_e2e(dw, args, world, device):
     """Same metric through DecodeEngine.run_host_steps: every step copies q, k_new, v_new,
     positions and lengths (packed, one copy) from pinned host memory and its output back,
-    double-buffered so that the copies of the neighbouring steps overlap the step's compute."""
+    double-buffered so that the copies of the neighbouring steps overlap the step's compute.
+    The steps run as replays of one captured graph of ``e2e_per_graph`` steps (as a serving
+    loop replays the same graph), ``e2e_steps`` steps in all."""
     import torch
 
     from paged_kv_decode_12_gb300 import harness
@@ -732,17 +734,20 @@ def measure_e2e(dw, args, world, device):
     io = harness.host_pinned_inputs(dw)
     out_host = torch.empty(dw.out.shape, dtype=dw.out.dtype).pin_memory()
     outs = (dw.out, torch.empty_like(dw.out))
-    n = max(2, min(args.steps, args.e2e_steps))
+    per_graph = max(2, min(args.e2e_per_graph, args.e2e_steps))
+    replays = max(1, args.e2e_steps // per_graph)
+    n = per_graph * replays
     dw.eng.run_host_steps(io, outs, out_host, 2)
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
-        dw.eng.run_host_steps(io, outs, out_host, n)
+        dw.eng.run_host_steps(io, outs, out_host, per_graph)
     g.replay()
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record()
-    g.replay()
+    for _ in range(replays):
+        g.replay()
     end.record()
     torch.cuda.synchronize()
     ms = reduce_max(start.elapsed_time(end), world, device)
@@ -750,9 +755,10 @@ def measure_e2e(dw, args, world, device):
     d2h = out_host.numel() * out_host.element_size()
     return {"value": dw.w.kv_bytes_per_step(dw.eng.kv) * n * world / (ms / 1e3) / 1e9, "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n, "ms_per_step": ms / n,
+            "steps_per_graph": per_graph,
             "path": "DecodeEngine.run_host_steps (per step: one H2D copy of the packed pinned inputs and one D2H "
                     "copy of the output, double-buffered on two copy streams so that they overlap the "
-                    "neighbouring steps' compute; CUDA graph)"}
+                    f"neighbouring steps' compute; {replays} replays of a CUDA graph of {per_graph} steps)"}
 
 
 def main(argv=None):
@@ -790,6 +796,7 @@ def main(argv=None):
     ap.add_argument("--layers", type=int, default=None, help="override the layer count (small profiling runs)")
     ap.add_argument("--steps-per-graph", type=int, default=25)
     ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--e2e-per-graph", type=int, default=25, help="end-to-end steps per captured graph")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=8.0,

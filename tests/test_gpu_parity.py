@@ -263,32 +263,12 @@ def test_append_position_out_of_range_sets_flag():
 
 # ---------------------------------------------------------------------------- full-size, bench launch configuration
 
-@pytest.mark.parametrize("name", ["tiny", "b8", "b64", "b256"])
-def test_full_size_sampled(name):
-    dw = harness.setup(name, **launch.config(name))  # the benchmark's launch configuration
-    harness.warm(dw, 1)
-    dw.reset_q()
-    cap = harness.capture_steps(dw, 1)
-    cap.graph.replay()
-    torch.cuda.synchronize()
-    st, flag = dw.eng.check_errors()
-    assert st == pkv.PKV_OK and flag == 0
-    w = dw.w
-    n = 24 if name == "b256" else 40
-    samples = harness.sample_units(w, min(n, w.layers * w.batch * HQ), seed=5)
-    q0 = u16(dw.q0)
-    k_new, v_new = u16(dw.k_new), u16(dw.v_new)
-    out = u16(dw.out)
-    for (l, b, h) in samples:
-        L = int(w.seq_lens[b])
-        npg = -(-L // PS)
-        pages = torch.from_numpy(dw.eng.bt_host[l, b, :npg].astype(np.int64)).cuda()
-        mini = u16(dw.eng.pool_view()[pages]).reshape(-1).copy()
-        g = oracle.geom(npg)
-        bt_row = np.full((1, w.max_blocks), -1, dtype=np.int32)
-        bt_row[0, :npg] = np.arange(npg)
-        qrow = q0[l, b][None].copy()
-        oracle.append(mini, g, bt_row, [L - 1], k_new[l, b][None], v_new[l, b][None], qrow)
-        ref = oracle.decode_one(mini, g, bt_row[0], L, qrow[0, h], h // 4, SCALE)
-        assert_close(out[l, b, h], ref)
-    dw.eng.close()
+@pytest.mark.parametrize("name,layers", [("tiny", (0,)), ("b8", tuple(range(16))), ("b64", tuple(range(16))),
+                                         ("b256", (0, 15))])
+def test_full_size_every_unit(name, layers):
+    # every (layer, sequence, query head) of a whole b8 / b64 step and of two whole b256
+    # layers, at the benchmark's launch settings, against the oracle
+    from tests import full_size
+
+    checked = full_size.check_full_size(name, "bf16", layers)
+    assert checked == wl.make_workload(name).batch * len(layers) * HQ

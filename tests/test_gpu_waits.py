@@ -74,6 +74,7 @@ def test_expired_wait_flags_timeout_and_the_call_finishes(kv, path, sorted_units
 def test_expire_option_is_rejected_by_the_two_kernel_form():
     c = tp.make_case(91, [20, 40])
     eng = DecodeEngine(c["num_pages"], 1, c["B"], c["max_blocks"], 1, fused=False, split_merge=True)
+    eng.set_tables(c["bt"][None])
     q = tp.dev_bf16(c["q"])
     out = torch.zeros_like(q)
     lens = torch.from_numpy(c["seq_lens"]).cuda()

@@ -39,12 +39,16 @@ def _bf16(t):
     return t.float().cpu().numpy().astype(np.float64)
 
 
-def _inputs(seed, seq_lens, max_blocks=128):
+def _inputs(seed, seq_lens, max_blocks=128, kv="bf16", pages_per_chunk=16):
     lens = np.asarray(seq_lens, dtype=np.int32)
     B = lens.size
     need = int(sum(-(-int(L) // wl.PAGE_SIZE) for L in lens))
-    eng = DecodeEngine(need + 4, 1, B, max_blocks, pages_per_chunk=16)
-    wl.fill_bf16_normal_(eng.pool_view(), seed)
+    eng = DecodeEngine(need + 4, 1, B, max_blocks, pages_per_chunk=pages_per_chunk, kv=kv)
+    if kv == "fp8":
+        codes, scales = eng.fp8_views()
+        wl.fill_fp8_pages_(codes, scales, seed, 0.0)
+    else:
+        wl.fill_bf16_normal_(eng.pool_view(), seed)
     eng.build_tables(lens)
     q = wl.fill_bf16_normal_(torch.empty((B, wl.NUM_Q_HEADS, wl.HEAD_DIM), dtype=torch.bfloat16, device="cuda"),
                              seed + 1)
@@ -76,6 +80,37 @@ def test_noalloc_matches_regular_on_two_calls_in_a_row():
         st, flag = eng.check_errors()
         assert st == pkv.PKV_OK and flag == 0
         eng.close()
+
+
+def test_noalloc_fp8_pool_matches_regular():
+    # FP8 pages: the split kernel keeps its chunk partials in the static scratch too
+    for seed, lens in [(24, [2048, 90, 1, 513]), (25, [17, 640])]:
+        eng, q, lens_d = _inputs(seed, lens, kv="fp8")
+        ref = _bf16(_regular(eng, q, lens_d))
+        got = _bf16(_noalloc(eng, q, lens_d))
+        torch.cuda.synchronize()
+        assert np.all(np.abs(got - ref) <= ATOL + RTOL * np.abs(ref))
+        st, flag = eng.check_errors()
+        assert st == pkv.PKV_OK and flag == 0
+        eng.close()
+
+
+def test_noalloc_single_chunk_after_multi_chunk():
+    # a call whose sequences all fit one chunk writes its outputs directly (no partials,
+    # no merge) -- after a multi-chunk call has left partials in the scratch
+    eng, q, lens_d = _inputs(26, [2048, 1000, 37])
+    first, ref = _bf16(_noalloc(eng, q, lens_d)), _bf16(_regular(eng, q, lens_d))
+    torch.cuda.synchronize()
+    assert np.all(np.abs(first - ref) <= ATOL + RTOL * np.abs(ref))
+    eng.close()
+    eng, q, lens_d = _inputs(27, [5, 16, 17, 40], max_blocks=4, pages_per_chunk=4)
+    ref = _bf16(_regular(eng, q, lens_d))
+    got = _bf16(_noalloc(eng, q, lens_d))
+    torch.cuda.synchronize()
+    assert np.all(np.abs(got - ref) <= ATOL + RTOL * np.abs(ref))
+    st, flag = eng.check_errors()
+    assert st == pkv.PKV_OK and flag == 0
+    eng.close()
 
 
 def test_noalloc_rejects_problems_beyond_the_scratch_limit():
