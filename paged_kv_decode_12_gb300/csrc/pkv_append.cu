@@ -11,7 +11,10 @@
 // given) of 32 rotation pairs, and the 8 value rows copied unchanged.  A thread
 // rotates two adjacent pairs (i, i+1) with 4-byte loads/stores of both halves;
 // 64 threads copy the 1 KiB of values with 16-byte moves.  The bytes are tiny
-// (about 2 KiB written per sequence); the kernel is latency-bound.
+// (about 2 KiB written per sequence); the kernel is latency-bound, so it is launched
+// with programmatic dependent launch: its CTAs are scheduled while the previous kernel
+// finishes, wait for it (griddepcontrol.wait) before reading or writing anything, and
+// then let the next launch (the layer's attention) begin its early work.
 #include <cuda_bf16.h>
 
 #include "pkv_device.cuh"
@@ -27,6 +30,8 @@ append_rope_kernel(uint16_t *__restrict__ slab, int num_pages, const uint16_t *_
                    int max_blocks, const int32_t *__restrict__ pos, const float4 *__restrict__ rope, int max_pos,
                    int32_t *__restrict__ err)
 {
+    dev::grid_dependency_wait();
+    dev::allow_dependent_launch();
     const int b = blockIdx.x;
     const int p = pos[b];
     const int limit = min(max_pos, max_blocks * kPage);
@@ -96,11 +101,9 @@ extern "C" int pkv_append_rope(const pkv_pool *pool, const uint16_t *k_new, cons
     if (pool->kv_format == PKV_KV_FP8)
         return fp8_append_rope(pool, k_new, v_new, q, bt_dev, max_blocks, pos_dev, B, rope_table, max_pos,
                                dev_err_flag, s);
-    append_rope_kernel<<<B, kAppendThreads, 0, s>>>(reinterpret_cast<uint16_t *>(pool->slab), pool->num_pages,
-                                                    k_new, v_new, q, bt_dev, max_blocks, pos_dev,
-                                                    reinterpret_cast<const float4 *>(rope_table), max_pos,
-                                                    dev_err_flag);
-    return status_from_cuda(cudaGetLastError());
+    return launch_kernel(append_rope_kernel, dim3(B), dim3(kAppendThreads), 0, s, true,
+                         reinterpret_cast<uint16_t *>(pool->slab), pool->num_pages, k_new, v_new, q, bt_dev,
+                         max_blocks, pos_dev, reinterpret_cast<const float4 *>(rope_table), max_pos, dev_err_flag);
 }
 
 // ---------------------------------------------------------------------------
@@ -168,6 +171,7 @@ extern "C" int pkv_prefill_append(const pkv_pool *pool, const uint16_t *k, const
         15u)
         return PKV_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    pool->serialize_next_launch = true;  // the next decode launch may read these pages
     if (pool->kv_format == PKV_KV_FP8)
         return fp8_prefill_append(pool, k, v, bt_rows, max_blocks, layers, start_pos, T, rope_table, max_pos,
                                   dev_err_flag, s);

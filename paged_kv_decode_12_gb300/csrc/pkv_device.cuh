@@ -25,6 +25,11 @@ static_assert(kThreads == kGroup * 32, "combine maps one thread per (head, dim p
 
 // ------------------------------------------------------------------ PTX helpers
 
+// Programmatic dependent launch: wait until every earlier grid this one depends on
+// has completed and its memory is visible; let the next grid on the stream launch.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_dependent_launch() { asm volatile("griddepcontrol.launch_dependents;" ::); }
+
 __device__ __forceinline__ uint32_t smem_addr(const void *p)
 {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));

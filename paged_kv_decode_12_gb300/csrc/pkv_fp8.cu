@@ -90,6 +90,8 @@ append_rope_fp8_kernel(uint8_t *__restrict__ slab, int num_pages, const uint16_t
                        int max_blocks, const int32_t *__restrict__ pos,
                        const float4 *__restrict__ rope, int max_pos, int32_t *__restrict__ err)
 {
+    grid_dependency_wait();  // launched with programmatic dependent launch: see append_rope_kernel
+    allow_dependent_launch();
     const int b = blockIdx.x;
     const int p = pos[b];
     if (p < 0 || p >= min(max_pos, max_blocks * kPage)) {
@@ -317,10 +319,9 @@ int fp8_append_rope(const pkv_pool *pool, const uint16_t *k_new, const uint16_t 
                     const int32_t *bt, int max_blocks, const int32_t *pos, int B, const float *rope,
                     int max_pos, int32_t *err, cudaStream_t s)
 {
-    append_rope_fp8_kernel<<<B, kAppendThreads, 0, s>>>(reinterpret_cast<uint8_t *>(pool->slab), pool->num_pages,
-                                                        k_new, v_new, q, bt, max_blocks, pos,
-                                                        reinterpret_cast<const float4 *>(rope), max_pos, err);
-    return status_from_cuda(cudaGetLastError());
+    return launch_kernel(append_rope_fp8_kernel, dim3(B), dim3(kAppendThreads), 0, s, true,
+                         reinterpret_cast<uint8_t *>(pool->slab), pool->num_pages, k_new, v_new, q, bt, max_blocks,
+                         pos, reinterpret_cast<const float4 *>(rope), max_pos, err);
 }
 
 int fp8_prefill_append(const pkv_pool *pool, const uint16_t *k, const uint16_t *v, const int32_t *bt_rows,

@@ -6,6 +6,7 @@
 
 #include <cstdint>
 #include <mutex>
+#include <utility>
 #include <vector>
 
 #include "../../include/pkv.h"
@@ -138,6 +139,22 @@ inline cudaLaunchAttribute pdl_attribute()
     attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr.val.programmaticStreamSerializationAllowed = 1;
     return attr;
+}
+
+// Launch `kernel` on `s`, with programmatic dependent launch if `pdl`.
+template <class... Params, class... Args>
+int launch_kernel(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                  Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attrs[1] = {pdl_attribute()};
+    cfg.attrs = attrs;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return status_from_cuda(cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...));
 }
 
 // Whether a decode launch on `pool` may use programmatic dependent launch: not the

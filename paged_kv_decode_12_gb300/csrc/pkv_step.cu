@@ -69,9 +69,6 @@ struct StepArgs {
 constexpr int kMaxSortedBatch = 1024;
 static_assert(kMaxPagesPerChunk + 1 + kWarps + 5 <= kWarps * kScratchFloats, "sorted-order scratch");
 
-__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void allow_dependent_launch() { asm volatile("griddepcontrol.launch_dependents;" ::); }
-
 // Take a ticket: atomic increment with release and acquire semantics at GPU scope.
 __device__ __forceinline__ int ticket_acq_rel(int *counter)
 {

@@ -68,6 +68,67 @@ def test_prefill_fill_matches_oracle(start, T):
     pkv.pkv_pool_destroy(p)
 
 
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_prefill_then_decode_back_to_back(kv):
+    # prompts filled by pkv_prefill_append and decoded right after, every launch in one
+    # CUDA graph with no other work between them: the decode launch after a prefill on the
+    # pool must not read the prompt pages before the prefill has finished
+    from paged_kv_decode_12_gb300.engine import DecodeEngine
+
+    rng = np.random.default_rng(41)
+    prompts = np.array([30, 17, 64, 5, 1, 48], dtype=np.int32)
+    B, layers, max_blocks = prompts.size, 1, 8
+    lens = prompts + 1
+    eng = DecodeEngine(B * max_blocks + 4, layers, B, max_blocks, pages_per_chunk=1, kv=kv)
+    bt = eng.build_tables(lens)
+    k = [wl.bf16_normal_host(rng, (layers, int(T), HKV, D)) for T in prompts]
+    v = [wl.bf16_normal_host(rng, (layers, int(T), HKV, D)) for T in prompts]
+    q = wl.bf16_normal_host(rng, (layers, B, wl.NUM_Q_HEADS, D))
+    k_new = wl.bf16_normal_host(rng, (layers, B, HKV, D))
+    v_new = wl.bf16_normal_host(rng, (layers, B, HKV, D))
+    kd, vd = [dev_bf16(x) for x in k], [dev_bf16(x) for x in v]
+    rows = [torch.from_numpy(np.ascontiguousarray(bt[:, b])).cuda() for b in range(B)]
+    qd, knd, vnd = dev_bf16(q), dev_bf16(k_new), dev_bf16(v_new)
+    lens_d = torch.from_numpy(lens).cuda()
+    out = torch.zeros_like(qd)
+    slab0 = eng.slab.clone()
+    # first pass eager (kernel attributes, tensor map), then restore and replay from a graph
+    for b in range(B):
+        pkv.pkv_prefill_append(eng.pool, kd[b], vd[b], rows[b], max_blocks, layers, 0, int(prompts[b]), eng.rope,
+                               eng.max_pos, eng.err)
+    eng.step(qd.clone(), knd, vnd, lens_d - 1, lens_d, out.clone())
+    torch.cuda.synchronize()
+    eng.slab.copy_(slab0)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for b in range(B):
+            pkv.pkv_prefill_append(eng.pool, kd[b], vd[b], rows[b], max_blocks, layers, 0, int(prompts[b]),
+                                   eng.rope, eng.max_pos, eng.err)
+        eng.step(qd, knd, vnd, lens_d - 1, lens_d, out)
+    g.replay()
+    torch.cuda.synchronize()
+    st, flag = eng.check_errors()
+    assert st == pkv.PKV_OK and flag == 0
+    got = u16(out)
+    eng.close()
+    fp8 = kv == "fp8"
+    append = oracle.append_fp8 if fp8 else oracle.append
+    decode_one = oracle.decode_one_fp8 if fp8 else oracle.decode_one
+    for b in range(B):
+        L = int(lens[b])
+        npg = math.ceil(L / PS)
+        gg = oracle.geom(npg)
+        row = np.full((1, max_blocks), -1, dtype=np.int32)
+        row[0, :npg] = np.arange(npg)
+        mini = np.zeros(npg * oracle.FP8_PAGE_BYTES, np.uint8) if fp8 else ph.new_pool(npg)
+        for t in range(L - 1):
+            append(mini, gg, row, [t], k[b][0, t][None], v[b][0, t][None])
+        qq = q[0, b][None].copy()
+        append(mini, gg, row, [L - 1], k_new[0, b][None], v_new[0, b][None], qq)
+        for h in range(wl.NUM_Q_HEADS):
+            assert_close(got[0, b, h], decode_one(mini, gg, row[0], L, qq[0, h], h // 4, 1.0 / math.sqrt(D)))
+
+
 @pytest.mark.parametrize("kv,chains,static", [("bf16", 1, False), ("fp8", 1, False), ("bf16", 3, False),
                                                ("bf16", 1, True), ("fp8", 1, True)])
 def test_trace_steps_match_oracle(kv, chains, static):
