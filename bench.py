@@ -724,30 +724,27 @@ def run_pkv(args):
 def measure_e2e(dw, args, world, device):
     """Same metric through DecodeEngine.run_host_steps: every step copies q, k_new, v_new,
     positions and lengths (packed, one copy) from pinned host memory and its output back,
-    double-buffered so that the copies of the neighbouring steps overlap the step's compute.
-    The steps run as replays of one captured graph of ``e2e_per_graph`` steps (as a serving
-    loop replays the same graph), ``e2e_steps`` steps in all."""
+    through rotating buffers on two copy streams, so that the copies of the neighbouring
+    steps overlap the step's compute.  Each step's kernels replay a captured graph of that
+    step (one graph per buffer); the copies are stream operations between the replays."""
     import torch
 
     from paged_kv_decode_12_gb300 import harness
 
     io = harness.host_pinned_inputs(dw)
     out_host = torch.empty(dw.out.shape, dtype=dw.out.dtype).pin_memory()
-    outs = (dw.out, torch.empty_like(dw.out))
-    per_graph = max(2, min(args.e2e_per_graph, args.e2e_steps))
-    replays = max(1, args.e2e_steps // per_graph)
-    n = per_graph * replays
-    dw.eng.run_host_steps(io, outs, out_host, 2)
+    group = max(1, args.e2e_group)
+    nbuf = max(2 * group, -(-args.e2e_buffers // group) * group)
+    outs = [dw.out] + [torch.empty_like(dw.out) for _ in range(nbuf - 1)]
+    n = max(group, args.e2e_steps // group * group)
+    dw.eng.run_host_steps(io, outs, out_host, len(outs))   # eager first pass: every buffer once
     torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
-        dw.eng.run_host_steps(io, outs, out_host, per_graph)
-    g.replay()
+    graphs = dw.eng.step_graphs(io, outs, group)
+    dw.eng.run_host_steps(io, outs, out_host, len(outs), graphs=graphs, group=group)
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record()
-    for _ in range(replays):
-        g.replay()
+    dw.eng.run_host_steps(io, outs, out_host, n, graphs=graphs, group=group)
     end.record()
     torch.cuda.synchronize()
     ms = reduce_max(start.elapsed_time(end), world, device)
@@ -755,10 +752,10 @@ def measure_e2e(dw, args, world, device):
     d2h = out_host.numel() * out_host.element_size()
     return {"value": dw.w.kv_bytes_per_step(dw.eng.kv) * n * world / (ms / 1e3) / 1e9, "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n, "ms_per_step": ms / n,
-            "steps_per_graph": per_graph,
             "path": "DecodeEngine.run_host_steps (per step: one H2D copy of the packed pinned inputs and one D2H "
-                    "copy of the output, double-buffered on two copy streams so that they overlap the "
-                    f"neighbouring steps' compute; {replays} replays of a CUDA graph of {per_graph} steps)"}
+                    f"copy of the output, through {len(outs)} rotating buffers on two copy streams so that they "
+                    f"overlap the neighbouring steps' compute; the steps' kernels replay captured graphs of {group} "
+                    "steps, the copies are stream operations between the replays)", "steps_per_graph": group}
 
 
 def main(argv=None):
@@ -795,8 +792,10 @@ def main(argv=None):
     ap.add_argument("--seed", type=int, default=12)
     ap.add_argument("--layers", type=int, default=None, help="override the layer count (small profiling runs)")
     ap.add_argument("--steps-per-graph", type=int, default=25)
-    ap.add_argument("--e2e-steps", type=int, default=50)
-    ap.add_argument("--e2e-per-graph", type=int, default=25, help="end-to-end steps per captured graph")
+    ap.add_argument("--e2e-steps", type=int, default=100)
+    ap.add_argument("--e2e-buffers", type=int, default=2, help="end-to-end input/output buffers in rotation "
+                    "(at least twice --e2e-group)")
+    ap.add_argument("--e2e-group", type=int, default=4, help="end-to-end steps per captured graph replay")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=8.0,

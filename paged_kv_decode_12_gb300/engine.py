@@ -235,20 +235,52 @@ class DecodeEngine:
         self.step(d["q"], d["k_new"], d["v_new"], d["pos"], d["seq_lens"], out_dev, stream)
         out_host.copy_(out_dev, non_blocking=True)
 
-    def run_host_steps(self, io: "PackedIO", out_devs, out_host, steps: int, stream=None) -> None:
+    def step_graphs(self, io: "PackedIO", out_devs, group: int = 1) -> list:
+        """Captured CUDA graphs for ``run_host_steps``: with K = len(out_devs) buffers (a
+        multiple of ``group``), graph j runs ``group`` consecutive steps, the i-th on device
+        input buffer j * group + i of ``io`` into ``out_devs[j * group + i]``.  Capture after a
+        first eager pass (kernel attributes and tensor maps are set up outside any capture)."""
+        K = len(out_devs)
+        if group < 1 or K % group:
+            raise ValueError(f"{K} buffers do not split into graphs of {group} steps")
+        graphs = []
+        for j in range(K // group):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for k in range(j * group, (j + 1) * group):
+                    d = io.buffer(k)
+                    self.step(d["q"], d["k_new"], d["v_new"], d["pos"], d["seq_lens"], out_devs[k])
+            graphs.append(g)
+        return graphs
+
+    def run_host_steps(self, io: "PackedIO", out_devs, out_host, steps: int, stream=None, graphs=None,
+                       group: int = 1) -> None:
         """``steps`` end-to-end steps, each with its own copy of the inputs from pinned host
-        memory and its own copy of the output back, double-buffered: step s reads device
-        input buffer s % 2 and writes ``out_devs[s % 2]``.  Host-to-device copies run on one
-        copy stream and device-to-host copies on another, so that step s+1's inputs arrive
-        and step s-1's output leaves while step s computes.  A buffer is refilled only after
-        the step that used it has finished, and an output buffer is rewritten only after its
-        copy to the host has finished.  ``out_host`` receives the outputs in step order and
-        ends holding the last step's."""
+        memory and its own copy of the output back, through K = len(out_devs) rotating
+        buffers: step s reads device input buffer s % K (``io.buffer(s % K)``) and writes
+        ``out_devs[s % K]``.  Host-to-device copies run on one copy stream and device-to-host
+        copies on another, so that the inputs of the next steps arrive and earlier outputs
+        leave while step s computes.  A buffer is refilled only after the step that used it
+        has finished, and an output buffer is rewritten only after its copy to the host has
+        finished.  ``out_host`` receives the outputs in step order and ends holding the last
+        step's.
+        With ``graphs`` (from ``step_graphs(io, out_devs, group)``) the steps' kernels replay
+        those graphs, ``group`` steps per replay, and the copies stay plain stream operations
+        between the replays: inside a captured graph, copy nodes delay the kernels beside them
+        (measured on GB300: about 10 us per node plus part of the copy), while stream copies
+        overlap them; more steps per replay means fewer graph boundaries (each costs a few
+        microseconds of idle GPU).  ``steps`` must then be a multiple of ``group``, and K of
+        2 x ``group`` lets one group's copies overlap the other group's compute."""
         cur = torch.cuda.current_stream(self.device) if stream is None else stream
         if not hasattr(self, "_h2d"):
             self._h2d, self._d2h = torch.cuda.Stream(device=self.device), torch.cuda.Stream(device=self.device)
-        devs = (io.d, io.second())
-        raws = (io.dev, io.dev2)
+        K = len(out_devs)
+        if K < 2:
+            raise ValueError("run_host_steps needs at least two output buffers")
+        if graphs is not None and (len(graphs) * group != K or steps % group):
+            raise ValueError("graphs, group, buffers and steps do not match")
+        devs = [io.buffer(k) for k in range(K)]
+        raws = [io.raw(k) for k in range(K)]
         start = torch.cuda.Event()
         start.record(cur)
         self._h2d.wait_event(start)
@@ -256,27 +288,40 @@ class DecodeEngine:
         ready = [torch.cuda.Event() for _ in range(steps)]
         done = [torch.cuda.Event() for _ in range(steps)]
         sent = [torch.cuda.Event() for _ in range(steps)]
+        lead = K - 1 if graphs is None else K - group   # uploads issued ahead of the step in progress
 
         def upload(s):
-            if s >= 2:
-                self._h2d.wait_event(done[s - 2])      # the step that last read this buffer
+            if s >= K:
+                self._h2d.wait_event(done[s - K])      # the step that last read this buffer
             with torch.cuda.stream(self._h2d):
-                raws[s % 2].copy_(io.host, non_blocking=True)
+                raws[s % K].copy_(io.host, non_blocking=True)
             ready[s].record(self._h2d)
 
-        upload(0)
+        issued = 0
         for s in range(steps):
-            if s + 1 < steps:
-                upload(s + 1)
-            cur.wait_event(ready[s])
-            if s >= 2:
-                cur.wait_event(sent[s - 2])            # this output buffer has left for the host
-            d = devs[s % 2]
-            self.step(d["q"], d["k_new"], d["v_new"], d["pos"], d["seq_lens"], out_devs[s % 2], cur)
-            done[s].record(cur)
+            first = graphs is None or s % group == 0
+            while first and issued < min(steps, s + lead + (1 if graphs is None else group)):
+                upload(issued)
+                issued += 1
+            if graphs is None:
+                cur.wait_event(ready[s])
+                if s >= K:
+                    cur.wait_event(sent[s - K])        # this output buffer has left for the host
+                d = devs[s % K]
+                self.step(d["q"], d["k_new"], d["v_new"], d["pos"], d["seq_lens"], out_devs[s % K], cur)
+                done[s].record(cur)
+            elif first:
+                for t in range(s, s + group):
+                    cur.wait_event(ready[t])
+                    if t >= K:
+                        cur.wait_event(sent[t - K])
+                with torch.cuda.stream(cur):
+                    graphs[(s % K) // group].replay()
+                for t in range(s, s + group):
+                    done[t].record(cur)
             self._d2h.wait_event(done[s])
             with torch.cuda.stream(self._d2h):
-                out_host.copy_(out_devs[s % 2], non_blocking=True)
+                out_host.copy_(out_devs[s % K], non_blocking=True)
             sent[s].record(self._d2h)
         cur.wait_event(sent[steps - 1])
         cur.wait_event(ready[steps - 1])
@@ -309,9 +354,11 @@ def chain_bounds(batch: int, chains: int, seq_lens=None) -> list:
 
 
 class PackedIO:
-    """A step's inputs packed back to back (256-byte aligned) in one pinned host buffer and one
-    device buffer of the same layout, so that the end-to-end step moves them with one copy.
-    ``h[name]`` / ``d[name]`` are host / device views with the tensors' shapes and dtypes."""
+    """A step's inputs packed back to back (256-byte aligned) in one pinned host buffer and
+    device buffers of the same layout, so that the end-to-end step moves them with one copy.
+    ``h[name]`` / ``d[name]`` are host / device views with the tensors' shapes and dtypes;
+    ``buffer(k)`` / ``raw(k)`` are the views / bytes of device buffer k (allocated on first
+    use; buffer 0 is ``d``)."""
 
     def __init__(self, tensors: dict, device):
         offsets, off = {}, 0
@@ -320,22 +367,30 @@ class PackedIO:
             off += (t.numel() * t.element_size() + 255) // 256 * 256
         self.host = torch.empty(off, dtype=torch.uint8).pin_memory()
         self.dev = torch.empty(off, dtype=torch.uint8, device=device)
-        self.dev2 = None
         self.bytes = sum(t.numel() * t.element_size() for t in tensors.values())
         self._layout = {name: (offsets[name], t.numel() * t.element_size(), t.dtype, t.shape)
                         for name, t in tensors.items()}
-        self.h, self.d = {}, {}
+        self.h = {}
         for name, (o, n, dtype, shape) in self._layout.items():
             self.h[name] = self.host[o:o + n].view(dtype).view(shape)
-            self.d[name] = self.dev[o:o + n].view(dtype).view(shape)
             self.h[name].copy_(tensors[name].cpu())
-        self.d2 = None
+        self._raws = [self.dev]
+        self._views = [self._viewsof(self.dev)]
+        self.d = self._views[0]
+
+    def _viewsof(self, raw) -> dict:
+        return {name: raw[o:o + n].view(dtype).view(shape) for name, (o, n, dtype, shape) in self._layout.items()}
+
+    def raw(self, k: int):
+        while len(self._raws) <= k:
+            self._raws.append(torch.empty_like(self.dev))
+            self._views.append(self._viewsof(self._raws[-1]))
+        return self._raws[k]
+
+    def buffer(self, k: int) -> dict:
+        self.raw(k)
+        return self._views[k]
 
     def second(self) -> dict:
-        """Views of a second device buffer of the same layout (allocated on first use),
-        for double-buffered steps."""
-        if self.dev2 is None:
-            self.dev2 = torch.empty_like(self.dev)
-            self.d2 = {name: self.dev2[o:o + n].view(dtype).view(shape)
-                       for name, (o, n, dtype, shape) in self._layout.items()}
-        return self.d2
+        """Views of device buffer 1."""
+        return self.buffer(1)

@@ -194,10 +194,10 @@ def test_step_layers_call_matches_per_layer_calls(kv):
         assert torch.equal(a, b)
 
 
-@pytest.mark.parametrize("chains", [1, 2])
-def test_run_host_steps_double_buffered(chains):
-    # the double-buffered end-to-end steps compute what the plain step computes: every
-    # step's output reaches the host, and the last one stays there
+@pytest.mark.parametrize("chains,buffers", [(1, 2), (2, 2), (2, 3), (1, 4)])
+def test_run_host_steps_rotating_buffers(chains, buffers):
+    # the end-to-end steps through rotating buffers compute what the plain step computes:
+    # every step's output reaches the host, and the last one stays there
     from paged_kv_decode_12_gb300 import harness
 
     dw = harness.setup("tiny", pages_per_chunk=1, ring=2, chains=chains)
@@ -207,7 +207,7 @@ def test_run_host_steps_double_buffered(chains):
     ref = u16(dw.out)
     io = harness.host_pinned_inputs(dw)
     out_host = torch.empty(dw.out.shape, dtype=dw.out.dtype).pin_memory()
-    outs = (dw.out, torch.empty_like(dw.out))
+    outs = [dw.out] + [torch.empty_like(dw.out) for _ in range(buffers - 1)]
     for steps in (1, 2, 5):
         dw.eng.slab.copy_(pool0)
         out_host.zero_()
@@ -216,8 +216,8 @@ def test_run_host_steps_double_buffered(chains):
         dw.eng.run_host_steps(io, outs, out_host, steps)
         torch.cuda.synchronize()
         assert np.array_equal(u16(out_host), ref), steps
-        if steps >= 2:
-            assert np.array_equal(u16(outs[0]), ref) and np.array_equal(u16(outs[1]), ref)
+        for o in outs[:steps]:
+            assert np.array_equal(u16(o), ref), steps
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
         dw.eng.run_host_steps(io, outs, out_host, 3)
@@ -226,6 +226,21 @@ def test_run_host_steps_double_buffered(chains):
     g.replay()
     torch.cuda.synchronize()
     assert np.array_equal(u16(out_host), ref)
+    # the same steps with the kernels replayed from graphs of `group` steps, copies between
+    for group in (1, 2):
+        if len(outs) % group:
+            continue
+        graphs = dw.eng.step_graphs(io, outs, group)
+        for steps in (group, len(outs) + 2 * group):
+            dw.eng.slab.copy_(pool0)
+            out_host.zero_()
+            for o in outs:
+                o.zero_()
+            dw.eng.run_host_steps(io, outs, out_host, steps, graphs=graphs, group=group)
+            torch.cuda.synchronize()
+            assert np.array_equal(u16(out_host), ref), (group, steps)
+            for o in outs[:steps]:
+                assert np.array_equal(u16(o), ref), (group, steps)
     st, flag = dw.eng.check_errors()
     assert st == pkv.PKV_OK and flag == 0
     dw.eng.close()
