@@ -244,3 +244,49 @@ def test_run_host_steps_rotating_buffers(chains, buffers):
     st, flag = dw.eng.check_errors()
     assert st == pkv.PKV_OK and flag == 0
     dw.eng.close()
+
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+@pytest.mark.parametrize("chunk", [16, 20, 43, 64])   # 8, 7, 3 and 2 chunk slots at 128 table entries
+def test_cluster_merge_equals_ticket_merge_and_split_merge(kv, chunk):
+    # the default merge for 2..8 chunk slots runs the chunk CTAs of a (sequence, KV head) as a
+    # thread-block cluster; it must give the ticket merge's and the two-kernel form's bits
+    from tests import test_gpu_fp8 as f8
+
+    lens = [2048, 1, 16, 17, 320, 321, 1000, 640, 641, 1500, 33, 2047]
+    c = (f8.make_case if kv == "fp8" else make_case)(38, lens, max_blocks=128)
+    pool = c["pool"].view(np.uint8)
+
+    def run(fused, options):
+        eng = DecodeEngine(c["num_pages"], 1, c["B"], c["max_blocks"], chunk, kv=kv, fused=fused,
+                           split_merge=bool(options & pkv.PKV_DECODE_SPLIT_MERGE))
+        eng.step_options |= options & pkv.PKV_STEP_TICKET_MERGE
+        eng.attn_options |= options & pkv.PKV_STEP_TICKET_MERGE
+        eng.slab.copy_(torch.from_numpy(pool).cuda())
+        eng.set_tables(c["bt"][None])
+        lens_d = torch.from_numpy(c["seq_lens"]).cuda()
+        outs = []
+        for _ in range(2):   # a second call on the same workspace
+            q = dev_bf16(c["q"])[None].contiguous()
+            out = torch.full((1, c["B"], 32, 64), 7.0, dtype=torch.bfloat16, device="cuda")
+            eng.step(q, dev_bf16(c["k_new"])[None], dev_bf16(c["v_new"])[None], lens_d - 1, lens_d, out)
+            outs.append(u16(out)[0])
+        st, flag = eng.check_errors()
+        counters = eng.step_ws[: c["B"] * 8 * 4].view(torch.int32).cpu().numpy()
+        res = dict(out=outs, q=u16(q)[0], pool=eng.slab.cpu().numpy(), st=st, flag=flag, counters=counters)
+        eng.close()
+        return res
+
+    cluster = run(True, 0)
+    ticket = run(True, pkv.PKV_STEP_TICKET_MERGE)
+    sep = run(False, 0)
+    two_kernel = run(False, pkv.PKV_DECODE_SPLIT_MERGE)
+    for r in (cluster, ticket, sep, two_kernel):
+        assert r["st"] == pkv.PKV_OK and r["flag"] == 0 and np.all(r["counters"] == 0)
+        assert np.array_equal(r["out"][0], r["out"][1])
+    for r in (ticket, sep, two_kernel):
+        assert np.array_equal(cluster["out"][0], r["out"][0])
+        assert np.array_equal(cluster["pool"], r["pool"])
+    assert np.array_equal(cluster["q"], ticket["q"])
+    ref = (f8.oracle_run if kv == "fp8" else oracle_run)(c)
+    assert_close(cluster["out"][0], ref["out_f64"])
