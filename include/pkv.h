@@ -367,14 +367,6 @@ int pkv_prefill_append(const pkv_pool *pool, const uint16_t *k, const uint16_t *
  * usual, and the merge counters are left at zero.  No copy stalls and nothing faults. */
 #define PKV_STEP_TEST_EXPIRE_WAIT 0x40000
 
-/* Merge the chunk partials through the workspace and a per-(sequence, KV head) ticket
- * (the last chunk CTA merges) even where the default would use the cluster merge: when a
- * launch's sequences span 2..8 chunks (ceil(max_blocks / pages_per_chunk)), the MMA
- * policy in grid order runs the chunk CTAs of one (sequence, KV head) as a thread-block
- * cluster and merges through distributed shared memory instead.  Results are identical;
- * the option exists for comparison. */
-#define PKV_STEP_TICKET_MERGE 0x100000
-
 /* Bytes of device workspace pkv_decode_step needs: pkv_decode_workspace_bytes. */
 size_t pkv_decode_step_workspace_bytes(int B, int max_blocks, int pages_per_chunk);
 

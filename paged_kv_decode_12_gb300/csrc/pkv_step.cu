@@ -326,67 +326,12 @@ __device__ __forceinline__ void write_zero_unit(const StepArgs &a, int b, int g)
 // Chunk counts up to which the merging unit holds every partial in registers.
 constexpr int kMergeRegs = 8;
 
-// ------------------------------------------------------------------ cluster merge
-//
-// When a launch's sequences span 2..8 chunks, the chunk CTAs of one (sequence, KV
-// head) form a thread-block cluster (cluster dims 1 x 1 x chunks).  Each chunk CTA
-// pushes its partial (m, l, o of the 4 heads) into slot c of chunk 0's shared merge
-// area through distributed shared memory and arrives on the cluster barrier; chunk 0
-// waits on the barrier and merges the slots in chunk order with the ticket merge's
-// arithmetic.  No global partials, no fence before an atomic, no second L2 round trip.
-// The barrier runs two phases, and every thread of every CTA of the cluster -- empty
-// chunk slots and invalid lengths included -- takes part in both: it arrives on phase 1
-// at entry and, on its way out, waits for phase 1 (every CTA of the cluster has started,
-// so its shared memory may be written) and arrives on phase 2.  Only chunk 0 of a
-// sequence with several chunks waits on phase 2, after which every push into its merge
-// area is done and visible (release / acquire); it cannot exit while others still write.
-constexpr int kMaxClusterChunks = 8;                          // the portable cluster size
-constexpr int kMergeSlotFloats = 2 * kGroup + kGroup * kD;    // (m, l) of 4 heads, o[4][64]
-constexpr int kMergeBytes = kMaxClusterChunks * kMergeSlotFloats * 4;
-
-__device__ __forceinline__ void cluster_arrive_relaxed()
-{
-    asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
-}
-
-__device__ __forceinline__ void cluster_arrive_release()
-{
-    asm volatile("barrier.cluster.arrive.release;" ::: "memory");
-}
-
-__device__ __forceinline__ void cluster_wait_acquire()
-{
-    asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
-}
-
-// The way out of a cluster CTA that merges nothing: phase 1 done, arrive on phase 2.
-__device__ __forceinline__ void cluster_leave()
-{
-    cluster_wait_acquire();
-    cluster_arrive_release();
-}
-
-// The address in CTA `rank`'s shared memory of this CTA's shared address `local`.
-__device__ __forceinline__ uint32_t cluster_map(uint32_t local, uint32_t rank)
-{
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
-    return r;
-}
-
-__device__ __forceinline__ void st_cluster_f32x2(uint32_t addr, float x, float y)
-{
-    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(x), "f"(y) : "memory");
-}
-
 // Unit epilogue, all threads: combine the warps' states through `state`, then
-// write the output (single chunk) or hand the chunk partial to the merge -- the cluster
-// merge (CLUSTER) or the ticket merge: the partial is published in the workspace and a
-// ticket taken; the unit drawing the last ticket merges every chunk of (b, g) in chunk
-// order and resets the counter.  The merging unit writes the output and, WRITE_Q, the
-// rotated query rows.
-template <bool WRITE_Q, bool CLUSTER, class Warp>
-__device__ __forceinline__ void finish_unit(const StepArgs &a, Warp &w, float *state, int *ticket, float *merge,
+// write the output (single chunk) or publish the chunk partial and take a ticket;
+// the unit drawing the last ticket merges every chunk of (b, g) in chunk order,
+// writes the output (and, WRITE_Q, the rotated query rows), and resets the counter.
+template <bool WRITE_Q, class Warp>
+__device__ __forceinline__ void finish_unit(const StepArgs &a, Warp &w, float *state, int *ticket,
                                             const uint16_t *q_rot, int b, int g, int c, int nchunks)
 {
     const int tid = threadIdx.x, warp = tid >> 5;
@@ -401,52 +346,6 @@ __device__ __forceinline__ void finish_unit(const StepArgs &a, Warp &w, float *s
     const uint32_t q_word = reinterpret_cast<const uint32_t *>(q_rot + hl * kD)[dp];
     if (nchunks == 1) {
         out_row[dp] = finish_pair(o0, o1, lsum);
-        if (WRITE_Q)
-            q_row[dp] = q_word;
-        if (CLUSTER)
-            cluster_leave();
-        return;
-    }
-    if (CLUSTER) {
-        float *slot = merge + c * kMergeSlotFloats;
-        cluster_wait_acquire();  // phase 1: every CTA of the cluster has started
-        if (c != 0) {            // push into chunk 0's slot c, then arrive (release: the pushes first)
-            const uint32_t base = cluster_map(smem_addr(slot), 0);
-            st_cluster_f32x2(base + (uint32_t)(2 * kGroup + hl * kD + 2 * dp) * 4u, o0, o1);
-            if (dp == 0)
-                st_cluster_f32x2(base + (uint32_t)(2 * hl) * 4u, M, lsum);
-            cluster_arrive_release();
-            return;
-        }
-        reinterpret_cast<float2 *>(slot + 2 * kGroup + hl * kD)[dp] = make_float2(o0, o1);
-        if (dp == 0)
-            reinterpret_cast<float2 *>(slot)[hl] = make_float2(M, lsum);
-        cluster_arrive_release();
-        cluster_wait_acquire();  // phase 2: every chunk's slot is written
-        float2 ml[kMaxClusterChunks], oc[kMaxClusterChunks];
-#pragma unroll
-        for (int cc = 0; cc < kMaxClusterChunks; ++cc)
-            if (cc < nchunks) {
-                const float *sl = merge + cc * kMergeSlotFloats;
-                ml[cc] = reinterpret_cast<const float2 *>(sl)[hl];
-                oc[cc] = reinterpret_cast<const float2 *>(sl + 2 * kGroup + hl * kD)[dp];
-            }
-        float Mx = -INFINITY, ls = 0.f, r0 = 0.f, r1 = 0.f;
-#pragma unroll
-        for (int cc = 0; cc < kMaxClusterChunks; ++cc)
-            if (cc < nchunks)
-                Mx = fmaxf(Mx, ml[cc].x);
-        if (Mx != -INFINITY) {
-#pragma unroll
-            for (int cc = 0; cc < kMaxClusterChunks; ++cc)
-                if (cc < nchunks) {
-                    const float f = (ml[cc].x == -INFINITY) ? 0.f : exp2f(ml[cc].x - Mx);
-                    ls = fmaf(f, ml[cc].y, ls);
-                    r0 = fmaf(f, oc[cc].x, r0);
-                    r1 = fmaf(f, oc[cc].y, r1);
-                }
-        }
-        out_row[dp] = finish_pair(r0, r1, ls);
         if (WRITE_Q)
             q_row[dp] = q_word;
         return;
@@ -577,7 +476,7 @@ struct Timeline {  // compiled out
 
 constexpr int kGridExtraBytes = kGroup * kD * 2 + 2 * kD * 2 + 16;  // rotated q rows, new K/V rows, ticket
 
-template <class Warp, int STAGES, bool APPEND, bool CLUSTER>
+template <class Warp, int STAGES, bool APPEND>
 __global__ void __launch_bounds__(kThreads) decode_step_kernel(const __grid_constant__ CUtensorMap tmap, StepArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -585,14 +484,11 @@ __global__ void __launch_bounds__(kThreads) decode_step_kernel(const __grid_cons
     uint16_t *q_rot = reinterpret_cast<uint16_t *>(sm.extra);  // [4][64] query rows (rotated when APPEND)
     uint16_t *new_kv = q_rot + kGroup * kD;                     // [2][64] rotated key row, value row
     int *ticket = reinterpret_cast<int *>(new_kv + 2 * kD);
-    float *merge = reinterpret_cast<float *>(sm.extra + kGridExtraBytes);  // CLUSTER: chunk slots
-    if (CLUSTER)
-        cluster_arrive_relaxed();  // phase 1: this CTA has started
     Timeline tl;
     tl.begin();
 
-    int g = blockIdx.x, b = blockIdx.y, c = blockIdx.z;  // CLUSTER: c is the rank in the cluster
-    if (!CLUSTER && a.sorted) {
+    int g = blockIdx.x, b = blockIdx.y, c = blockIdx.z;
+    if (a.sorted) {
         const int lin = blockIdx.x + kHkv * (blockIdx.y + gridDim.y * blockIdx.z);
         if (!sorted_unit(a, gridDim.y, lin, reinterpret_cast<int *>(sm.scratch), b, g, c)) {
             tl.none();
@@ -615,16 +511,12 @@ __global__ void __launch_bounds__(kThreads) decode_step_kernel(const __grid_cons
             grid_dependency_wait();
             write_zero_unit(a, b, g);
         }
-        if (CLUSTER)
-            cluster_leave();
         tl.none();
         return;
     }
     const int npages = (L + kPage - 1) / kPage;
     const int nchunks = chunks_of(a, L);
     if (c >= nchunks) {
-        if (CLUSTER)
-            cluster_leave();
         tl.none();
         return;
     }
@@ -673,7 +565,7 @@ __global__ void __launch_bounds__(kThreads) decode_step_kernel(const __grid_cons
     tl.stamp(3);
     allow_dependent_launch();
     // the stages are free now: they hold the combine area
-    finish_unit<APPEND, CLUSTER>(a, w, reinterpret_cast<float *>(sm.stages), ticket, merge, q_rot, b, g, c, nchunks);
+    finish_unit<APPEND>(a, w, reinterpret_cast<float *>(sm.stages), ticket, q_rot, b, g, c, nchunks);
     tl.end(b, c, jn);
 }
 
@@ -691,7 +583,7 @@ struct Fp8StepSmem {
     static constexpr int kBarsBytes = kWarps * STAGES * 8;
     static constexpr int kSortInts = kMaxPagesPerChunk + 1 + kWarps + 5;
     static constexpr int kExtraBytes = kGroup * kD * 2 + 2 * kD * 2 + 2 * kD + 16 + 16 + kSortInts * 4;
-    static constexpr int kBytes = 128 + kStagesBytes + kBarsBytes + kExtraBytes + 16;  // incl. alignment slack
+    static constexpr int kBytes = 128 + kStagesBytes + kBarsBytes + kExtraBytes;  // incl. alignment slack
     static_assert(kStagesBytes >= kWarps * kStateFloats * 4, "the combine reuses the stages");
     uint8_t *stages;
     uint64_t *bars;
@@ -701,7 +593,6 @@ struct Fp8StepSmem {
     float *new_scales;    // [2] their row scales
     int *ticket;
     int *sort_scratch;
-    float *merge;         // cluster merge slots (launches with the cluster merge: kMergeBytes more)
 
     __device__ __forceinline__ explicit Fp8StepSmem(uint8_t *raw)
     {
@@ -715,8 +606,6 @@ struct Fp8StepSmem {
         new_scales = reinterpret_cast<float *>(new_codes + 2 * kD);
         ticket = reinterpret_cast<int *>(new_scales + 4);
         sort_scratch = ticket + 4;
-        merge = reinterpret_cast<float *>(
-            (reinterpret_cast<uintptr_t>(sort_scratch + kSortInts) + 15) & ~uintptr_t(15));
     }
 };
 
@@ -740,18 +629,15 @@ __device__ __forceinline__ void put_new_token_fp8(uint8_t *unit, int slot, const
 // units of 2176 B in flight per SM; the other rings keep six (80 registers, none spilled).
 constexpr int fp8_ctas_per_sm(int stages) { return stages == 3 ? 7 : 6; }
 
-template <int STAGES, bool APPEND, bool CLUSTER>
+template <int STAGES, bool APPEND>
 __global__ void __launch_bounds__(kThreads, fp8_ctas_per_sm(STAGES))
     decode_step_fp8_kernel(const __grid_constant__ CUtensorMap tmap, StepArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
     Fp8StepSmem<STAGES> sm(smem_raw);
-    float *merge = sm.merge;  // CLUSTER: chunk slots
-    if (CLUSTER)
-        cluster_arrive_relaxed();  // phase 1: this CTA has started
 
-    int g = blockIdx.x, b = blockIdx.y, c = blockIdx.z;  // CLUSTER: c is the rank in the cluster
-    if (!CLUSTER && a.sorted) {
+    int g = blockIdx.x, b = blockIdx.y, c = blockIdx.z;
+    if (a.sorted) {
         const int lin = blockIdx.x + kHkv * (blockIdx.y + gridDim.y * blockIdx.z);
         if (!sorted_unit(a, gridDim.y, lin, sm.sort_scratch, b, g, c))
             return;
@@ -769,17 +655,12 @@ __global__ void __launch_bounds__(kThreads, fp8_ctas_per_sm(STAGES))
             grid_dependency_wait();
             write_zero_unit(a, b, g);
         }
-        if (CLUSTER)
-            cluster_leave();
         return;
     }
     const int npages = (L + kPage - 1) / kPage;
     const int nchunks = chunks_of(a, L);
-    if (c >= nchunks) {
-        if (CLUSTER)
-            cluster_leave();
+    if (c >= nchunks)
         return;
-    }
     const bool last_chunk = c == nchunks - 1;
     const int jn = min(npages - j0, a.pages_per_chunk);
     const int nmine = warp < jn ? (jn - warp + kWarps - 1) / kWarps : 0;
@@ -872,8 +753,7 @@ __global__ void __launch_bounds__(kThreads, fp8_ctas_per_sm(STAGES))
     }
     allow_dependent_launch();
     // the stages are free now: they hold the combine area
-    finish_unit<APPEND, CLUSTER>(a, w, reinterpret_cast<float *>(sm.stages), sm.ticket, merge, sm.q_rot, b, g, c,
-                                 nchunks);
+    finish_unit<APPEND>(a, w, reinterpret_cast<float *>(sm.stages), sm.ticket, sm.q_rot, b, g, c, nchunks);
 }
 
 // ------------------------------------------------------------------ launch
@@ -883,89 +763,69 @@ __global__ void __launch_bounds__(kThreads, fp8_ctas_per_sm(STAGES))
 // for 128-page chunks and for 16- to 32-page chunks of ragged batches respectively.
 int default_ring(int pages_per_chunk) { return pages_per_chunk >= 64 ? 3 : 2; }
 
-// Launch attributes: programmatic dependent launch (pdl) and, for the cluster merge, a
-// cluster of the chunk CTAs of one (sequence, KV head): dims 1 x 1 x max_chunks.
-struct LaunchAttrs {
-    cudaLaunchAttribute attrs[2];
-    unsigned n = 0;
-    LaunchAttrs(bool pdl, int cluster_z)
-    {
-        if (pdl)
-            attrs[n++] = pdl_attribute();
-        if (cluster_z > 0) {
-            attrs[n].id = cudaLaunchAttributeClusterDimension;
-            attrs[n].val.clusterDim.x = 1;
-            attrs[n].val.clusterDim.y = 1;
-            attrs[n].val.clusterDim.z = (unsigned)cluster_z;
-            ++n;
-        }
-    }
-};
-
-template <class Warp, int STAGES, bool APPEND, bool CLUSTER>
+template <class Warp, int STAGES, bool APPEND>
 int launch_grid(const CUtensorMap *tmap, const StepArgs &a, int B, cudaStream_t s, bool pdl)
 {
-    auto kernel = decode_step_kernel<Warp, STAGES, APPEND, CLUSTER>;
-    constexpr int smem = SmemLayout<STAGES>::kBaseBytes + kGridExtraBytes + (CLUSTER ? kMergeBytes : 0);
+    auto kernel = decode_step_kernel<Warp, STAGES, APPEND>;
+    constexpr int smem = SmemLayout<STAGES>::kBaseBytes + kGridExtraBytes;
     static PerDeviceOnce attr;
     if (const int st = ensure_smem_attr(attr, kernel, smem); st != PKV_OK)
         return st;
-    LaunchAttrs la(pdl, CLUSTER ? a.max_chunks : 0);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(kHkv, B, a.max_chunks);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cfg.attrs = la.attrs;
-    cfg.numAttrs = la.n;
+    cudaLaunchAttribute attrs[1] = {pdl_attribute()};
+    cfg.attrs = attrs;
+    cfg.numAttrs = pdl ? 1 : 0;
     return status_from_cuda(cudaLaunchKernelEx(&cfg, kernel, *tmap, a));
 }
 
 // FP8 pages: ring depth per warp 2..4 units (2176 B each).
-template <int STAGES, bool APPEND, bool CLUSTER>
+template <int STAGES, bool APPEND>
 int launch_fp8_grid(const CUtensorMap *tmap, const StepArgs &a, int B, cudaStream_t s, bool pdl)
 {
-    auto kernel = decode_step_fp8_kernel<STAGES, APPEND, CLUSTER>;
-    constexpr int smem = Fp8StepSmem<STAGES>::kBytes + (CLUSTER ? kMergeBytes : 0);
+    auto kernel = decode_step_fp8_kernel<STAGES, APPEND>;
+    constexpr int smem = Fp8StepSmem<STAGES>::kBytes;
     static PerDeviceOnce attr;
     if (const int st = ensure_smem_attr(attr, kernel, smem); st != PKV_OK)
         return st;
-    LaunchAttrs la(pdl, CLUSTER ? a.max_chunks : 0);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(kHkv, B, a.max_chunks);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cfg.attrs = la.attrs;
-    cfg.numAttrs = la.n;
+    cudaLaunchAttribute attrs[1] = {pdl_attribute()};
+    cfg.attrs = attrs;
+    cfg.numAttrs = pdl ? 1 : 0;
     return status_from_cuda(cudaLaunchKernelEx(&cfg, kernel, *tmap, a));
 }
 
-template <bool APPEND, bool CLUSTER>
+template <bool APPEND>
 int launch_fp8_depth(const CUtensorMap *tmap, const StepArgs &a, int B, cudaStream_t s, bool pdl, int depth)
 {
     switch (depth) {
-    case 2: return launch_fp8_grid<2, APPEND, CLUSTER>(tmap, a, B, s, pdl);
-    case 3: return launch_fp8_grid<3, APPEND, CLUSTER>(tmap, a, B, s, pdl);
-    default: return launch_fp8_grid<4, APPEND, CLUSTER>(tmap, a, B, s, pdl);
+    case 2: return launch_fp8_grid<2, APPEND>(tmap, a, B, s, pdl);
+    case 3: return launch_fp8_grid<3, APPEND>(tmap, a, B, s, pdl);
+    default: return launch_fp8_grid<4, APPEND>(tmap, a, B, s, pdl);
     }
 }
 
-// Ring depth per warp: 2 stages (36 KB per CTA, 6 CTAs per SM; 44 KB and 5 with the cluster
-// merge), 3 (4 per SM) or 4 (3 per SM).
-template <class Warp, bool APPEND, bool CLUSTER>
+// Ring depth per warp: 2 stages (36 KB per CTA, 6 CTAs per SM), 3 (4 per SM) or 4 (3 per SM).
+template <class Warp, bool APPEND>
 int launch_grid_depth(const CUtensorMap *tmap, const StepArgs &a, int B, cudaStream_t s, bool pdl, int depth)
 {
     switch (depth) {
-    case 2: return launch_grid<Warp, 2, APPEND, CLUSTER>(tmap, a, B, s, pdl);
-    case 3: return launch_grid<Warp, 3, APPEND, CLUSTER>(tmap, a, B, s, pdl);
-    default: return launch_grid<Warp, 4, APPEND, CLUSTER>(tmap, a, B, s, pdl);
+    case 2: return launch_grid<Warp, 2, APPEND>(tmap, a, B, s, pdl);
+    case 3: return launch_grid<Warp, 3, APPEND>(tmap, a, B, s, pdl);
+    default: return launch_grid<Warp, 4, APPEND>(tmap, a, B, s, pdl);
     }
 }
 
 // Option bits both entry points accept for the fused grid kernel.
 constexpr int kGridOptions = 0xff | PKV_STEP_NO_PDL | PKV_STEP_GRID | PKV_STEP_RING_MASK | PKV_STEP_SORTED |
-                             PKV_STEP_TEST_EXPIRE_WAIT | PKV_STEP_TICKET_MERGE;
+                             PKV_STEP_TEST_EXPIRE_WAIT;
 
 // Validates the options, fills the launch-dependent fields of `a` and launches the
 // kernel for the pool's format.
@@ -1003,17 +863,10 @@ int launch_fused(const pkv_pool *pool, StepArgs &a, int B, int max_blocks, int p
     a.expire_seq = (options & PKV_STEP_TEST_EXPIRE_WAIT) ? 0 : -1;
     const bool pdl = take_pdl_permission(pool, !(options & PKV_STEP_NO_PDL));
     const int depth = ring ? ring : default_ring(pages_per_chunk);
-    // the cluster merge: 2..8 chunk slots, grid order, the MMA policy (the SIMT policy and
-    // the sorted dispatch keep the ticket merge)
-    const bool cluster = max_chunks >= 2 && max_chunks <= kMaxClusterChunks && !a.sorted &&
-                         variant != PKV_DECODE_SIMT && !(options & PKV_STEP_TICKET_MERGE);
     if (pool->kv_format == PKV_KV_FP8)
-        return cluster ? launch_fp8_depth<APPEND, true>(tmap, a, B, s, pdl, depth)
-                       : launch_fp8_depth<APPEND, false>(tmap, a, B, s, pdl, depth);
-    if (variant == PKV_DECODE_SIMT)
-        return launch_grid_depth<SimtWarp, APPEND, false>(tmap, a, B, s, pdl, depth);
-    return cluster ? launch_grid_depth<MmaWarp, APPEND, true>(tmap, a, B, s, pdl, depth)
-                   : launch_grid_depth<MmaWarp, APPEND, false>(tmap, a, B, s, pdl, depth);
+        return launch_fp8_depth<APPEND>(tmap, a, B, s, pdl, depth);
+    return variant == PKV_DECODE_SIMT ? launch_grid_depth<SimtWarp, APPEND>(tmap, a, B, s, pdl, depth)
+                                      : launch_grid_depth<MmaWarp, APPEND>(tmap, a, B, s, pdl, depth);
 }
 
 }  // namespace

@@ -47,7 +47,6 @@ PKV_STEP_RING_MASK = 0xF000
 PKV_STEP_SORTED = 0x20000
 PKV_STEP_TEST_EXPIRE_WAIT = 0x40000
 PKV_DECODE_SPLIT_MERGE = 0x80000
-PKV_STEP_TICKET_MERGE = 0x100000
 
 
 def PKV_STEP_RING(n: int) -> int:
