@@ -248,20 +248,18 @@ def test_run_host_steps_rotating_buffers(chains, buffers):
 
 @pytest.mark.parametrize("kv", ["bf16", "fp8"])
 @pytest.mark.parametrize("chunk", [16, 20, 43, 64])   # 8, 7, 3 and 2 chunk slots at 128 table entries
-def test_cluster_merge_equals_ticket_merge_and_split_merge(kv, chunk):
-    # the default merge for 2..8 chunk slots runs the chunk CTAs of a (sequence, KV head) as a
-    # thread-block cluster; it must give the ticket merge's and the two-kernel form's bits
+def test_in_kernel_merge_equals_two_kernel_form(kv, chunk):
+    # the fused step and the default attention call merge chunk partials inside the launch
+    # (ticket); the two-kernel form merges them in a second kernel: same bits
     from tests import test_gpu_fp8 as f8
 
     lens = [2048, 1, 16, 17, 320, 321, 1000, 640, 641, 1500, 33, 2047]
     c = (f8.make_case if kv == "fp8" else make_case)(38, lens, max_blocks=128)
     pool = c["pool"].view(np.uint8)
 
-    def run(fused, options):
+    def run(fused, split_merge):
         eng = DecodeEngine(c["num_pages"], 1, c["B"], c["max_blocks"], chunk, kv=kv, fused=fused,
-                           split_merge=bool(options & pkv.PKV_DECODE_SPLIT_MERGE))
-        eng.step_options |= options & pkv.PKV_STEP_TICKET_MERGE
-        eng.attn_options |= options & pkv.PKV_STEP_TICKET_MERGE
+                           split_merge=split_merge)
         eng.slab.copy_(torch.from_numpy(pool).cuda())
         eng.set_tables(c["bt"][None])
         lens_d = torch.from_numpy(c["seq_lens"]).cuda()
@@ -277,16 +275,14 @@ def test_cluster_merge_equals_ticket_merge_and_split_merge(kv, chunk):
         eng.close()
         return res
 
-    cluster = run(True, 0)
-    ticket = run(True, pkv.PKV_STEP_TICKET_MERGE)
-    sep = run(False, 0)
-    two_kernel = run(False, pkv.PKV_DECODE_SPLIT_MERGE)
-    for r in (cluster, ticket, sep, two_kernel):
+    fused = run(True, False)
+    sep = run(False, False)
+    two_kernel = run(False, True)
+    for r in (fused, sep, two_kernel):
         assert r["st"] == pkv.PKV_OK and r["flag"] == 0 and np.all(r["counters"] == 0)
         assert np.array_equal(r["out"][0], r["out"][1])
-    for r in (ticket, sep, two_kernel):
-        assert np.array_equal(cluster["out"][0], r["out"][0])
-        assert np.array_equal(cluster["pool"], r["pool"])
-    assert np.array_equal(cluster["q"], ticket["q"])
+    for r in (sep, two_kernel):
+        assert np.array_equal(fused["out"][0], r["out"][0])
+        assert np.array_equal(fused["pool"], r["pool"])
     ref = (f8.oracle_run if kv == "fp8" else oracle_run)(c)
-    assert_close(cluster["out"][0], ref["out_f64"])
+    assert_close(fused["out"][0], ref["out_f64"])
