@@ -513,7 +513,7 @@ def run_settings(args, config: str, kv: str = "bf16", path: str = "fused", split
         a.pages_per_chunk = DEFAULT_CHUNK[config]
         a.ring = (DEFAULT_RING if kv == "bf16" else DEFAULT_RING_FP8)[config]
         a.sorted = DEFAULT_SORTED[config] and not split_merge
-        a.chains = (DEFAULT_CHAINS if kv == "bf16" else DEFAULT_CHAINS_FP8)[config]
+        a.chains = LAUNCH.chains(config, kv, path)
         a.no_pdl = False
     if steps is not None:
         a.steps = steps
@@ -820,7 +820,7 @@ def main(argv=None):
     if args.split_merge and args.path != "separate":
         raise SystemExit("--split-merge selects the separate path's two-kernel attention (--path separate)")
     if args.chains is None:
-        args.chains = (DEFAULT_CHAINS if args.kv == "bf16" else DEFAULT_CHAINS_FP8)[args.config]
+        args.chains = LAUNCH.chains(args.config, args.kv, args.path)
     if args.impl == "reference":
         return run_reference(args)
     if args.config == "trace":

@@ -27,11 +27,23 @@ SORTED = {"tiny": True, "b256": False, "b64": False, "b8": True, "trace": False}
 # each step, where more launches cost more than the overlap gains
 CHAINS = {"tiny": 2, "b256": 2, "b64": 8, "b8": 1, "trace": 1}
 CHAINS_FP8 = {"tiny": 2, "b256": 2, "b64": 8, "b8": 1, "trace": 1}
+# the two named calls per layer (pkv_append_rope, then pkv_decode_attention): twice the
+# launches, whose latencies more chains hide (b64: 16 chains 0.205 ms per step, 8 chains 0.215)
+CHAINS_SEPARATE = {"tiny": 2, "b256": 2, "b64": 16, "b8": 1, "trace": 1}
 
 
-def config(name: str, kv: str = "bf16") -> dict:
+def chains(name: str, kv: str = "bf16", path: str = "fused") -> int:
+    """Micro-batch chains of workload ``name`` for ``kv`` pages on the fused or separate path."""
+    if path == "separate":
+        return CHAINS_SEPARATE[name]
+    return (CHAINS if kv == "bf16" else CHAINS_FP8)[name]
+
+
+def config(name: str, kv: str = "bf16", path: str = "fused") -> dict:
     """Keyword arguments of ``harness.setup`` for workload ``name`` with ``kv`` pages."""
     if kv not in ("bf16", "fp8"):
         raise ValueError(f"kv must be 'bf16' or 'fp8', not {kv!r}")
+    if path not in ("fused", "separate"):
+        raise ValueError(f"path must be 'fused' or 'separate', not {path!r}")
     return {"pages_per_chunk": CHUNK[name], "ring": (RING if kv == "bf16" else RING_FP8)[name],
-            "sorted_units": SORTED[name], "chains": (CHAINS if kv == "bf16" else CHAINS_FP8)[name], "kv": kv}
+            "sorted_units": SORTED[name], "chains": chains(name, kv, path), "kv": kv, "fused": path == "fused"}

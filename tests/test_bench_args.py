@@ -44,7 +44,7 @@ def test_explicit_flags_win(captured):
 def test_separate_path_options(captured):
     # the separate path (pkv_append_rope + pkv_decode_attention) takes the workload's chains
     bench.main(["--path", "separate", "--config", "b64"])
-    assert captured["args"].chains == launch.CHAINS["b64"] and not captured["args"].split_merge
+    assert captured["args"].chains == launch.CHAINS_SEPARATE["b64"] and not captured["args"].split_merge
     bench.main(["--path", "separate", "--chains", "2", "--split-merge"])
     a = captured["args"]
     assert a.chains == 2 and a.split_merge and a.sorted is False

@@ -11,11 +11,15 @@ from paged_kv_decode_12_gb300.engine import chain_bounds
 def test_launch_config_covers_every_workload():
     for name in ("tiny", "b8", "b64", "b256", "trace"):
         for kv in ("bf16", "fp8"):
-            c = launch.config(name, kv)
-            assert set(c) == {"pages_per_chunk", "ring", "sorted_units", "chains", "kv"}
-            assert 1 <= c["pages_per_chunk"] <= 128 and c["ring"] in (2, 3, 4) and c["chains"] >= 1
+            for path in ("fused", "separate"):
+                c = launch.config(name, kv, path)
+                assert set(c) == {"pages_per_chunk", "ring", "sorted_units", "chains", "kv", "fused"}
+                assert 1 <= c["pages_per_chunk"] <= 128 and c["ring"] in (2, 3, 4) and c["chains"] >= 1
+                assert c["fused"] == (path == "fused") and c["chains"] == launch.chains(name, kv, path)
     with pytest.raises(ValueError):
         launch.config("b64", "int4")
+    with pytest.raises(ValueError):
+        launch.config("b64", "bf16", "split")
 
 
 def test_chain_bounds_even_split():
