@@ -1,4 +1,12 @@
-// pkv_decode.cu -- paged decode attention: split-sequence kernel + log-sum-exp merge.
+// pkv_decode.cu -- paged decode attention: the entry points, and the two-kernel form
+// (split-sequence kernel + log-sum-exp merge kernel).
+//
+// pkv_decode_attention runs, by default, the grid kernel of pkv_step.cu without the
+// append: the same unit of work as below, with the chunk partials merged inside the
+// same launch.  The two-kernel form here (PKV_DECODE_SPLIT_MERGE) keeps the merge in a
+// second small kernel; it needs no zeroed workspace, which is why the allocation-free
+// entry point uses it.  Both merge in chunk order with the same arithmetic, so their
+// results are identical bit for bit.
 //
 // What is computed (samir-vllm README summary, "从零用 C++ 和 CUDA 实现 Llama 3.2 1B
 // 推理引擎", section "目前已完成的功能": each query head streams its sequence's
@@ -39,7 +47,6 @@
 #include <cuda_bf16.h>
 
 #include <cmath>
-#include <mutex>
 
 #include "pkv_device.cuh"
 
