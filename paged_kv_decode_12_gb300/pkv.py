@@ -368,22 +368,36 @@ def pkv_sched_submit(sched, rid: int, prompt_tokens: int, max_new_tokens: int) -
     _check(lib().pkv_sched_submit(sched, int(rid), int(prompt_tokens), int(max_new_tokens)), "pkv_sched_submit")
 
 
-def pkv_sched_admit(sched, max_n: int, layers: int, max_blocks: int):
-    """Returns (ids int64 [n], prompt_lens int32 [n], bt_rows int32 [n][layers][max_blocks])."""
-    ids = np.empty(max_n, dtype=np.int64)
-    lens = np.empty(max_n, dtype=np.int32)
-    bt = np.empty((max_n, layers, max_blocks), dtype=np.int32)
+def _out_array(given, size: int, dtype):
+    """A caller's output array (C-contiguous, of ``dtype``, at least ``size`` elements), flat."""
+    if given is None:
+        return np.empty(size, dtype=dtype)
+    flat = given.reshape(-1)
+    if flat.dtype != dtype or flat.size < size or not flat.flags["C_CONTIGUOUS"] or not np.shares_memory(flat, given):
+        raise ValueError(f"output array must be C-contiguous {np.dtype(dtype).name} with >= {size} elements")
+    return flat
+
+
+def pkv_sched_admit(sched, max_n: int, layers: int, max_blocks: int, ids_out=None, lens_out=None, bt_out=None):
+    """Returns (ids int64 [n], prompt_lens int32 [n], bt_rows int32 [n][layers][max_blocks]),
+    written into the given arrays (e.g. views of pinned host memory) if any."""
+    ids = _out_array(ids_out, max_n, np.int64)
+    lens = _out_array(lens_out, max_n, np.int32)
+    bt = _out_array(bt_out, max_n * layers * max_blocks, np.int32).reshape(max_n, layers, max_blocks)
     n = ctypes.c_int(0)
     _check(lib().pkv_sched_admit(sched, max_n, ids.ctypes.data_as(_i64p), lens.ctypes.data_as(_i32p),
                                  bt.ctypes.data_as(_i32p), ctypes.byref(n)), "pkv_sched_admit")
     return ids[:n.value], lens[:n.value], bt[:n.value]
 
 
-def pkv_sched_decode_batch(sched, max_b: int, layers: int, max_blocks: int):
-    """Returns (ids int64 [B], seq_lens int32 [B], bt int32 [layers][B][max_blocks])."""
-    ids = np.empty(max_b, dtype=np.int64)
-    lens = np.empty(max_b, dtype=np.int32)
-    bt = np.empty(layers * max_b * max_blocks, dtype=np.int32)
+def pkv_sched_decode_batch(sched, max_b: int, layers: int, max_blocks: int, ids_out=None, lens_out=None,
+                           bt_out=None):
+    """Returns (ids int64 [B], seq_lens int32 [B], bt int32 [layers][B][max_blocks]), written
+    into the given arrays (e.g. views of pinned host memory) if any; bt is compact: layer l's
+    rows start at l * B * max_blocks."""
+    ids = _out_array(ids_out, max_b, np.int64)
+    lens = _out_array(lens_out, max_b, np.int32)
+    bt = _out_array(bt_out, layers * max_b * max_blocks, np.int32)
     B = ctypes.c_int(0)
     _check(lib().pkv_sched_decode_batch(sched, max_b, ids.ctypes.data_as(_i64p), lens.ctypes.data_as(_i32p),
                                         bt.ctypes.data_as(_i32p), ctypes.byref(B)), "pkv_sched_decode_batch")

@@ -81,9 +81,21 @@ class TraceRunner:
         self.v_new = draw((layers, max_batch, wl.NUM_KV_HEADS, wl.HEAD_DIM), seed + 3)
         self.out = torch.zeros((layers, max_batch, wl.NUM_Q_HEADS, wl.HEAD_DIM), dtype=torch.bfloat16,
                                device=self.device)
-        self.bt = torch.full((layers, max_batch, max_blocks), -1, dtype=torch.int32, device=self.device)
+        # block tables of a decode step, compact [layers][B][max_blocks] (layer stride B x max_blocks)
+        self.bt = torch.full((layers * max_batch * max_blocks,), -1, dtype=torch.int32, device=self.device)
         self.lens = torch.zeros(max_batch, dtype=torch.int32, device=self.device)
-        self.prompt_bt = torch.full((layers, max_blocks), -1, dtype=torch.int32, device=self.device)
+        self.prompt_bt = torch.full((max_batch, layers, max_blocks), -1, dtype=torch.int32, device=self.device)
+        # two sets of pinned host buffers that the scheduler writes into directly and that are
+        # copied to the device asynchronously; a set is rewritten only after the copies out of
+        # it have finished (its event), so the host schedules a step while earlier ones run
+        def pinned(n, dtype):
+            return torch.empty(n, dtype=dtype).pin_memory()
+
+        self._stage = [dict(ids=np.empty(max_batch, np.int64), lens=pinned(max_batch, torch.int32),
+                            bt=pinned(layers * max_batch * max_blocks, torch.int32),
+                            pids=np.empty(max_batch, np.int64), plens=np.empty(max_batch, np.int32),
+                            pbt=pinned(max_batch * layers * max_blocks, torch.int32), ev=None) for _ in range(2)]
+        self._nstage = 0
         self.launches = 0
         # every decode call gets its arguments as addresses computed from these bases and row
         # strides (no tensor views per call: the trace launches from the host every step)
@@ -115,37 +127,42 @@ class TraceRunner:
         v = torch.randn(shape, generator=g, device=self.device, dtype=torch.float32).to(torch.bfloat16)
         return k, v
 
-    def prefill(self, bt_rows: np.ndarray, prompt_len: int, rid: int = -1):
-        """Fill one prompt's pages in every layer with seeded N(0,1) K/V."""
-        self.prompt_bt.copy_(torch.from_numpy(bt_rows))
+    def prefill(self, bt_rows, prompt_len: int, rid: int = -1, slot: int = 0):
+        """Fill one prompt's pages in every layer with seeded N(0,1) K/V.  ``bt_rows``
+        [layers][max_blocks]: a device tensor (row ``slot`` of the prompt tables, already
+        uploaded) or host rows (copied to that row first)."""
+        rows = self.prompt_bt[slot]
+        if not isinstance(bt_rows, torch.Tensor) or not bt_rows.is_cuda:
+            rows.copy_(torch.as_tensor(np.asarray(bt_rows)))
         self._prompt_seed += 1
         self.prompt_seeds[rid] = (self._prompt_seed, prompt_len)
         k, v = self.prompt_kv(self._prompt_seed, prompt_len)
-        pkv.pkv_prefill_append(self.pool, k, v, self.prompt_bt, self.max_blocks, self.layers, 0, prompt_len,
-                               self.rope, self.max_context, self.err)
+        pkv.pkv_prefill_append(self.pool, k, v, rows, self.max_blocks, self.layers, 0, prompt_len, self.rope,
+                               self.max_context, self.err)
         self.launches += 1
 
-    def _layers(self, r0: int, r1: int, ws, stream=None):
-        """Every layer of one decode step for batch rows r0..r1-1 (contiguous slices of the
-        per-layer [max_batch] arrays, passed as addresses)."""
+    def _layers(self, r0: int, r1: int, B: int, ws, stream=None):
+        """Every layer of one decode step for batch rows r0..r1-1 of B (contiguous slices of
+        the per-layer [max_batch] arrays and of the compact [layers][B] tables, as addresses)."""
         self.launches += self.layers
         a, st = self._base, self._stride
         ws_ptr, lens = ws.data_ptr(), a["lens"] + 4 * r0
         stream = torch.cuda.current_stream(self.device).cuda_stream if stream is None else stream.cuda_stream
-        # one library call for all layers: layer l's rows are r0.. of layer l's [max_batch] arrays
+        # one library call for all layers: layer l's rows are r0.. of layer l's arrays
         pkv.pkv_decode_step_layers(self.pool, self.layers, a["k"] + r0 * st["kv"], a["v"] + r0 * st["kv"],
                                    a["q"] + r0 * st["q"], a["bt"] + r0 * st["bt"], self.max_blocks, lens, r1 - r0,
                                    a["rope"], self.max_context, self.scale, self.pages_per_chunk, ws_ptr,
                                    self.ws_bytes, a["out"] + r0 * st["q"], a["err"], stream, self.options,
                                    self.max_batch * st["kv"] // 2, self.max_batch * st["q"] // 2,
-                                   self.max_batch * st["bt"] // 4)
+                                   B * st["bt"] // 4)
 
     def decode(self, B: int, lens_host=None):
-        """All layers of one decode step over the first B batch rows; with chains, as
-        micro-batch chains cut by the rows' page counts (``lens_host``)."""
+        """All layers of one decode step over the first B batch rows (tables: compact
+        [layers][B][max_blocks]); with chains, as micro-batch chains cut by the rows' page
+        counts (``lens_host``)."""
         k = min(self.chains, B)
         if k <= 1:
-            self._layers(0, B, self.ws)
+            self._layers(0, B, B, self.ws)
             return
         from .engine import chain_bounds
 
@@ -155,7 +172,7 @@ class TraceRunner:
         for i in range(k):
             s = self.chain_streams[i]
             s.wait_event(self._fork)
-            self._layers(bounds[i], bounds[i + 1], self.chain_ws[i], s)
+            self._layers(bounds[i], bounds[i + 1], B, self.chain_ws[i], s)
             self._joins[i].record(s)
         for i in range(k):
             cur.wait_event(self._joins[i])
@@ -171,6 +188,7 @@ class TraceRunner:
         timed = []
         self.launches = 0
         per_token = wl.kv_bytes_per_token(self.layers, kv=self.kv)
+        row = self.layers * self.max_blocks
         t0 = time.perf_counter()
         for step in range(steps):
             for r in by_step.get(step, []):
@@ -179,17 +197,30 @@ class TraceRunner:
                 except pkv.PkvError as e:
                     if e.status != pkv.PKV_ERR_BUDGET_EXCEEDS_POOL:
                         raise
-            ids, plens, bt_rows = pkv.pkv_sched_admit(self.sched, self.max_batch, self.layers, self.max_blocks)
+            st = self._stage[self._nstage % 2]
+            self._nstage += 1
+            if st["ev"] is not None:
+                st["ev"].synchronize()  # the copies out of this set (two steps ago) are done
+            ids, plens, bt_rows = pkv.pkv_sched_admit(self.sched, self.max_batch, self.layers, self.max_blocks,
+                                                      st["pids"], st["plens"], st["pbt"].numpy())
+            if ids.size:
+                self.prompt_bt.view(-1)[: ids.size * row].copy_(st["pbt"][: ids.size * row], non_blocking=True)
             for i in range(ids.size):
-                self.prefill(bt_rows[i], int(plens[i]), int(ids[i]))
-            ids, lens, bt = pkv.pkv_sched_decode_batch(self.sched, self.max_batch, self.layers, self.max_blocks)
+                self.prefill(self.prompt_bt[i], int(plens[i]), int(ids[i]), i)
+            ids, lens, bt = pkv.pkv_sched_decode_batch(self.sched, self.max_batch, self.layers, self.max_blocks,
+                                                       st["ids"], st["lens"].numpy(), st["bt"].numpy())
             B = ids.size
             sizes.append(B)
+            if B:
+                self.lens[:B].copy_(st["lens"][:B], non_blocking=True)
+                self.bt[: B * row].copy_(st["bt"][: B * row], non_blocking=True)
+            st["ev"] = torch.cuda.Event()
+            st["ev"].record()  # after every copy out of this set (prompt tables included)
             if B == 0:
                 continue
-            self.lens[:B].copy_(torch.from_numpy(lens))
-            self.bt[:, :B].copy_(torch.from_numpy(bt))
             self.q[:, :B].copy_(self.q0[:, :B])
+            if before_step or after_step:   # the callbacks keep what they see: copies
+                ids, lens, bt = ids.copy(), lens.copy(), bt.copy()
             if before_step:
                 before_step(step, ids, lens, bt)
             start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
