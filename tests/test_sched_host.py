@@ -211,3 +211,37 @@ def test_random_trace_matches_reference(seed, static):
         assert st["admission_waits"] == ref.waits
     pkv.pkv_sched_destroy(s)
     pkv.pkv_pool_destroy(pool)
+
+
+def test_outputs_written_into_given_arrays():
+    # the trace runner hands the scheduler views of pinned host buffers; the results must be
+    # exactly those of the wrapper-allocated call, written in place (the block tables of a
+    # decode batch compact: layer l's rows start at l * B * max_blocks)
+    results = []
+    for given in (False, True):
+        pool, sched = make(64, layers=2, max_blocks=8, max_batch=4)
+        for rid, (p, n) in enumerate([(20, 5), (40, 3), (3, 9)]):
+            pkv.pkv_sched_submit(sched, rid, p, n)
+        bufs = dict(ids_out=np.full(4, -7, np.int64), lens_out=np.full(4, -7, np.int32),
+                    bt_out=np.full(4 * 2 * 8, -7, np.int32)) if given else {}
+        a = pkv.pkv_sched_admit(sched, 4, 2, 8, **bufs)
+        if given:
+            assert np.shares_memory(a[2], bufs["bt_out"]) and np.shares_memory(a[0], bufs["ids_out"])
+        dbufs = dict(ids_out=np.full(4, -7, np.int64), lens_out=np.full(4, -7, np.int32),
+                     bt_out=np.full(2 * 4 * 8, -7, np.int32)) if given else {}
+        d = pkv.pkv_sched_decode_batch(sched, 4, 2, 8, **dbufs)
+        if given:
+            B = d[0].size
+            assert np.array_equal(dbufs["bt_out"][: 2 * B * 8], d[2].reshape(-1))
+        results.append([np.array(x) for x in a + d])
+        pkv.pkv_sched_destroy(sched)
+        pkv.pkv_pool_destroy(pool)
+    for x, y in zip(*results):
+        assert np.array_equal(x, y)
+    pool, sched = make(8)
+    with pytest.raises(ValueError):     # too small / wrong dtype output arrays are refused
+        pkv.pkv_sched_decode_batch(sched, 4, 2, 8, bt_out=np.empty(10, np.int32))
+    with pytest.raises(ValueError):
+        pkv.pkv_sched_admit(sched, 4, 2, 8, ids_out=np.empty(4, np.int32))
+    pkv.pkv_sched_destroy(sched)
+    pkv.pkv_pool_destroy(pool)
