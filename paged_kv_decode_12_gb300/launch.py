@@ -14,8 +14,9 @@ from __future__ import annotations
 CHUNK = {"tiny": 1, "b256": 128, "b64": 20, "b8": 16, "trace": 32}
 # TMA stages per warp on the grid schedule, BF16 pages (4 KiB each)
 RING = {"tiny": 2, "b256": 3, "b64": 2, "b8": 2, "trace": 2}
-# TMA stages per warp, FP8 pages (units of 2176 B)
-RING_FP8 = {"tiny": 2, "b256": 3, "b64": 2, "b8": 2, "trace": 2}
+# TMA stages per warp, FP8 pages (units of 2176 B); b256 with 2 chains: ring 2 / 3 / 4 give
+# 1.352 / 1.337 / 1.320 ms per step (3 or 4 chains: the same)
+RING_FP8 = {"tiny": 2, "b256": 4, "b64": 2, "b8": 2, "trace": 2}
 # largest-first unit dispatch (PKV_STEP_SORTED): a gain on a ragged one-wave layer run as
 # one launch (b8); with micro-batch chains the grid order is faster (b64), and on b256
 # every unit has the same size
