@@ -656,6 +656,9 @@ def measure(a, rank, world, device, peak, peak_src, read_peak, with_cpu: bool):
 # further configurations measured beside the headline one in the default run: the other
 # 70 %-target batch (b64), the batch-8 shape, the two named calls per layer (b64), FP8 pages
 EXTRA_DEFAULT = ("b64", "b8", "b64:separate", "b64:fp8", "b256:fp8")
+# extra configurations that also carry a CPU baseline on their own GPU batch: b8 its whole
+# step, b64 one of its 16 layers (CPU_SAMPLE)
+EXTRA_CPU = ("b64", "b8")
 
 
 def parse_extra(spec: str):
@@ -700,7 +703,9 @@ def run_pkv(args):
             continue
         a = run_settings(args, config, kv, path, split,
                          steps=max(args.steps, args.extra_min_steps) if config != "b256" else args.steps)
-        extras[spec] = measure(a, rank, world, device, peak, peak_src, read_peak, with_cpu=False)
+        a.cpu_seconds = args.extra_cpu_seconds
+        with_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline and spec in EXTRA_CPU
+        extras[spec] = measure(a, rank, world, device, peak, peak_src, read_peak, with_cpu=with_cpu)
 
     line = {"metric": METRIC, "value": head["value"], "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
@@ -800,6 +805,9 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=8.0,
                     help="CPU baseline: seconds of oracle work, half single-threaded, half on every host core")
+    ap.add_argument("--extra-cpu-seconds", type=float, default=4.0,
+                    help="CPU baseline of the extra configurations " + ", ".join(EXTRA_CPU) + ": seconds of oracle "
+                         "work each")
     ap.add_argument("--ref-seqs", type=int, default=16, help="sequences per reference-arm step")
     ap.add_argument("--extra", default="default",
                     help="further configurations measured in the same run and reported under 'configs': "
