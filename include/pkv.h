@@ -313,13 +313,19 @@ int pkv_sched_submit(pkv_sched *sched, int64_t id, int prompt_tokens, int max_ne
 /* Admit waiting requests in FIFO order while credits and the batch cap allow (at
  * most max_n).  For each: its id, prompt length and block-table rows
  * bt_rows_out[i][layers][max_blocks] holding the pages of its prompt (allocated
- * now), for the caller's prefill.  *n_out = number admitted. */
+ * now), for the caller's prefill.  *n_out = number admitted.  The credits are the
+ * pool's free pages when the scheduler was created; if pages were taken from the
+ * pool outside the scheduler since, a head whose prompt pages are not all free keeps
+ * waiting (counted in admission_waits) and nothing of it is allocated. */
 int pkv_sched_admit(pkv_sched *sched, int max_n, int64_t *ids_out, int32_t *prompt_lens_out, int32_t *bt_rows_out,
                     int *n_out);
 /* Next decode step: retire requests whose last step has run, then append one token
  * to every active request (taking a new page per layer when it crosses a page
  * boundary) and return the batch: ids_out[B], seq_lens_out[B] (lengths after the
- * append) and bt_out[layers][B][max_blocks].  max_b bounds B. */
+ * append) and bt_out[layers][B][max_blocks].  max_b bounds B.  PKV_ERR_OUT_OF_PAGES
+ * only if pages were taken from the pool outside the scheduler: then no request
+ * advances (pages already taken for this step stay with their requests) and the
+ * call can be repeated once pages are back. */
 int pkv_sched_decode_batch(pkv_sched *sched, int max_b, int64_t *ids_out, int32_t *seq_lens_out, int32_t *bt_out,
                            int *B_out);
 /* Early stop (e.g. an end-of-sequence token): free the request's pages and credits

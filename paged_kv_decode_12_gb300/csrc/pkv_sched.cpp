@@ -20,6 +20,7 @@
 //    batching admits waiting requests whenever credits allow, static batching
 //    admits the next group only after the current group has finished
 //    (same page, "构建": --static / --continuous).
+#include <algorithm>
 #include <deque>
 #include <new>
 #include <unordered_set>
@@ -51,22 +52,31 @@ namespace {
 
 int64_t pages_for(int tokens) { return (tokens + PKV_PAGE_SIZE - 1) / PKV_PAGE_SIZE; }
 
-// Give every layer of r the pages it needs for `tokens` tokens (credits guarantee success).
+// Give every layer of r the pages it needs for `tokens` tokens, all or nothing.  The
+// credits guarantee success while the scheduler is the pool's only user; if pages were
+// taken from the pool outside it, the pages this call took go back and the status of the
+// failed allocation is returned, with r unchanged.
 int grow(pkv_sched *s, pkv_sched::Req &r, int tokens)
 {
     const int need = (int)pages_for(tokens);
     if (need > s->max_blocks)
         return PKV_ERR_INVALID_ARG;
+    if (need <= r.npages)
+        return PKV_OK;
+    const int add = need - r.npages;
     for (int l = 0; l < s->layers; ++l) {
-        for (int j = r.npages; j < need; ++j) {
-            int32_t id;
-            const int st = pkv_pool_alloc(s->pool, 1, &id);
-            if (st != PKV_OK)
-                return st;
-            r.pages[(size_t)l * s->max_blocks + j] = id;
-            ++s->allocated;
+        int32_t *row = &r.pages[(size_t)l * s->max_blocks];
+        const int st = pkv_pool_alloc(s->pool, add, row + r.npages);
+        if (st != PKV_OK) {
+            for (int k = 0; k < l; ++k) {  // undo the layers already grown
+                int32_t *done = &r.pages[(size_t)k * s->max_blocks] + r.npages;
+                (void)pkv_pool_free(s->pool, add, done);
+                std::fill(done, done + add, -1);
+            }
+            return st;
         }
     }
+    s->allocated += (int64_t)add * s->layers;
     r.npages = need;
     if (s->allocated > s->st.peak_allocated_pages)
         s->st.peak_allocated_pages = s->allocated;
@@ -189,13 +199,16 @@ int pkv_sched_admit(pkv_sched *s, int max_n, int64_t *ids_out, int32_t *prompt_l
             ++s->st.admission_waits;  // FIFO: nobody overtakes the head
             break;
         }
+        head.pages.assign((size_t)s->layers * s->max_blocks, -1);
+        if (grow(s, head, head.prompt) != PKV_OK) {
+            // pages were taken from the pool outside the scheduler: the head waits, as for
+            // credits, until enough pages are back
+            ++s->st.admission_waits;
+            break;
+        }
         pkv_sched::Req r = std::move(head);
         s->waiting.pop_front();
         s->free_credits -= r.budget_pages;
-        r.pages.assign((size_t)s->layers * s->max_blocks, -1);
-        const int st = grow(s, r, r.prompt);
-        if (st != PKV_OK)
-            return st;  // cannot happen while credits <= free pages
         r.length = r.prompt;
         r.remaining = r.allowed - 1;
         ids_out[n] = r.id;
@@ -224,11 +237,17 @@ int pkv_sched_decode_batch(pkv_sched *s, int max_b, int64_t *ids_out, int32_t *s
     const int B = (int)s->active.size();
     if (B > max_b)
         return PKV_ERR_INVALID_ARG;
+    // every new token's page first (lazily), then the step: a failed allocation advances
+    // no request, and the pages already taken stay with their requests (within budget)
+    for (int i = 0; i < B; ++i) {
+        const int st = grow(s, s->active[i], s->active[i].length + 1);
+        if (st != PKV_OK) {
+            refresh_free(s);
+            return st;
+        }
+    }
     for (int i = 0; i < B; ++i) {
         pkv_sched::Req &r = s->active[i];
-        const int st = grow(s, r, r.length + 1);  // the new token's page, lazily
-        if (st != PKV_OK)
-            return st;
         r.length += 1;
         r.remaining -= 1;
         ids_out[i] = r.id;

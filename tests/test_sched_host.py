@@ -245,3 +245,33 @@ def test_outputs_written_into_given_arrays():
         pkv.pkv_sched_admit(sched, 4, 2, 8, ids_out=np.empty(4, np.int32))
     pkv.pkv_sched_destroy(sched)
     pkv.pkv_pool_destroy(pool)
+
+
+def test_pages_taken_outside_the_scheduler():
+    # credits are the pool's free pages when the scheduler was created; pages a caller takes
+    # from the pool directly afterwards make allocations fail: admission then waits (nothing
+    # of the head is allocated) and a decode step advances no request until pages are back
+    pool, s = make(pages=12, layers=2)
+    outside = pkv.pkv_pool_alloc(pool, 9)                       # 3 pages left
+    pkv.pkv_sched_submit(s, 1, 48, 2)                           # 49 tokens: 4 pages x 2 layers of credit
+    ids, _, _ = pkv.pkv_sched_admit(s, 4, 2, 8)                 # its prompt needs 3 x 2 = 6 pages now
+    st = pkv.pkv_sched_get_stats(s)
+    assert ids.size == 0 and st["waiting"] == 1 and st["admission_waits"] == 1
+    assert st["allocated_pages"] == 0 and st["free_credits"] == 12 and st["final_free_pages"] == 3
+    pkv.pkv_pool_free(pool, outside[:6])                        # 9 free
+    ids, lens, bt = pkv.pkv_sched_admit(s, 4, 2, 8)
+    assert ids.tolist() == [1] and lens.tolist() == [48] and np.all(bt[0, :, :3] >= 0)
+    assert pkv.pkv_sched_get_stats(s)["allocated_pages"] == 6
+    again = pkv.pkv_pool_alloc(pool, 3)                         # the pool is empty now
+    with pytest.raises(pkv.PkvError) as e:                      # length 49 needs page 3 in both layers
+        pkv.pkv_sched_decode_batch(s, 4, 2, 8)
+    assert e.value.status == pkv.PKV_ERR_OUT_OF_PAGES
+    st = pkv.pkv_sched_get_stats(s)
+    assert st["allocated_pages"] == 6 and st["final_free_pages"] == 0
+    pkv.pkv_pool_free(pool, again)
+    ids, lens, bt = pkv.pkv_sched_decode_batch(s, 4, 2, 8)      # repeated: the request advances once
+    assert ids.tolist() == [1] and lens.tolist() == [49] and np.all(bt[:, 0, :4] >= 0)
+    assert pkv.pkv_sched_get_stats(s)["allocated_pages"] == 8
+    pkv.pkv_sched_destroy(s)
+    pkv.pkv_pool_free(pool, outside[6:])
+    pkv.pkv_pool_destroy(pool)
