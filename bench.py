@@ -800,7 +800,7 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--e2e-buffers", type=int, default=2, help="end-to-end input/output buffers in rotation "
                     "(at least twice --e2e-group)")
-    ap.add_argument("--e2e-group", type=int, default=4, help="end-to-end steps per captured graph replay")
+    ap.add_argument("--e2e-group", type=int, default=8, help="end-to-end steps per captured graph replay")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=8.0,
