@@ -393,6 +393,7 @@ def config_block(w, a, variant_name: str, graph: bool) -> dict:
             "ring": getattr(a, "ring", 0), "sorted_units": getattr(a, "sorted", False),
             "split_merge": getattr(a, "split_merge", False),
             "chains": getattr(a, "chains", 1),
+            "pipelined": getattr(a, "pipelined", False),
             "steps_per_graph": getattr(a, "steps_per_graph", None) if graph else None,
             "kv_pages": getattr(a, "kv", "bf16"),
             "kv_bytes_per_step": kv,
@@ -504,10 +505,12 @@ def run_trace(args):
 
 
 def run_settings(args, config: str, kv: str = "bf16", path: str = "fused", split_merge: bool = False,
-                 steps: int | None = None):
+                 steps: int | None = None, pipelined: bool | None = None):
     """Launch settings of one measured configuration: the workload's measured defaults
     (launch table), or the command line's for the headline configuration."""
     a = argparse.Namespace(**vars(args))
+    if pipelined is not None:
+        a.pipelined = pipelined
     if config != args.config or kv != args.kv or path != args.path or split_merge != args.split_merge:
         a.config, a.kv, a.path, a.split_merge = config, kv, path, split_merge
         a.pages_per_chunk = DEFAULT_CHUNK[config]
@@ -547,7 +550,8 @@ def measure(a, rank, world, device, peak, peak_src, read_peak, with_cpu: bool):
     dw.reset_q()
     ext = harness.external_events_supported()
     per_graph = max(1, min(a.steps, a.steps_per_graph))
-    warm_cap = harness.capture_steps(dw, max(1, min(a.warmup, per_graph)))
+    pipe = bool(getattr(a, "pipelined", False))
+    warm_cap = harness.capture_steps(dw, max(1, min(a.warmup, per_graph)), pipelined=pipe)
 
     # The timed steps replay one captured graph of per_graph steps (plus one graph for the
     # remainder): a serving loop replays the same graph every step, and many distinct graph
@@ -555,9 +559,9 @@ def measure(a, rank, world, device, peak, peak_src, read_peak, with_cpu: bool):
     # switch between.  The step time comes from these plain graphs: a timing event between
     # two launches would turn their programmatic (overlapping) dependency into a full one.
     n_full, rem = divmod(a.steps, per_graph)
-    timed = [harness.capture_steps(dw, per_graph)] * n_full
+    timed = [harness.capture_steps(dw, per_graph, pipelined=pipe)] * n_full
     if rem:
-        timed.append(harness.capture_steps(dw, rem))
+        timed.append(harness.capture_steps(dw, rem, pipelined=pipe))
     # per-launch durations: one instrumented graph of the same per_graph steps
     timed_ev = [harness.capture_steps(dw, per_graph, time_attention=True)] if ext else []
     torch.cuda.synchronize()
@@ -623,6 +627,8 @@ def measure(a, rank, world, device, peak, peak_src, read_peak, with_cpu: bool):
             achieved = kv_launch / (eff_ms / 1e3) / 1e9
             timing = ("GPU time per attention launch = step time / attention launches per step, from the timed "
                       "region (CUDA events on the caller's stream around it)" +
+                      ("; the micro-batch chains pipelined across the steps of a graph (joined once per graph, "
+                       "not after every step)" if pipe else "") +
                       (", which also holds the separate path's append launches" if a.path != "fused" else "") +
                       "; launch_alone: " + timing + ", the chains one after another")
         roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
@@ -654,8 +660,9 @@ def measure(a, rank, world, device, peak, peak_src, read_peak, with_cpu: bool):
 
 
 # further configurations measured beside the headline one in the default run: the other
-# 70 %-target batch (b64), the batch-8 shape, the two named calls per layer (b64), FP8 pages
-EXTRA_DEFAULT = ("b64", "b8", "b64:separate", "b64:fp8", "b256:fp8")
+# 70 %-target batch (b64), the batch-8 shape, the two named calls per layer (b64), FP8 pages,
+# and b64 with its micro-batch chains pipelined across steps (DecodeEngine.steps)
+EXTRA_DEFAULT = ("b64", "b8", "b64:separate", "b64:fp8", "b256:fp8", "b64:pipelined")
 # extra configurations that also carry a CPU baseline on their own GPU batch: b8 its whole
 # step, b64 one of its 16 layers (CPU_SAMPLE)
 EXTRA_CPU = ("b64", "b8")
@@ -663,7 +670,7 @@ EXTRA_CPU = ("b64", "b8")
 
 def parse_extra(spec: str):
     parts = spec.split(":")
-    config, kv, path, split = parts[0], "bf16", "fused", False
+    config, kv, path, split, pipelined = parts[0], "bf16", "fused", False, False
     for p in parts[1:]:
         if p == "fp8":
             kv = "fp8"
@@ -671,11 +678,13 @@ def parse_extra(spec: str):
             path = "separate"
         elif p == "split-merge":
             path, split = "separate", True
+        elif p == "pipelined":
+            pipelined = True
         else:
             raise SystemExit(f"unknown extra configuration part {p!r} in {spec!r}")
     if config not in DEFAULT_CHUNK or config == "trace":
         raise SystemExit(f"unknown extra configuration {spec!r}")
-    return config, kv, path, split
+    return config, kv, path, split, pipelined
 
 
 def run_pkv(args):
@@ -698,11 +707,13 @@ def run_pkv(args):
     extras = {}
     specs = EXTRA_DEFAULT if args.extra == "default" else tuple(x for x in args.extra.split(",") if x and x != "none")
     for spec in specs:
-        config, kv, path, split = parse_extra(spec)
-        if (config, kv, path, split) == (args.config, args.kv, args.path, args.split_merge):
+        config, kv, path, split, pipelined = parse_extra(spec)
+        if (config, kv, path, split, pipelined) == (args.config, args.kv, args.path, args.split_merge,
+                                                    args.pipelined):
             continue
         a = run_settings(args, config, kv, path, split,
-                         steps=max(args.steps, args.extra_min_steps) if config != "b256" else args.steps)
+                         steps=max(args.steps, args.extra_min_steps) if config != "b256" else args.steps,
+                         pipelined=pipelined)
         a.cpu_seconds = args.extra_cpu_seconds
         with_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline and spec in EXTRA_CPU
         extras[spec] = measure(a, rank, world, device, peak, peak_src, read_peak, with_cpu=with_cpu)
@@ -744,7 +755,7 @@ def measure_e2e(dw, args, world, device):
     n = max(group, args.e2e_steps // group * group)
     dw.eng.run_host_steps(io, outs, out_host, len(outs))   # eager first pass: every buffer once
     torch.cuda.synchronize()
-    graphs = dw.eng.step_graphs(io, outs, group)
+    graphs = dw.eng.step_graphs(io, outs, group, pipelined=bool(getattr(args, "pipelined", False)))
     dw.eng.run_host_steps(io, outs, out_host, len(outs), graphs=graphs, group=group)
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -760,7 +771,9 @@ def measure_e2e(dw, args, world, device):
             "path": "DecodeEngine.run_host_steps (per step: one H2D copy of the packed pinned inputs and one D2H "
                     f"copy of the output, through {len(outs)} rotating buffers on two copy streams so that they "
                     f"overlap the neighbouring steps' compute; the steps' kernels replay captured graphs of {group} "
-                    "steps, the copies are stream operations between the replays)", "steps_per_graph": group}
+                    "steps" + (" with the micro-batch chains pipelined across them" if getattr(args, "pipelined", False)
+                               else "") +
+                    ", the copies are stream operations between the replays)", "steps_per_graph": group}
 
 
 def main(argv=None):
@@ -792,6 +805,9 @@ def main(argv=None):
                          "group on its own stream (default: per workload, BF16 "
                          + ", ".join(f"{k} {v}" for k, v in DEFAULT_CHAINS.items()) + "; FP8 "
                          + ", ".join(f"{k} {v}" for k, v in DEFAULT_CHAINS_FP8.items()) + ")")
+    ap.add_argument("--pipelined", action="store_true",
+                    help="micro-batch chains pipelined across the steps of a captured graph "
+                         "(DecodeEngine.steps: joined once per graph instead of after every step)")
     ap.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
                     help="KV page format: BF16 (the engine's) or FP8 E4M3 with per-row scales")
     ap.add_argument("--seed", type=int, default=12)

@@ -19,6 +19,14 @@ groups, each group runs its own chain of per-layer launches on its own stream
 (forked from and joined back to the caller's stream), so one group's layer tail
 overlaps another group's streaming.  Layer order is kept inside every group;
 sequences never interact, so every output byte is the same as with one chain.
+
+``steps()`` runs several decode steps with the chains pipelined across the step
+boundaries: every chain runs its rows through step 0, 1, ... back to back and the
+chains are joined once, after the last step, instead of after every step.  Every
+step still appends one token to every sequence and attends over all of its pages;
+only the barrier that made all micro-batches finish step s before any began step
+s + 1 is gone (a micro-batch's next step depends on its own sequences only).  The
+bytes written are those of the same steps run one by one.
 """
 from __future__ import annotations
 
@@ -226,6 +234,33 @@ class DecodeEngine:
             return
         self._rows_layers(q, k_new, v_new, pos_dev, seq_lens_dev, out, stream, None, self.step_ws, layer_hook)
 
+    def steps(self, step_args, stream=None) -> None:
+        """Several decode steps, ``step_args`` a sequence of (q, k_new, v_new, pos_dev,
+        seq_lens_dev, out) tuples as for ``step``, in step order.  With micro-batch chains
+        each chain runs its rows through every step on its own stream (forked from the
+        caller's stream once, joined back once at the end); one chain runs the steps in
+        order on the caller's stream.  The results equal those of ``step`` called for each
+        tuple in turn."""
+        step_args = list(step_args)
+        if self.chains == 1:
+            for args in step_args:
+                self.step(*args, stream=stream)
+            return
+        cur = torch.cuda.current_stream(self.device) if stream is None else stream
+        fork = torch.cuda.Event()
+        fork.record(cur)
+        joins = []
+        for k, rows in enumerate(zip(self.chain_bounds[:-1], self.chain_bounds[1:])):
+            s = self.chain_streams[k]
+            s.wait_event(fork)
+            for q, k_new, v_new, pos_dev, seq_lens_dev, out in step_args:
+                self._rows_layers(q, k_new, v_new, pos_dev, seq_lens_dev, out, s, rows, self.chain_ws[k])
+            done = torch.cuda.Event()
+            done.record(s)
+            joins.append(done)
+        for done in joins:
+            cur.wait_event(done)
+
     def run_host(self, io: "PackedIO", out_dev, out_host, stream=None) -> None:
         """End-to-end step: one copy of the step's inputs (q, k_new, v_new, pos, seq_lens, packed
         back to back in pinned host memory) to the device, the step, one copy of the output back
@@ -235,21 +270,28 @@ class DecodeEngine:
         self.step(d["q"], d["k_new"], d["v_new"], d["pos"], d["seq_lens"], out_dev, stream)
         out_host.copy_(out_dev, non_blocking=True)
 
-    def step_graphs(self, io: "PackedIO", out_devs, group: int = 1) -> list:
+    def step_graphs(self, io: "PackedIO", out_devs, group: int = 1, pipelined: bool = False) -> list:
         """Captured CUDA graphs for ``run_host_steps``: with K = len(out_devs) buffers (a
         multiple of ``group``), graph j runs ``group`` consecutive steps, the i-th on device
-        input buffer j * group + i of ``io`` into ``out_devs[j * group + i]``.  Capture after a
-        first eager pass (kernel attributes and tensor maps are set up outside any capture)."""
+        input buffer j * group + i of ``io`` into ``out_devs[j * group + i]`` (``pipelined``:
+        through ``steps``, the chains joined once per graph).  Capture after a first eager
+        pass (kernel attributes and tensor maps are set up outside any capture)."""
         K = len(out_devs)
         if group < 1 or K % group:
             raise ValueError(f"{K} buffers do not split into graphs of {group} steps")
         graphs = []
         for j in range(K // group):
+            args = []
+            for k in range(j * group, (j + 1) * group):
+                d = io.buffer(k)
+                args.append((d["q"], d["k_new"], d["v_new"], d["pos"], d["seq_lens"], out_devs[k]))
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
-                for k in range(j * group, (j + 1) * group):
-                    d = io.buffer(k)
-                    self.step(d["q"], d["k_new"], d["v_new"], d["pos"], d["seq_lens"], out_devs[k])
+                if pipelined:
+                    self.steps(args)
+                else:
+                    for a in args:
+                        self.step(*a)
             graphs.append(g)
         return graphs
 

@@ -110,10 +110,13 @@ class CapturedSteps:
     split_events: list  # (start, end) event pairs around each attention launch, or []
 
 
-def capture_steps(dw: DeviceWorkload, steps: int, time_attention: bool = False) -> CapturedSteps:
+def capture_steps(dw: DeviceWorkload, steps: int, time_attention: bool = False,
+                  pipelined: bool = False) -> CapturedSteps:
     """Capture ``steps`` consecutive decode steps into one CUDA graph.  With
     ``time_attention`` an external timing event is recorded before and after every
-    attention launch inside the graph (each graph has its own events)."""
+    attention launch inside the graph (each graph has its own events).  ``pipelined``:
+    the steps through ``DecodeEngine.steps`` (micro-batch chains joined once, after the
+    last step)."""
     events = []
 
     def hook(layer, phase):
@@ -124,10 +127,15 @@ def capture_steps(dw: DeviceWorkload, steps: int, time_attention: bool = False) 
             events[-1][1] = torch.cuda.Event(enable_timing=True, external=True)
             events[-1][1].record()
 
+    if pipelined and time_attention:
+        raise ValueError("per-launch events need the steps one after another")
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
-        for _ in range(steps):
-            dw.step(layer_hook=hook if time_attention else None)
+        if pipelined:
+            dw.eng.steps([(dw.q, dw.k_new, dw.v_new, dw.pos, dw.seq_lens, dw.out)] * steps)
+        else:
+            for _ in range(steps):
+                dw.step(layer_hook=hook if time_attention else None)
     return CapturedSteps(g, steps, [tuple(e) for e in events])
 
 

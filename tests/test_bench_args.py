@@ -59,3 +59,19 @@ def test_trace_and_reference_arms(captured):
     assert captured["arm"] == "trace" and captured["args"].chains == launch.CHAINS["trace"]
     bench.main(["--impl", "reference", "--config", "b64"])
     assert captured["arm"] == "reference" and captured["args"].chains == launch.CHAINS["b64"]
+
+
+def test_extra_specs_and_pipelined_settings(captured):
+    assert bench.parse_extra("b64") == ("b64", "bf16", "fused", False, False)
+    assert bench.parse_extra("b64:fp8:pipelined") == ("b64", "fp8", "fused", False, True)
+    assert bench.parse_extra("b64:split-merge") == ("b64", "bf16", "separate", True, False)
+    for bad in ("b64:nope", "trace", "b99"):
+        with pytest.raises(SystemExit):
+            bench.parse_extra(bad)
+    for spec in bench.EXTRA_DEFAULT:     # every default extra parses
+        bench.parse_extra(spec)
+    bench.main(["--config", "b64", "--pipelined"])
+    args = captured["args"]
+    assert args.pipelined is True
+    a = bench.run_settings(args, "b64", pipelined=False)
+    assert a.pipelined is False and a.chains == launch.CHAINS["b64"] and args.pipelined is True
