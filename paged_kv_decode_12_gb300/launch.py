@@ -24,9 +24,11 @@ SORTED = {"tiny": True, "b256": False, "b64": False, "b8": True, "trace": False}
 # micro-batch chains: independent per-layer launch chains over contiguous row groups,
 # each on its own stream, so that one group's layer tail overlaps another's streaming.
 # Every chain adds a launch per layer: past 8 chains b64 gains nothing in multi-step
-# graphs and loses at one step per graph, and the trace launches eagerly from the host
-# each step, where more launches cost more than the overlap gains
-CHAINS = {"tiny": 2, "b256": 2, "b64": 8, "b8": 1, "trace": 1}
+# graphs and loses at one step per graph.  The trace launches eagerly from the host each
+# step (one library call per chain for all layers): 2 chains give +5 % device time and
+# +3 % wall time on the continuous BF16 trace (+18 % / +15 % static), 4 chains lose; FP8
+# pages gain 3 % of device time and lose 1 % of wall time, so they keep one
+CHAINS = {"tiny": 2, "b256": 2, "b64": 8, "b8": 1, "trace": 2}
 CHAINS_FP8 = {"tiny": 2, "b256": 2, "b64": 8, "b8": 1, "trace": 1}
 # the two named calls per layer (pkv_append_rope, then pkv_decode_attention): twice the
 # launches, whose latencies more chains hide (b64: 16 chains 0.205 ms per step, 8 chains 0.215)
