@@ -363,17 +363,24 @@ struct MmaWarp {
         const int gid = lane >> 2, tig = lane & 3;
         const uint32_t kbase = smem_addr(st);
         const uint32_t vbase = kbase + kTileBytes;
-        // ---- S^T[16 tokens][8 heads] = K . Q^T
+        // ---- S^T[16 tokens][8 heads] = K . Q^T, the even and the odd k-steps in two
+        // accumulators (two MMA chains of two instead of one of four), added at the end
         float s[4] = {0.f, 0.f, 0.f, 0.f};
         {
             const int mi = lane >> 3, r = lane & 7;
             const int tok = r + ((mi & 1) ? 8 : 0);
+            float s1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-                uint32_t a[4];
-                ldsm_x4(kbase + swz(tok, 2 * ks + (mi >> 1)), a);
-                mma_bf16(s, a, qb[ks][0], qb[ks][1]);
+            for (int ks = 0; ks < 4; ks += 2) {
+                uint32_t a0[4], a1[4];
+                ldsm_x4(kbase + swz(tok, 2 * ks + (mi >> 1)), a0);
+                ldsm_x4(kbase + swz(tok, 2 * (ks + 1) + (mi >> 1)), a1);
+                mma_bf16(s, a0, qb[ks][0], qb[ks][1]);
+                mma_bf16(s1, a1, qb[ks + 1][0], qb[ks + 1][1]);
             }
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                s[i] += s1[i];
         }
         // s[0], s[1]: token gid, heads 2tig, 2tig+1; s[2], s[3]: token gid+8
         float x[4];
