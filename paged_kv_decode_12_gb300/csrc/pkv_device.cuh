@@ -80,6 +80,22 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, u
     return false;
 }
 
+// Hardware approximations (PTX ex2.approx.ftz / rcp.approx.ftz): the softmax weights and
+// the FP8 V-scale ratios tolerate their ~2 ulp error; ex2(-inf) = 0.
+__device__ __forceinline__ float ex2_approx(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float rcp_approx(float x)
+{
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ uint64_t l2_evict_first_policy()
 {
     uint64_t p;
@@ -398,9 +414,9 @@ struct MmaWarp {
             pm1 = fmaxf(pm1, __shfl_xor_sync(kFull, pm1, off));
         }
         const float mn0 = fmaxf(m[0], pm0), mn1 = fmaxf(m[1], pm1);
-        const float al0 = exp2f(m[0] - mn0), al1 = exp2f(m[1] - mn1);
-        const float p0 = exp2f(x[0] - mn0), p1 = exp2f(x[1] - mn1);
-        const float p2 = exp2f(x[2] - mn0), p3 = exp2f(x[3] - mn1);
+        const float al0 = ex2_approx(m[0] - mn0), al1 = ex2_approx(m[1] - mn1);
+        const float p0 = ex2_approx(x[0] - mn0), p1 = ex2_approx(x[1] - mn1);
+        const float p2 = ex2_approx(x[2] - mn0), p3 = ex2_approx(x[3] - mn1);
         l[0] = fmaf(l[0], al0, p0 + p2);
         l[1] = fmaf(l[1], al1, p1 + p3);
         m[0] = mn0;

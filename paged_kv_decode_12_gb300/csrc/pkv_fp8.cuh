@@ -83,21 +83,6 @@ __device__ __forceinline__ void e4m3x4_to_f16x2(uint32_t w, uint32_t &lo, uint32
         : "r"(w));
 }
 
-// Hardware approximations (PTX ex2.approx.ftz / rcp.approx.ftz): the softmax weights
-// and the V-scale ratios tolerate their ~2 ulp error; ex2(-inf) = 0.
-__device__ __forceinline__ float ex2_approx(float x)
-{
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
-__device__ __forceinline__ float rcp_approx(float x)
-{
-    float y;
-    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
 
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
 {
