@@ -353,14 +353,17 @@ class DecodeEngine:
                 self.step(d["q"], d["k_new"], d["v_new"], d["pos"], d["seq_lens"], out_devs[s % K], cur)
                 done[s].record(cur)
             elif first:
-                for t in range(s, s + group):
-                    cur.wait_event(ready[t])
-                    if t >= K:
-                        cur.wait_event(sent[t - K])
+                # the copy streams run their copies in order: the group's last upload and the
+                # send out of the last buffer it reuses imply all the others
+                last = s + group - 1
+                cur.wait_event(ready[last])
+                if last >= K:
+                    cur.wait_event(sent[last - K])
                 with torch.cuda.stream(cur):
                     graphs[(s % K) // group].replay()
-                for t in range(s, s + group):
-                    done[t].record(cur)
+                done[s].record(cur)
+                for t in range(s + 1, s + group):
+                    done[t] = done[s]
             self._d2h.wait_event(done[s])
             with torch.cuda.stream(self._d2h):
                 out_host.copy_(out_devs[s % K], non_blocking=True)
