@@ -813,7 +813,9 @@ def main(argv=None):
     ap.add_argument("--seed", type=int, default=12)
     ap.add_argument("--layers", type=int, default=None, help="override the layer count (small profiling runs)")
     ap.add_argument("--steps-per-graph", type=int, default=25)
-    ap.add_argument("--e2e-steps", type=int, default=100)
+    ap.add_argument("--e2e-steps", type=int, default=400,
+                    help="end-to-end steps timed (the first group's uploads and the last group's copies back "
+                         "are not overlapped: more steps measure the steady state)")
     ap.add_argument("--e2e-buffers", type=int, default=2, help="end-to-end input/output buffers in rotation "
                     "(at least twice --e2e-group)")
     ap.add_argument("--e2e-group", type=int, default=8, help="end-to-end steps per captured graph replay")
